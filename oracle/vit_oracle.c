@@ -1,0 +1,251 @@
+/*
+ * vit_oracle.c -- plain float64 CPU oracle of one pre-LayerNorm ViT encoder block.
+ *
+ * TEST INFRASTRUCTURE. Only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark may load this code. The product path (the CUDA library) never calls
+ * it, shares no code with it, and fails loudly when its own extension is missing.
+ *
+ * Everything here is the plain definition written out in float64, in the order the
+ * pages state it; there is no blocking, fusion or reordering:
+ *
+ *   "ViT Encoder Block" (crackedaicode), sections "Inputs and output",
+ *   "Normalize before each stage", "Multi-head attention", "Feed-forward stage":
+ *     xn  = LN(x)                         population variance, eps a parameter
+ *     Q,K,V = xn @ w_q, xn @ w_k, xn @ w_v  weights stored (in, out)
+ *     per sequence n and head h (columns [h*dh, (h+1)*dh), dh = D/H):
+ *       s   = Q_h K_h^T / sqrt(dh);  p = stable softmax over all T keys (no mask)
+ *       o_h = p V_h
+ *     y   = x + concat_h(o_h) @ w_o
+ *     out = y + GELU_tanh(LN(y) @ w_mlp1) @ w_mlp2
+ *
+ *   "ViT Encoder Block" (ai-engineer-exhaustive), Key Equations, Steps 1, 4 and 5:
+ *     optional LN gain/bias (gamma, beta), one pair per LN, and MLP biases b1, b2.
+ *     A NULL pointer means "absent": gain 1, bias 0.
+ *
+ * Every array is C-contiguous float64. Nothing is allocated on the caller's behalf
+ * except per-thread scratch, which is freed before return.
+ *
+ * Pins: tests/test_oracle_pins.py checks every function below against the pages'
+ * worked examples, closed forms, invariants and float64 library routines.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* LayerNorm over the last axis of a (rows, D) array.
+ * "ViT Encoder Block" (crackedaicode), "Normalize before each stage":
+ *   LN(x) = (x - mean) / sqrt(variance + eps), variance divides by D.
+ * Gain/bias: "ViT Encoder Block" (ai-engineer-exhaustive), Key Equations, Step 1. */
+void oracle_layernorm(const double* x, int64_t rows, int64_t D, double eps,
+                      const double* gamma, const double* beta, double* out)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * D;
+        double* o = out + r * D;
+        double mean = 0.0;
+        for (int64_t j = 0; j < D; ++j) mean += xr[j];
+        mean /= (double)D;
+        double var = 0.0;
+        for (int64_t j = 0; j < D; ++j) {
+            double d = xr[j] - mean;
+            var += d * d;
+        }
+        var /= (double)D;
+        double denom = sqrt(var + eps);
+        for (int64_t j = 0; j < D; ++j) {
+            double v = (xr[j] - mean) / denom;
+            if (gamma) v = gamma[j] * v;
+            if (beta) v = v + beta[j];
+            o[j] = v;
+        }
+    }
+}
+
+/* tanh-approximation GELU.
+ * "ViT Encoder Block" (crackedaicode), "Feed-forward stage":
+ *   GELU(z) = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). */
+double oracle_gelu_tanh(double z)
+{
+    const double pi = 3.14159265358979323846;
+    return 0.5 * z * (1.0 + tanh(sqrt(2.0 / pi) * (z + 0.044715 * z * z * z)));
+}
+
+void oracle_gelu_tanh_array(const double* z, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_gelu_tanh(z[i]);
+}
+
+/* C (M, N) = A (M, K) @ W (K, N) [+ bias (N)].
+ * Each C[m][n] is the sum over k = 0..K-1, in ascending k, of A[m][k] * W[k][n];
+ * the bias, when present, is added after the sum. */
+void oracle_matmul(const double* A, const double* W, const double* bias,
+                   int64_t M, int64_t K, int64_t N, double* C)
+{
+    for (int64_t m = 0; m < M; ++m) {
+        double* c = C + m * N;
+        for (int64_t n = 0; n < N; ++n) c[n] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double a = A[m * K + k];
+            const double* w = W + k * N;
+            for (int64_t n = 0; n < N; ++n) c[n] += a * w[n];
+        }
+        if (bias)
+            for (int64_t n = 0; n < N; ++n) c[n] += bias[n];
+    }
+}
+
+/* Stable softmax of each row of a (rows, n) array: subtract the row maximum,
+ * exponentiate, divide by the sum. "ViT Encoder Block" (crackedaicode),
+ * "Multi-head attention" ("Use stable softmax across key positions"). */
+void oracle_softmax_rows(const double* s, int64_t rows, int64_t n, double* p)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* sr = s + r * n;
+        double* pr = p + r * n;
+        double m = sr[0];
+        for (int64_t u = 1; u < n; ++u)
+            if (sr[u] > m) m = sr[u];
+        double z = 0.0;
+        for (int64_t u = 0; u < n; ++u) {
+            pr[u] = exp(sr[u] - m);
+            z += pr[u];
+        }
+        for (int64_t u = 0; u < n; ++u) pr[u] = pr[u] / z;
+    }
+}
+
+/* Multi-head attention of ONE sequence, no mask.
+ * Q, K, V, O are (T, D); head h owns columns [h*dh, (h+1)*dh), dh = D/H.
+ * scratch must hold 2*T doubles.
+ * "ViT Encoder Block" (crackedaicode), "Multi-head attention":
+ *   scores = Q_h K_h^T / sqrt(D/H); weights = softmax(scores, axis=-1);
+ *   head_output = weights V_h; heads concatenated in their original order. */
+static void attention_one_sequence(const double* Q, const double* K, const double* V,
+                                   int64_t T, int64_t D, int64_t H, double* O,
+                                   double* scratch)
+{
+    const int64_t dh = D / H;
+    const double scale = sqrt((double)dh);
+    double* s = scratch;
+    double* p = scratch + T;
+    for (int64_t h = 0; h < H; ++h) {
+        const int64_t c0 = h * dh;
+        for (int64_t t = 0; t < T; ++t) {
+            for (int64_t u = 0; u < T; ++u) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < dh; ++c)
+                    dot += Q[t * D + c0 + c] * K[u * D + c0 + c];
+                s[u] = dot / scale;
+            }
+            oracle_softmax_rows(s, 1, T, p);
+            for (int64_t c = 0; c < dh; ++c) {
+                double acc = 0.0;
+                for (int64_t u = 0; u < T; ++u) acc += p[u] * V[u * D + c0 + c];
+                O[t * D + c0 + c] = acc;
+            }
+        }
+    }
+}
+
+/* Attention over N sequences laid out (N, T, D). */
+void oracle_attention(const double* Q, const double* K, const double* V,
+                      int64_t N, int64_t T, int64_t D, int64_t H, double* O)
+{
+    double* scratch = (double*)malloc(sizeof(double) * 2 * (size_t)T);
+    for (int64_t n = 0; n < N; ++n)
+        attention_one_sequence(Q + n * T * D, K + n * T * D, V + n * T * D, T, D, H,
+                               O + n * T * D, scratch);
+    free(scratch);
+}
+
+/* The whole block over N independent sequences (x is (N, T, D)).
+ *
+ * Optional stage outputs (each NULL or the stated shape) expose the intermediate
+ * values for stage-by-stage comparison:
+ *   xn (N,T,D), qkv (N,T,3D) laid out [Q | K | V], o (N,T,D) heads concatenated,
+ *   y (N,T,D), yn (N,T,D), g (N,T,F) = GELU output.
+ *
+ * Returns 0 on success, -1 on invalid sizes (non-positive, or H not dividing D),
+ * -2 if scratch allocation fails. nthreads <= 0 uses the OpenMP default. */
+int oracle_vit_block(const double* x, const double* w_q, const double* w_k,
+                     const double* w_v, const double* w_o, const double* w_mlp1,
+                     const double* w_mlp2, const double* ln1_g, const double* ln1_b,
+                     const double* ln2_g, const double* ln2_b, const double* b1,
+                     const double* b2, int64_t N, int64_t T, int64_t D, int64_t F,
+                     int64_t H, double eps, double* out, double* st_xn, double* st_qkv,
+                     double* st_o, double* st_y, double* st_yn, double* st_g,
+                     int nthreads)
+{
+    if (N <= 0 || T <= 0 || D <= 0 || F <= 0 || H <= 0 || D % H != 0) return -1;
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        const size_t TD = (size_t)(T * D), TF = (size_t)(T * F);
+        double* buf = (double*)malloc(sizeof(double) * (8 * TD + 2 * TF + 2 * (size_t)T));
+        if (!buf) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            continue;
+        }
+        double *xn = buf, *q = xn + TD, *k = q + TD, *v = k + TD, *o = v + TD;
+        double *a = o + TD, *y = a + TD, *yn = y + TD, *z = yn + TD, *g = z + TF;
+        double* scratch = g + TF;
+        const double* xs = x + (size_t)n * TD;
+        double* os = out + (size_t)n * TD;
+
+        /* 1. xn = LN1(x) */
+        oracle_layernorm(xs, T, D, eps, ln1_g, ln1_b, xn);
+        /* 2. Q, K, V = xn @ w_q, xn @ w_k, xn @ w_v (no projection biases) */
+        oracle_matmul(xn, w_q, NULL, T, D, D, q);
+        oracle_matmul(xn, w_k, NULL, T, D, D, k);
+        oracle_matmul(xn, w_v, NULL, T, D, D, v);
+        /* 3. per-head unmasked attention, heads concatenated in order */
+        attention_one_sequence(q, k, v, T, D, H, o, scratch);
+        /* 4. y = x + o @ w_o  (the residual adds to the un-normalised x) */
+        oracle_matmul(o, w_o, NULL, T, D, D, a);
+        for (size_t i = 0; i < TD; ++i) y[i] = xs[i] + a[i];
+        /* 5. yn = LN2(y)  (LN of y, not of x) */
+        oracle_layernorm(y, T, D, eps, ln2_g, ln2_b, yn);
+        /* 6. g = GELU_tanh(yn @ w_mlp1 [+ b1]) */
+        oracle_matmul(yn, w_mlp1, b1, T, D, F, z);
+        oracle_gelu_tanh_array(z, (int64_t)TF, g);
+        /* 7. out = y + g @ w_mlp2 [+ b2] */
+        oracle_matmul(g, w_mlp2, b2, T, F, D, a);
+        for (size_t i = 0; i < TD; ++i) os[i] = y[i] + a[i];
+
+        if (st_xn) memcpy(st_xn + (size_t)n * TD, xn, sizeof(double) * TD);
+        if (st_qkv) {
+            double* dst = st_qkv + (size_t)n * 3 * TD;
+            for (int64_t t = 0; t < T; ++t) {
+                memcpy(dst + (size_t)t * 3 * D, q + (size_t)t * D, sizeof(double) * D);
+                memcpy(dst + (size_t)t * 3 * D + D, k + (size_t)t * D, sizeof(double) * D);
+                memcpy(dst + (size_t)t * 3 * D + 2 * D, v + (size_t)t * D, sizeof(double) * D);
+            }
+        }
+        if (st_o) memcpy(st_o + (size_t)n * TD, o, sizeof(double) * TD);
+        if (st_y) memcpy(st_y + (size_t)n * TD, y, sizeof(double) * TD);
+        if (st_yn) memcpy(st_yn + (size_t)n * TD, yn, sizeof(double) * TD);
+        if (st_g) memcpy(st_g + (size_t)n * TF, g, sizeof(double) * TF);
+        free(buf);
+    }
+    return failed ? -2 : 0;
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

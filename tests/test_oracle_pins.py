@@ -1,0 +1,390 @@
+"""Pins of the float64 oracle to facts that do not come from the oracle itself.
+
+Each test checks the oracle against one of: a value the pages print for a worked
+example (fixtures under tests/golden/, each with its citation), a closed form, an
+invariant the pages state, or a float64 library routine that computes the same
+mathematical function. Together they are chosen so that a plausible slip anywhere in
+the oracle (wrong eps, sample instead of population variance, a dropped residual,
+a transposed weight, a wrong head offset or score scale, a masked key, the erf GELU
+instead of the tanh one) fails at least one of them; test_pins_reject_mutants shows
+that for each such slip.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as Fn
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand_block(N, T, D, F, seed, affine=False):
+    rng = np.random.default_rng(seed)
+    a = dict(
+        x=rng.standard_normal((N, T, D)),
+        w_q=rng.standard_normal((D, D)) / np.sqrt(D),
+        w_k=rng.standard_normal((D, D)) / np.sqrt(D),
+        w_v=rng.standard_normal((D, D)) / np.sqrt(D),
+        w_o=rng.standard_normal((D, D)) / np.sqrt(D),
+        w_mlp1=rng.standard_normal((D, F)) / np.sqrt(D),
+        w_mlp2=rng.standard_normal((F, D)) / np.sqrt(F),
+    )
+    if affine:
+        a.update(ln1_g=1 + 0.1 * rng.standard_normal(D), ln1_b=0.1 * rng.standard_normal(D),
+                 ln2_g=1 + 0.1 * rng.standard_normal(D), ln2_b=0.1 * rng.standard_normal(D),
+                 b1=0.1 * rng.standard_normal(F), b2=0.1 * rng.standard_normal(D))
+    return a
+
+
+def _call(a, H, eps, **kw):
+    return oracle.vit_block(a["x"], a["w_q"], a["w_k"], a["w_v"], a["w_o"], a["w_mlp1"],
+                            a["w_mlp2"], H, eps, ln1_g=a.get("ln1_g"), ln1_b=a.get("ln1_b"),
+                            ln2_g=a.get("ln2_g"), ln2_b=a.get("ln2_b"), b1=a.get("b1"),
+                            b2=a.get("b2"), **kw)
+
+
+def _p2_args(ex):
+    return dict(x=np.array(ex["x"], float), w_q=np.array(ex["Wq"], float),
+                w_k=np.array(ex["Wk"], float), w_v=np.array(ex["Wv"], float),
+                w_o=np.array(ex["Wo"], float), w_mlp1=np.array(ex["W1"], float),
+                w_mlp2=np.array(ex["W2"], float))
+
+
+# ---------------------------------------------------------------------------------
+# Whole block: the three worked examples printed to 6 d.p.
+# ---------------------------------------------------------------------------------
+@pytest.mark.parametrize("i", [0, 1, 2])
+def test_p2_worked_examples(i):
+    g = _load("p2_worked_examples.json")
+    ex = g["examples"][i]
+    out = _call(_p2_args(ex), ex["num_heads"], g["eps"])
+    np.testing.assert_allclose(out, np.array(ex["output"]), rtol=0, atol=g["print_tolerance"])
+
+
+def test_p2_example2_constant_row_is_exact():
+    # token [1, 1] has zero variance: LN gives exactly 0, so both stage outputs are 0
+    # for that row and it leaves the block unchanged.
+    g = _load("p2_worked_examples.json")
+    ex = g["examples"][1]
+    out = _call(_p2_args(ex), ex["num_heads"], g["eps"])
+    assert out[0, 2, 0] == 1.0 and out[0, 2, 1] == 1.0
+
+
+def test_p2_examples_discriminate_eps_gelu_orientation():
+    """The examples only fit eps = 1e-6, x @ W and the tanh GELU: other readings miss."""
+    g = _load("p2_worked_examples.json")
+    worst_eps = 0.0
+    for ex in g["examples"]:
+        out = _call(_p2_args(ex), ex["num_heads"], 1e-5)
+        worst_eps = max(worst_eps, np.abs(out - np.array(ex["output"])).max())
+    assert worst_eps > 1e-4
+    ex = g["examples"][2]
+    a = _p2_args(ex)
+    at = {k: (v.T.copy() if k != "x" else v) for k, v in a.items()}
+    out = _call(at, ex["num_heads"], g["eps"])
+    assert np.abs(out - np.array(ex["output"])).max() > 0.1
+
+
+# ---------------------------------------------------------------------------------
+# Sub-steps: the partially worked numerical example (4 d.p.)
+# ---------------------------------------------------------------------------------
+def test_p4_layernorm_rows():
+    f = _load("p4_numerical_example.json")["layernorm"]
+    x = np.array(f["x"])
+    np.testing.assert_allclose(x.mean(axis=1), f["mean"], atol=1e-15)
+    np.testing.assert_allclose(((x - x.mean(1, keepdims=True)) ** 2).mean(1), f["variance"],
+                               atol=1e-15)
+    out = oracle.layernorm(x, f["eps"])
+    np.testing.assert_allclose(out, np.array(f["normalized"]), atol=f["tolerance"])
+
+
+def test_p4_softmax_rows():
+    f = _load("p4_numerical_example.json")["softmax"]
+    p = oracle.softmax_rows(np.array(f["scaled_scores"]))
+    for r in range(2):
+        np.testing.assert_allclose(p[r], f["weights"][r], atol=f["tolerance_row"][r])
+
+
+def test_p4_residual_adds_unnormalised_input():
+    """y = x + MSA(LN(x)): choose w_o so that the block's MSA output equals the page's
+    'suppose' values, then the block's y must equal the page's x' (printed exactly)."""
+    f = _load("p4_numerical_example.json")["residual"]
+    rng = np.random.default_rng(3)
+    x = np.array(f["x"])[None]
+    D = 4
+    a = dict(x=x, w_q=rng.standard_normal((D, D)), w_k=rng.standard_normal((D, D)),
+             w_v=rng.standard_normal((D, D)), w_o=np.eye(D), w_mlp1=np.eye(D, 8),
+             w_mlp2=np.eye(8, D))
+    _, st = _call(a, 2, 1e-5, stages=True)
+    o = st["o"][0]                                   # (2, 4), rank 2
+    a["w_o"] = np.linalg.pinv(o) @ np.array(f["msa_output"])
+    _, st = _call(a, 2, 1e-5, stages=True)
+    np.testing.assert_allclose(st["y"][0], np.array(f["x_prime"]), atol=1e-12)
+
+
+def test_p4_gelu_half():
+    f = _load("p4_numerical_example.json")["gelu"]
+    assert abs(oracle.gelu_tanh(np.array([f["z"]]))[0] - f["value"]) <= f["tolerance"]
+
+
+# ---------------------------------------------------------------------------------
+# Library special cases and closed forms
+# ---------------------------------------------------------------------------------
+def test_gelu_matches_torch_tanh_gelu():
+    z = np.linspace(-8, 8, 2001)
+    ref = Fn.gelu(torch.from_numpy(z), approximate="tanh").numpy()
+    np.testing.assert_allclose(oracle.gelu_tanh(z), ref, rtol=0, atol=1e-15)
+    erf = Fn.gelu(torch.from_numpy(z)).numpy()
+    assert np.abs(oracle.gelu_tanh(z) - erf).max() > 1e-4   # not the erf form
+
+
+def test_gelu_limits():
+    g = oracle.gelu_tanh(np.array([0.0, 20.0, -20.0]))
+    assert g[0] == 0.0 and g[1] == 20.0 and abs(g[2]) < 1e-300 + 1e-12
+
+
+def test_layernorm_d2_closed_form():
+    """D = 2: LN([a, b]) = (+-1) * |a-b|/2 / sqrt((a-b)^2/4 + eps), signs (sgn(a-b), sgn(b-a))."""
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((50, 2)) * 3
+    eps = 1e-5
+    h = (x[:, 0] - x[:, 1]) / 2
+    mag = np.abs(h) / np.sqrt(h * h + eps)
+    exp = np.stack([np.sign(h) * mag, -np.sign(h) * mag], axis=1)
+    np.testing.assert_allclose(oracle.layernorm(x, eps), exp, atol=1e-14)
+
+
+def test_layernorm_matches_torch_and_affine():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((37, 24)) * 2 + 0.5
+    g, b = rng.standard_normal(24), rng.standard_normal(24)
+    for eps in (1e-5, 1e-6):
+        ref = Fn.layer_norm(torch.from_numpy(x), (24,), torch.from_numpy(g), torch.from_numpy(b),
+                            eps=eps).numpy()
+        np.testing.assert_allclose(oracle.layernorm(x, eps, g, b), ref, atol=1e-13)
+
+
+def test_softmax_rows_sum_to_one_and_are_shift_invariant():
+    rng = np.random.default_rng(2)
+    s = rng.standard_normal((20, 197)) * 10
+    p = oracle.softmax_rows(s)
+    np.testing.assert_allclose(p.sum(1), 1.0, atol=1e-14)
+    assert (p > 0).all()
+    np.testing.assert_allclose(oracle.softmax_rows(s + 1000.0), p, atol=1e-14)
+    np.testing.assert_allclose(p, torch.softmax(torch.from_numpy(s), -1).numpy(), atol=1e-15)
+
+
+def test_matmul_matches_numpy():
+    rng = np.random.default_rng(4)
+    a, w, b = rng.standard_normal((7, 13)), rng.standard_normal((13, 5)), rng.standard_normal(5)
+    np.testing.assert_allclose(oracle.matmul(a, w), a @ w, atol=1e-13)
+    np.testing.assert_allclose(oracle.matmul(a, w, b), a @ w + b, atol=1e-13)
+
+
+def _torch_block(a, H, eps):
+    """The block written with float64 PyTorch library routines (layer_norm,
+    scaled_dot_product_attention, tanh GELU) -- an independent composition."""
+    t = {k: torch.from_numpy(np.asarray(v, dtype=np.float64)) for k, v in a.items()}
+    x = t["x"]
+    N, T, D = x.shape
+    dh = D // H
+    xn = Fn.layer_norm(x, (D,), t.get("ln1_g"), t.get("ln1_b"), eps=eps)
+
+    def heads(m):
+        return m.reshape(N, T, H, dh).transpose(1, 2)
+    q, k, v = heads(xn @ t["w_q"]), heads(xn @ t["w_k"]), heads(xn @ t["w_v"])
+    o = Fn.scaled_dot_product_attention(q, k, v).transpose(1, 2).reshape(N, T, D)
+    y = x + o @ t["w_o"]
+    yn = Fn.layer_norm(y, (D,), t.get("ln2_g"), t.get("ln2_b"), eps=eps)
+    z = yn @ t["w_mlp1"]
+    if "b1" in t:
+        z = z + t["b1"]
+    m = Fn.gelu(z, approximate="tanh") @ t["w_mlp2"]
+    if "b2" in t:
+        m = m + t["b2"]
+    return (y + m).numpy()
+
+
+@pytest.mark.parametrize("shape", [(2, 7, 12, 20, 3), (1, 1, 8, 32, 2), (3, 5, 6, 6, 6),
+                                   (2, 33, 16, 64, 1), (1, 13, 20, 40, 4),
+                                   (2, 197, 192, 768, 3), (1, 65, 160, 320, 2)])
+@pytest.mark.parametrize("affine", [False, True])
+def test_block_matches_torch_library_composition(shape, affine):
+    N, T, D, F, H = shape
+    a = _rand_block(N, T, D, F, seed=hash(shape) % 1000, affine=affine)
+    np.testing.assert_allclose(_call(a, H, 1e-5), _torch_block(a, H, 1e-5), rtol=0, atol=1e-11)
+
+
+def test_stages_match_torch_steps():
+    a = _rand_block(2, 9, 12, 24, seed=5)
+    out, st = _call(a, 3, 1e-6, stages=True)
+    x = torch.from_numpy(a["x"])
+    xn = Fn.layer_norm(x, (12,), eps=1e-6).numpy()
+    np.testing.assert_allclose(st["xn"], xn, atol=1e-13)
+    qkv = np.concatenate([xn @ a["w_q"], xn @ a["w_k"], xn @ a["w_v"]], axis=-1)
+    np.testing.assert_allclose(st["qkv"], qkv, atol=1e-13)
+    np.testing.assert_allclose(st["y"], a["x"] + st["o"] @ a["w_o"], atol=1e-13)
+    np.testing.assert_allclose(out, st["y"] + st["g"] @ a["w_mlp2"], atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------
+# Invariants stated on the pages
+# ---------------------------------------------------------------------------------
+def test_zero_stage_outputs_return_x_exactly():
+    # "If both stage outputs are zero, the residual paths return x unchanged."
+    a = _rand_block(2, 6, 8, 16, seed=6, affine=True)
+    a["w_o"] = np.zeros_like(a["w_o"])
+    a["w_mlp2"] = np.zeros_like(a["w_mlp2"])
+    del a["b2"]
+    out, st = _call(a, 2, 1e-5, stages=True)
+    assert np.array_equal(st["y"], a["x"])
+    assert np.array_equal(out, a["x"])
+
+
+def test_permutation_equivariance():
+    # "E2E: Tiny Vision Transformer", "Why position embeddings matter".
+    a = _rand_block(1, 11, 12, 24, seed=7)
+    perm = np.random.default_rng(8).permutation(11)
+    out = _call(a, 3, 1e-5)
+    b = dict(a, x=a["x"][:, perm])
+    np.testing.assert_allclose(_call(b, 3, 1e-5), out[:, perm], atol=1e-13)
+
+
+def test_heads_read_only_their_slice():
+    a = _rand_block(1, 8, 12, 16, seed=9)
+    H, dh, h = 3, 4, 1
+    _, st0 = _call(a, H, 1e-5, stages=True)
+    # (a constant offset would vanish: LN output rows sum to zero)
+    rng = np.random.default_rng(15)
+    b = dict(a)
+    b["w_q"] = a["w_q"].copy()
+    b["w_q"][:, h * dh:(h + 1) * dh] += rng.standard_normal((12, dh))
+    b["w_k"] = a["w_k"].copy()
+    b["w_k"][:, h * dh:(h + 1) * dh] -= rng.standard_normal((12, dh))
+    _, st1 = _call(b, H, 1e-5, stages=True)
+    keep = np.ones(12, bool)
+    keep[h * dh:(h + 1) * dh] = False
+    assert np.array_equal(st0["o"][..., keep], st1["o"][..., keep])
+    assert np.abs(st0["o"][..., ~keep] - st1["o"][..., ~keep]).max() > 1e-3
+
+
+def test_sequences_are_independent():
+    a = _rand_block(3, 6, 8, 16, seed=10)
+    out = _call(a, 2, 1e-5)
+    b = dict(a, x=a["x"].copy())
+    b["x"][1] += np.random.default_rng(17).standard_normal((6, 8))
+    out2 = _call(b, 2, 1e-5)
+    assert np.array_equal(out[0], out2[0]) and np.array_equal(out[2], out2[2])
+    single = _call(dict(a, x=a["x"][2:3]), 2, 1e-5)
+    assert np.array_equal(single[0], out[2])
+
+
+def test_no_causal_mask():
+    # "ViT Encoder Block" (ai-engineer-exhaustive), "No Causal Mask" and "Pitfalls":
+    # the first token must see a change to the last one.
+    a = _rand_block(1, 6, 8, 16, seed=11)
+    out = _call(a, 2, 1e-5)
+    b = dict(a, x=a["x"].copy())
+    b["x"][0, -1] += np.random.default_rng(16).standard_normal(8)   # not a constant: LN removes those
+    assert np.abs(_call(b, 2, 1e-5)[0, 0] - out[0, 0]).max() > 1e-4
+
+
+def test_single_token_attention_is_value_row():
+    # T = 1: the only softmax weight is exactly 1, so Q and K cannot matter.
+    a = _rand_block(2, 1, 8, 16, seed=12)
+    out = _call(a, 2, 1e-5)
+    b = dict(a, w_q=a["w_q"] * 3 + 1, w_k=-a["w_k"])
+    assert np.array_equal(_call(b, 2, 1e-5), out)
+    _, st = _call(a, 2, 1e-5, stages=True)
+    np.testing.assert_allclose(st["o"], st["qkv"][..., 16:], atol=0)
+
+
+def test_zero_queries_give_uniform_weights():
+    # w_q = 0: every score is 0, weights are 1/T, the head output is the mean of V.
+    a = _rand_block(1, 7, 8, 16, seed=13)
+    a["w_q"] = np.zeros_like(a["w_q"])
+    _, st = _call(a, 2, 1e-5, stages=True)
+    v = st["qkv"][..., 16:]
+    np.testing.assert_allclose(st["o"][0], np.broadcast_to(v[0].mean(0), (7, 8)), atol=1e-15)
+    b = dict(a, w_k=a["w_k"] * 5)
+    _, st2 = _call(b, 2, 1e-5, stages=True)
+    assert np.array_equal(st["o"], st2["o"])
+
+
+def test_invalid_sizes_rejected():
+    a = _rand_block(1, 3, 6, 8, seed=14)
+    with pytest.raises(ValueError):
+        _call(a, 4, 1e-5)      # 4 does not divide 6
+
+
+# ---------------------------------------------------------------------------------
+# The pins above catch plausible slips: each mutant is a copy of the oracle source
+# with one mistake planted (compiled on the CPU into a temporary library).
+# ---------------------------------------------------------------------------------
+MUTANTS = {
+    "eps_fixed_1e-5": ("sqrt(var + eps)", "sqrt(var + 1e-5)"),
+    "sample_variance": ("var /= (double)D;", "var /= (double)(D - 1 > 0 ? D - 1 : 1);"),
+    "drop_residual_1": ("y[i] = xs[i] + a[i];", "y[i] = a[i];"),
+    "residual_1_on_normalised": ("y[i] = xs[i] + a[i];", "y[i] = xn[i] + a[i];"),
+    "drop_residual_2": ("os[i] = y[i] + a[i];", "os[i] = a[i];"),
+    "residual_2_on_x": ("os[i] = y[i] + a[i];", "os[i] = xs[i] + a[i];"),
+    "ln2_of_x": ("oracle_layernorm(y, T, D, eps, ln2_g, ln2_b, yn);",
+                 "oracle_layernorm(xs, T, D, eps, ln2_g, ln2_b, yn);"),
+    "shared_ln_params": ("oracle_layernorm(y, T, D, eps, ln2_g, ln2_b, yn);",
+                         "oracle_layernorm(y, T, D, eps, ln1_g, ln1_b, yn);"),
+    "weight_transposed": ("const double* w = W + k * N;\n            for (int64_t n = 0; n < N; ++n) c[n] += a * w[n];",
+                          "for (int64_t n = 0; n < N; ++n) c[n] += a * W[n * K + k];"),
+    "head_offset_zero": ("const int64_t c0 = h * dh;", "const int64_t c0 = 0 * h;"),
+    "score_scale_sqrt_D": ("const double scale = sqrt((double)dh);", "const double scale = sqrt((double)D);"),
+    "score_scale_missing": ("s[u] = dot / scale;", "s[u] = dot + 0.0 * scale;"),
+    "causal_mask": ("s[u] = dot / scale;", "s[u] = (u > t) ? -INFINITY : dot / scale;"),
+    "gelu_erf": ("return 0.5 * z * (1.0 + tanh(sqrt(2.0 / pi) * (z + 0.044715 * z * z * z)));",
+                 "return 0.5 * z * (1.0 + erf(z / sqrt(2.0))) + 0.0 * pi;"),
+    "gelu_constant": ("0.044715 * z * z * z", "0.04471 * z * z * z"),
+    "gelu_square": ("0.044715 * z * z * z", "0.044715 * z * z"),
+    "drop_b1": ("oracle_matmul(yn, w_mlp1, b1, T, D, F, z);", "oracle_matmul(yn, w_mlp1, NULL, T, D, F, z);"),
+    "wk_for_wv": ("oracle_matmul(xn, w_v, NULL, T, D, D, v);", "oracle_matmul(xn, w_k, NULL, T, D, D, v);"),
+}
+
+
+def _pins_pass(lib):
+    """Run the whole-block pins (worked examples + library composition) on a library."""
+    g = _load("p2_worked_examples.json")
+    for ex in g["examples"]:
+        out = _call(_p2_args(ex), ex["num_heads"], g["eps"], lib=lib)
+        if not np.allclose(out, np.array(ex["output"]), rtol=0, atol=g["print_tolerance"]):
+            return False
+    for shape, affine in (((2, 7, 12, 20, 3), False), ((2, 7, 12, 20, 3), True)):
+        N, T, D, F, H = shape
+        a = _rand_block(N, T, D, F, seed=21, affine=affine)
+        if not np.allclose(_call(a, H, 1e-5, lib=lib), _torch_block(a, H, 1e-5), rtol=0, atol=1e-11):
+            return False
+    return True
+
+
+def test_pins_pass_on_unmodified_source(tmp_path):
+    src = open(oracle._SRC).read()
+    p = tmp_path / "clean.c"
+    p.write_text(src)
+    lib = oracle.open_library(oracle.build(force=True, src=str(p), out=str(tmp_path / "clean.so")))
+    assert _pins_pass(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutants(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(oracle._SRC).read()
+    assert src.count(old) == 1, name
+    p = tmp_path / ("m_%s.c" % name)
+    p.write_text(src.replace(old, new))
+    lib = oracle.open_library(oracle.build(force=True, src=str(p), out=str(tmp_path / ("m_%s.so" % name))))
+    assert not _pins_pass(lib), "planted slip %r was not caught" % name
