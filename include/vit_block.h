@@ -1,0 +1,199 @@
+/*
+ * vit_block.h -- C ABI of the GB300 (sm_103a) ViT encoder block library.
+ *
+ * The library computes the forward pass of one pre-LayerNorm Vision Transformer
+ * encoder block on one GPU, with hand-written CUDA kernels:
+ *
+ *   xn  = LN1(x)                                  per token, over its D features
+ *   Q,K,V = xn @ w_q, xn @ w_k, xn @ w_v          weights stored (in, out)
+ *   o   = concat_h softmax(Q_h K_h^T / sqrt(D/H)) V_h     no mask, H heads of D/H
+ *   y   = x + o @ w_o
+ *   out = y + GELU_tanh(LN2(y) @ w_mlp1 [+ b1]) @ w_mlp2 [+ b2]
+ *
+ * Definition: "ViT Encoder Block" (crackedaicode), sections "Inputs and output",
+ * "Normalize before each stage", "Multi-head attention" and "Feed-forward stage".
+ * LN uses population variance (divide by D) and eps is a parameter: that page uses
+ * 1e-5, "ViT Encoder Block" (tensortonic.com), "Requirements", uses 1e-6.
+ * The optional LN gain/bias pairs and MLP biases are those of "ViT Encoder Block"
+ * (ai-engineer-exhaustive), Key Equations, Steps 1, 4 and 5.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers are device pointers unless the name says _host. Arrays are
+ *    C-contiguous (row-major) in the stated shapes, all in one element type
+ *    `dtype` (a vit_dtype value). The library never writes an input.
+ *  - Naming follows the first page: N independent sequences of T tokens of width D;
+ *    H heads of width D/H; F the MLP width.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is only
+ *    enqueued: calls return before the GPU finishes, unless the environment
+ *    variable VIT_DEBUG_SYNC=1 is set, in which case each call synchronises the
+ *    stream and reports device-side errors in its status.
+ *  - Scratch memory is taken from a library-owned, stream-ordered memory pool on the
+ *    current device and returned to it on `stream`; the caller owns every pointer it
+ *    passes.
+ *  - Every call returns a vit_status (0 = success). No call aborts, traps or throws.
+ *  - Results are deterministic: the same inputs give bit-identical outputs.
+ */
+#ifndef VIT_BLOCK_H
+#define VIT_BLOCK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. VIT_F64 runs on the CUDA-core path only. */
+typedef enum { VIT_F32 = 0, VIT_BF16 = 1, VIT_F64 = 2 } vit_dtype;
+
+/* Status codes. */
+typedef enum {
+    VIT_OK = 0,
+    VIT_ERR_ARG = -1,         /* null pointer, non-positive size, H not dividing D, aliasing */
+    VIT_ERR_DTYPE = -2,       /* unknown dtype, or a dtype the entry point does not take */
+    VIT_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed */
+    VIT_ERR_TIMEOUT = -4,     /* a device-side wait ran out (reported after a sync) */
+    VIT_ERR_NOMEM = -5,       /* scratch allocation failed */
+    VIT_ERR_UNSUPPORTED = -6  /* a step-level entry point's shape/alignment rule not met */
+} vit_status;
+
+/*
+ * vit_block -- one encoder block, no LN gain/bias and no biases (the first page).
+ *
+ *   x        (N, T, D)     input tokens
+ *   w_q, w_k, w_v, w_o (D, D)  attention projections, used as  xn @ w
+ *   w_mlp1   (D, F), w_mlp2 (F, D)
+ *   N, T, D, F, H > 0 with D % H == 0
+ *   eps      LN epsilon (> 0 recommended; any finite value is accepted)
+ *   dtype    VIT_BF16: bf16 storage, fp32 accumulation; LN statistics, softmax and
+ *            GELU in fp32; y kept in fp32; out rounded to bf16 (round-to-nearest-even).
+ *            VIT_F32: fp32 throughout. VIT_F64: fp64 throughout.
+ *   out      (N, T, D), must not overlap any input
+ * Errors: VIT_ERR_ARG, VIT_ERR_DTYPE, VIT_ERR_NOMEM, VIT_ERR_CUDA (and VIT_ERR_TIMEOUT
+ * under VIT_DEBUG_SYNC=1). On error nothing is guaranteed about `out`.
+ */
+int vit_block(const void* x, const void* w_q, const void* w_k, const void* w_v,
+              const void* w_o, const void* w_mlp1, const void* w_mlp2,
+              int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+              double eps, int dtype, void* out, void* stream);
+
+/*
+ * vit_block_ex -- vit_block with the optional affine terms, each nullable:
+ *   ln1_g, ln1_b, ln2_g, ln2_b  (D)   LN gain (NULL = 1) and bias (NULL = 0),
+ *                                     one pair per LN (the two LNs do not share them)
+ *   b1 (F), b2 (D)                    MLP biases (NULL = 0)
+ * "ViT Encoder Block" (ai-engineer-exhaustive), Key Equations, Steps 1, 4, 5.
+ * Same types, layouts, ownership and errors as vit_block.
+ */
+int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                 const void* w_o, const void* w_mlp1, const void* w_mlp2,
+                 const void* ln1_g, const void* ln1_b, const void* ln2_g,
+                 const void* ln2_b, const void* b1, const void* b2,
+                 int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+                 double eps, int dtype, void* out, void* stream);
+
+/*
+ * vit_block_host -- vit_block_ex on HOST arrays: copies the inputs to the device,
+ * runs the block and copies `out_host` back, all on `stream`, then synchronises
+ * the stream before returning (so out_host is ready on return). Host arrays that
+ * are page-locked (cudaHostAlloc / pinned) copy at full link speed; pageable ones
+ * work but copy slower. Device buffers come from the library's pool. The optional
+ * affine pointers are host pointers or NULL. Errors as vit_block.
+ */
+int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_host,
+                   const void* w_v_host, const void* w_o_host, const void* w_mlp1_host,
+                   const void* w_mlp2_host, const void* ln1_g_host, const void* ln1_b_host,
+                   const void* ln2_g_host, const void* ln2_b_host, const void* b1_host,
+                   const void* b2_host, int64_t N, int64_t T, int64_t D, int64_t F,
+                   int64_t H, double eps, int dtype, void* out_host, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Step-level entry points: each runs one stage of the block on its own. They use
+ * the same kernels as vit_block and exist for stage-by-stage checking and for
+ * callers that compose the stages differently.
+ * ------------------------------------------------------------------------------ */
+
+/*
+ * vit_layernorm -- out[r, :] = LN(x[r, :]) [* gamma + beta] for r < rows.
+ * "ViT Encoder Block" (crackedaicode), "Normalize before each stage".
+ *   x     (rows, D) of in_dtype; gamma, beta (D) of out_dtype or NULL
+ *   out   (rows, D) of out_dtype
+ * Type pairs: (BF16 -> BF16), (F32 -> BF16), (F32 -> F32), (F64 -> F64).
+ * Errors: VIT_ERR_ARG, VIT_ERR_DTYPE, VIT_ERR_CUDA.
+ */
+int vit_layernorm(const void* x, int64_t rows, int64_t D, double eps, const void* gamma,
+                  const void* beta, int in_dtype, void* out, int out_dtype, void* stream);
+
+/* Epilogues of vit_linear. */
+typedef enum {
+    VIT_EPI_STORE = 0,        /* out = a @ w [+ bias]                            */
+    VIT_EPI_GELU = 1,         /* out = GELU_tanh(a @ w [+ bias])                 */
+    VIT_EPI_RESIDUAL = 2      /* out = residual + a @ w [+ bias]                 */
+} vit_epilogue;
+
+/*
+ * vit_linear -- out (M, N) = epilogue(a (M, K) @ w (K, N)).
+ * "ViT Encoder Block" (crackedaicode): the projections of "Multi-head attention"
+ * and the two MLP matrices of "Feed-forward stage"; GELU as defined there.
+ *   dtype       element type of a, w, bias
+ *   residual    (M, N) of residual_dtype (EPI_RESIDUAL only, else NULL)
+ *   out_dtype   element type of out
+ * Supported: dtype BF16 with out BF16/F32 and residual BF16/F32 (tensor cores when
+ * K % 64 == 0, N % 64 == 0 and every pointer is 16-byte aligned, CUDA cores
+ * otherwise); dtype F32 or F64 with out, residual of the same type (CUDA cores).
+ * Errors: VIT_ERR_ARG, VIT_ERR_DTYPE, VIT_ERR_CUDA.
+ */
+int vit_linear(const void* a, const void* w, const void* bias, const void* residual,
+               int64_t M, int64_t K, int64_t N, int epilogue, int dtype,
+               int residual_dtype, void* out, int out_dtype, void* stream);
+
+/*
+ * vit_attention -- unmasked multi-head attention over a fused QKV buffer.
+ * "ViT Encoder Block" (crackedaicode), "Multi-head attention"; fused layout
+ * [Q | K | V] with head h at columns h*D/H of each block, as in
+ * "vision1 reference transcript" (nipunbatra.github.io), Page 106.
+ *   qkv  (N, T, 3D) of dtype;  o (N, T, D) of dtype, heads concatenated in order.
+ * Errors: VIT_ERR_ARG, VIT_ERR_DTYPE, VIT_ERR_CUDA.
+ */
+int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, int dtype,
+                  void* o, void* stream);
+
+/* ------------------------------------------------------------------------------
+ * Status, diagnostics and measurement
+ * ------------------------------------------------------------------------------ */
+
+/* Static English text for a status code (never NULL). */
+const char* vit_status_string(int status);
+
+/*
+ * vit_device_error -- synchronise the current device, then read and clear the
+ * device error word that kernels set when a bounded wait runs out. Writes the word
+ * to *word (0 = no error) and returns VIT_OK, VIT_ERR_TIMEOUT if it was set, or
+ * VIT_ERR_CUDA if the synchronisation failed.
+ */
+int vit_device_error(uint32_t* word);
+
+/* Number of kernels this library has launched in this process (all devices). */
+int64_t vit_launch_count(void);
+
+/*
+ * Per-kernel timing. With timing enabled, vit_block records a CUDA event before
+ * and after each kernel on the caller's stream. vit_timing_collect synchronises
+ * every stream with pending records, adds the elapsed times into per-kernel totals
+ * and releases the events. vit_timing_read returns the total milliseconds and the
+ * launch count for one kernel index (0 <= k < vit_timing_kernels()) and its name.
+ * vit_timing_reset clears the totals. Timing adds two event records per launch.
+ */
+int vit_timing_enable(int enable);
+int vit_timing_collect(void);
+int vit_timing_kernels(void);
+int vit_timing_read(int k, double* total_ms, int64_t* launches, const char** name);
+int vit_timing_reset(void);
+
+/* Library version string. */
+const char* vit_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VIT_BLOCK_H */

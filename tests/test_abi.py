@@ -1,0 +1,96 @@
+"""The C-ABI library without a GPU: it loads, exports every function the header
+declares, and the host-side argument checks answer before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from vision_transformer_encoder_gb300 import api, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vit_block.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return api.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vit_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_surface():
+    assert declared_functions() == sorted(api.SIGNATURES)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_are_exactly_the_header(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", api.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = sorted(set(re.findall(r" T (vit_[a-z_0-9]+)$", out, flags=re.M)))
+    assert exported == declared_functions()
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        s = api.status_string(code)
+        assert s and s != "unknown status"
+    assert api.status_string(-99) == "unknown status"
+
+
+def _fake(i):
+    # distinct, well-separated fake device addresses; never dereferenced because
+    # validation fails first
+    return ctypes.c_void_p(0x100000000 * (i + 1))
+
+
+def _call_block(lib, N=2, T=5, D=8, F=16, H=2, dtype=1, x=None, out=None, null_w=False):
+    ws = [None if null_w else _fake(i + 1) for i in range(6)]
+    return lib.vit_block(x if x is not None else _fake(0), *ws, N, T, D, F, H, 1e-5, dtype,
+                         out if out is not None else _fake(10), None)
+
+
+def test_invalid_sizes_are_rejected_on_the_host(lib):
+    assert _call_block(lib, D=8, H=3) == -1          # H does not divide D
+    assert _call_block(lib, N=0) == -1
+    assert _call_block(lib, T=-1) == -1
+    assert _call_block(lib, F=0) == -1
+    assert _call_block(lib, H=0) == -1
+    assert _call_block(lib, null_w=True) == -1
+
+
+def test_unknown_dtype_rejected(lib):
+    assert _call_block(lib, dtype=7) == -2
+
+
+def test_out_aliasing_an_input_is_rejected(lib):
+    x = _fake(0)
+    assert _call_block(lib, x=x, out=x) == -1
+    # out overlapping the tail of x
+    assert _call_block(lib, x=x, out=ctypes.c_void_p(x.value + 16)) == -1
+
+
+def test_step_entry_points_validate(lib):
+    assert lib.vit_layernorm(None, 4, 8, 1e-5, None, None, 1, _fake(1), 1, None) == -1
+    assert lib.vit_layernorm(_fake(0), 4, 8, 1e-5, None, None, 2, _fake(1), 1, None) == -2
+    assert lib.vit_linear(_fake(0), _fake(1), None, None, 4, 8, 8, 2, 1, 1, _fake(2), 1, None) == -1
+    assert lib.vit_linear(_fake(0), _fake(1), None, None, 4, 8, 8, 0, 0, 0, _fake(2), 1, None) == -2
+    assert lib.vit_attention(_fake(0), 1, 4, 8, 3, 1, _fake(1), None) == -1
+
+
+def test_timing_interface_without_gpu(lib):
+    assert lib.vit_timing_kernels() == 7
+    ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
+    assert lib.vit_timing_read(0, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm)) == 0
+    assert nm.value == b"ln1"
+    assert lib.vit_timing_read(99, None, None, None) == -1

@@ -1,0 +1,164 @@
+"""Whole-block parity of vit_block / vit_block_ex (GPU) against the float64 oracle.
+
+Tolerances are the ones the block is specified to: max-abs <= 3e-2 on the bf16
+path (bf16 storage, fp32 accumulation; outputs of O(1) scale) and <= 2e-4 on the
+fp32 path; the fp64 path is held to 1e-10. Small configurations are compared in
+full. At the full ViT-B/L/H sizes, in the launch configuration the benchmark times,
+the oracle recomputes a fixed sample of sequences {0, 1, N/2, N-1}: sequences are
+independent (a property the oracle's own tests pin), so those rows of the GPU
+output must equal the oracle run on those sequences alone.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vision_transformer_encoder_gb300 import api
+from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 3e-2, torch.float32: 2e-4, torch.float64: 1e-10}
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _run(inp, H, eps, affine=False):
+    d = inp.to(device=_dev())
+    out = torch.full_like(d.x, float("nan"))     # unwritten elements would stay NaN
+    if affine:
+        api.vit_block_ex(d.x, *d.weights(), H, eps, **d.affine(), out=out)
+    else:
+        api.vit_block(d.x, *d.weights(), H, eps, out=out)
+    torch.cuda.synchronize()
+    return out.cpu(), d
+
+
+def _oracle(inp, H, eps, idx=None, affine=False):
+    sel = (lambda t: t) if idx is None else (lambda t: t[idx])
+    kw = {k: v for k, v in inp.affine().items()} if affine else {}
+    return oracle.vit_block(sel(inp.x), *inp.weights(), H, eps, **kw)
+
+
+def _maxerr(gpu, ref):
+    g = gpu.double().numpy()
+    assert np.isfinite(g).all()
+    return float(np.abs(g - ref).max())
+
+
+@pytest.mark.parametrize("dtype", [torch.float64, torch.float32, torch.bfloat16])
+def test_tiny_config(dtype):
+    c = CONFIGS["tiny"]
+    inp = make_config_inputs("tiny", dtype=dtype)
+    out, _ = _run(inp, c["H"], c["eps"])
+    assert _maxerr(out, _oracle(inp, c["H"], c["eps"])) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("i", [0, 1, 2])
+@pytest.mark.parametrize("dtype", [torch.float64, torch.float32])
+def test_printed_worked_examples_on_gpu(i, dtype):
+    with open(os.path.join(GOLDEN, "p2_worked_examples.json")) as f:
+        g = json.load(f)
+    ex = g["examples"][i]
+    d = _dev()
+    t = lambda k: torch.tensor(ex[k], dtype=dtype, device=d)
+    x = t("x")
+    out = api.vit_block(x, t("Wq"), t("Wk"), t("Wv"), t("Wo"), t("W1"), t("W2"),
+                        ex["num_heads"], g["eps"])
+    torch.cuda.synchronize()
+    tol = g["print_tolerance"] + (0 if dtype == torch.float64 else 2e-6)
+    assert np.abs(out.double().cpu().numpy() - np.array(ex["output"])).max() <= tol
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_vit_ti16_config(dtype):
+    c = CONFIGS["vit_ti16"]
+    inp = make_config_inputs("vit_ti16", dtype=dtype)
+    out, _ = _run(inp, c["H"], c["eps"])
+    assert _maxerr(out, _oracle(inp, c["H"], c["eps"])) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("shape", [(3, 7, 40, 5, 72), (2, 130, 64, 1, 128), (1, 33, 128, 2, 192),
+                                   (2, 9, 96, 3, 256)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_odd_shapes(shape, dtype):
+    N, T, D, H, F = shape
+    inp = make_inputs(N, T, D, F, seed=5, dtype=dtype, affine=True)
+    out, _ = _run(inp, H, 1e-5, affine=True)
+    assert _maxerr(out, _oracle(inp, H, 1e-5, affine=True)) <= TOL[dtype]
+
+
+def _sample(N):
+    return sorted({0, 1, N // 2, N - 1})
+
+
+@pytest.mark.parametrize("name,affine", [("vit_b16", False), ("vit_b16", True),
+                                         ("vit_l16_384", False), ("vit_h14_448", False)])
+def test_full_size_configs_sampled(name, affine):
+    c = CONFIGS[name]
+    inp = make_config_inputs(name, dtype=torch.bfloat16, affine=affine)
+    out, d = _run(inp, c["H"], c["eps"], affine=affine)
+    idx = _sample(c["N"])
+    ref = _oracle(inp, c["H"], c["eps"], idx=idx, affine=affine)
+    err = _maxerr(out[idx], ref)
+    assert err <= TOL[torch.bfloat16], err
+    # the inputs are left unchanged
+    assert torch.equal(d.x.cpu(), inp.x)
+    for a, b in zip(d.weights(), inp.weights()):
+        assert torch.equal(a.cpu(), b)
+
+
+def test_b16_whole_output_properties():
+    """Every row of the full-size output is finite and of O(1) scale; the zero-update
+    identity holds at full size: w_o = 0 and w_mlp2 = 0 return x exactly."""
+    c = CONFIGS["vit_b16"]
+    inp = make_config_inputs("vit_b16", dtype=torch.bfloat16)
+    inp.w_o = torch.zeros_like(inp.w_o)
+    inp.w_mlp2 = torch.zeros_like(inp.w_mlp2)
+    out, _ = _run(inp, c["H"], c["eps"])
+    assert torch.equal(out, inp.x)
+
+
+def test_deterministic_bitwise():
+    c = CONFIGS["vit_b16"]
+    inp = make_config_inputs("vit_b16", dtype=torch.bfloat16, N=32)
+    a, _ = _run(inp, c["H"], c["eps"])
+    b, _ = _run(inp, c["H"], c["eps"])
+    assert torch.equal(a, b)
+
+
+def test_host_buffer_entry_point_matches_device_call():
+    c = CONFIGS["vit_ti16"]
+    inp = make_config_inputs("vit_ti16", dtype=torch.bfloat16, N=8, affine=True)
+    dev_out, _ = _run(inp, c["H"], c["eps"], affine=True)
+    pinned = inp.to(device="cpu")
+    args = [t.pin_memory() for t in [pinned.x] + pinned.weights()]
+    aff = {k: v.pin_memory() for k, v in pinned.affine().items()}
+    host_out = api.vit_block_host(*args, c["H"], c["eps"], **aff, out=torch.empty_like(args[0]).pin_memory())
+    assert torch.equal(host_out, dev_out)
+
+
+def test_stream_argument_is_honoured():
+    d = _dev()
+    c = CONFIGS["vit_ti16"]
+    inp = make_config_inputs("vit_ti16", dtype=torch.bfloat16, N=4)
+    di = inp.to(device=d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = api.vit_block(di.x, *di.weights(), c["H"], c["eps"], stream=s)
+    s.synchronize()
+    ref, _ = _run(inp, c["H"], c["eps"])
+    assert torch.equal(out.cpu(), ref)
+
+
+def test_no_device_error_after_block_tests():
+    _dev()
+    assert api.device_error() == 0

@@ -1,0 +1,171 @@
+"""Stage-by-stage parity of the CUDA kernels against the float64 oracle (GPU).
+
+Each stage is called alone through its C-ABI entry point on seeded inputs and
+compared element by element with the oracle's function for that stage, on shapes
+that span several tiles and leave ragged tails (rows not a multiple of 128, columns
+narrower than one 256-wide tile, key counts not a multiple of 64).
+
+Tolerances (bf16 outputs, fp32 accumulation): |gpu - ref| <= atol + rtol * |ref|
+with rtol = 2^-7 (two bf16 rounding steps: the kernel's output rounding and the
+rounding of an fp32 sum that differs from the float64 sum in its last bits).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vision_transformer_encoder_gb300 import api
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 2.0 ** -7
+
+
+def _dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda:0")
+
+
+def _rand(shape, seed, std=1.0, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(dtype)
+
+
+def _close(gpu, ref, atol, rtol=RTOL):
+    g = gpu.double().cpu().numpy()
+    assert np.isfinite(g).all(), "non-finite output (unwritten or overflowed element)"
+    err = np.abs(g - ref)
+    bound = atol + rtol * np.abs(ref)
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), "max excess at %s: gpu %g ref %g" % (worst, g[worst], ref[worst])
+    return err.max()
+
+
+@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (300, 192, 192), (1000, 768, 768),
+                                   (517, 1024, 2304), (64, 128, 64)])
+def test_linear_store_bf16(M, K, N):
+    d = _dev()
+    a, w = _rand((M, K), 1), _rand((K, N), 2, std=K ** -0.5)
+    out = api.linear(a.to(d), w.to(d))
+    torch.cuda.synchronize()
+    _close(out, oracle.matmul(a, w), atol=1e-3)
+
+
+@pytest.mark.parametrize("M,K,N", [(384, 192, 768), (131, 768, 3072)])
+def test_linear_gelu_bias_bf16(M, K, N):
+    d = _dev()
+    a, w, b = _rand((M, K), 3), _rand((K, N), 4, std=K ** -0.5), _rand((N,), 5, std=0.1)
+    out = api.linear(a.to(d), w.to(d), bias=b.to(d), epilogue=api.EPI_GELU)
+    torch.cuda.synchronize()
+    ref = oracle.gelu_tanh(oracle.matmul(a, w, b))
+    _close(out, ref, atol=2e-3)
+
+
+@pytest.mark.parametrize("res_dtype,out_dtype", [(torch.bfloat16, torch.float32),
+                                                 (torch.float32, torch.bfloat16)])
+@pytest.mark.parametrize("M,K,N", [(256, 768, 768), (200, 3072, 192)])
+def test_linear_residual_bf16(M, K, N, res_dtype, out_dtype):
+    d = _dev()
+    a, w = _rand((M, K), 6), _rand((K, N), 7, std=K ** -0.5)
+    r = _rand((M, N), 8, dtype=res_dtype)
+    out = api.linear(a.to(d), w.to(d), residual=r.to(d), epilogue=api.EPI_RESIDUAL,
+                     out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    ref = r.double().numpy() + oracle.matmul(a, w)
+    _close(out, ref, atol=2e-3 if out_dtype == torch.bfloat16 else 1e-3,
+           rtol=RTOL if out_dtype == torch.bfloat16 else 2.0 ** -12)
+
+
+def test_linear_bias_on_residual():
+    d = _dev()
+    M, K, N = 130, 256, 512
+    a, w, b = _rand((M, K), 9), _rand((K, N), 10, std=K ** -0.5), _rand((N,), 11, std=0.1)
+    r = _rand((M, N), 12, dtype=torch.float32)
+    out = api.linear(a.to(d), w.to(d), bias=b.to(d), residual=r.to(d), epilogue=api.EPI_RESIDUAL)
+    torch.cuda.synchronize()
+    _close(out, r.double().numpy() + oracle.matmul(a, w, b), atol=2e-3)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float64])
+def test_linear_cuda_core_types(dtype):
+    d = _dev()
+    M, K, N = 77, 45, 61
+    a, w, b = _rand((M, K), 13, dtype=dtype), _rand((K, N), 14, dtype=dtype), _rand((N,), 15, dtype=dtype)
+    out = api.linear(a.to(d), w.to(d), bias=b.to(d), epilogue=api.EPI_GELU)
+    torch.cuda.synchronize()
+    ref = oracle.gelu_tanh(oracle.matmul(a, w, b))
+    tol = 1e-5 if dtype == torch.float32 else 1e-12
+    _close(out, ref, atol=tol, rtol=tol)
+
+
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("D", [192, 768, 1280])
+@pytest.mark.parametrize("affine", [False, True])
+def test_layernorm_to_bf16(in_dtype, D, affine):
+    d = _dev()
+    x = _rand((333, D), 16, std=2.0, dtype=in_dtype) + 0.5
+    g = (1 + _rand((D,), 17, std=0.1)) if affine else None
+    b = _rand((D,), 18, std=0.1) if affine else None
+    out = api.layernorm(x.to(d), 1e-6, None if g is None else g.to(d), None if b is None else b.to(d),
+                        out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    _close(out, oracle.layernorm(x, 1e-6, g, b), atol=1e-3)
+
+
+def test_layernorm_constant_row_is_zero():
+    d = _dev()
+    x = torch.full((9, 768), 3.25).to(torch.bfloat16)
+    out = api.layernorm(x.to(d), 1e-6, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert (out.float() == 0).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float64])
+def test_layernorm_wide_types(dtype):
+    d = _dev()
+    x = _rand((50, 30), 19, dtype=dtype)
+    out = api.layernorm(x.to(d), 1e-5)
+    torch.cuda.synchronize()
+    tol = 1e-5 if dtype == torch.float32 else 1e-13
+    _close(out, oracle.layernorm(x, 1e-5), atol=tol, rtol=tol)
+
+
+@pytest.mark.parametrize("N,T,D,H", [(2, 197, 128, 2), (1, 65, 64, 1), (3, 77, 160, 2),
+                                     (1, 1, 64, 1), (2, 129, 256, 4), (1, 300, 96, 3)])
+def test_attention_bf16(N, T, D, H):
+    d = _dev()
+    qkv = _rand((N, T, 3 * D), 20 + T, std=1.5)
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    q, k, v = qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:]
+    ref = oracle.attention(q, k, v, H)
+    _close(out, ref, atol=4e-3, rtol=2.0 ** -6)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float64])
+def test_attention_cuda_core_types(dtype):
+    d = _dev()
+    N, T, D, H = 2, 37, 12, 3
+    qkv = _rand((N, T, 3 * D), 21, dtype=dtype)
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    ref = oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H)
+    tol = 1e-5 if dtype == torch.float32 else 1e-12
+    _close(out, ref, atol=tol, rtol=tol)
+
+
+def test_attention_bf16_generic_head_width():
+    # head width 24 is not one the tensor-core kernel takes: CUDA-core kernel, bf16 I/O
+    d = _dev()
+    N, T, D, H = 2, 50, 48, 2
+    qkv = _rand((N, T, 3 * D), 22)
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    ref = oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H)
+    _close(out, ref, atol=2e-3)
+
+
+def test_no_device_error_after_stages():
+    _dev()
+    assert api.device_error() == 0

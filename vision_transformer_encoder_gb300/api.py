@@ -1,0 +1,258 @@
+"""Python binding of the C ABI in include/vit_block.h (argument marshalling only).
+
+Every computation runs in the CUDA library ``libvit_block.so``; this module checks
+that tensors are contiguous and on the right device, picks the element-type code,
+passes raw pointers and the current CUDA stream, and turns a non-zero status into
+``VitError``. There is no fallback: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvit_block.so")
+
+VIT_F32, VIT_BF16, VIT_F64 = 0, 1, 2
+EPI_STORE, EPI_GELU, EPI_RESIDUAL = 0, 1, 2
+
+_DT = {torch.float32: VIT_F32, torch.bfloat16: VIT_BF16, torch.float64: VIT_F64}
+
+# Every exported symbol of the C ABI, with (restype, argtypes).
+_vp, _i64, _int, _dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+SIGNATURES = {
+    "vit_block": (_int, [_vp] * 7 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
+    "vit_block_ex": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
+    "vit_block_host": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
+    "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
+    "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
+    "vit_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _vp, _vp]),
+    "vit_status_string": (ctypes.c_char_p, [_int]),
+    "vit_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "vit_launch_count": (_i64, []),
+    "vit_timing_enable": (_int, [_int]),
+    "vit_timing_collect": (_int, []),
+    "vit_timing_kernels": (_int, []),
+    "vit_timing_read": (_int, [_int, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64),
+                               ctypes.POINTER(ctypes.c_char_p)]),
+    "vit_timing_reset": (_int, []),
+    "vit_version": (ctypes.c_char_p, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VitError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+def load_library(path: str | None = None):
+    """Open libvit_block.so (built by ``vision_transformer_encoder_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError("the vit_block CUDA library is not built (%s missing); run "
+                               "python -m vision_transformer_encoder_gb300.build" % p)
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().vit_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise VitError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    return t
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(dt):
+    if dt not in _DT:
+        raise ValueError("unsupported dtype %s" % dt)
+    return _DT[dt]
+
+
+def vit_block_ex(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln1_b=None,
+                 ln2_g=None, ln2_b=None, b1=None, b2=None, out=None, stream=None):
+    """out (N, T, D) = one pre-LN ViT encoder block of x (N, T, D); optional affine terms."""
+    lib = load_library()
+    dt = x.dtype
+    ts = dict(x=x, w_q=w_q, w_k=w_k, w_v=w_v, w_o=w_o, w_mlp1=w_mlp1, w_mlp2=w_mlp2,
+              ln1_g=ln1_g, ln1_b=ln1_b, ln2_g=ln2_g, ln2_b=ln2_b, b1=b1, b2=b2)
+    for k, v in ts.items():
+        _dev(v, k, dt)
+    N, T, D = x.shape
+    F = w_mlp1.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    _dev(out, "out", dt)
+    with torch.cuda.device(x.device):
+        rc = lib.vit_block_ex(*[_ptr(ts[k]) for k in ts], N, T, D, F, int(H), float(eps),
+                              _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_block_ex")
+    return out
+
+
+def vit_block(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, out=None, stream=None):
+    """out (N, T, D) = one pre-LN ViT encoder block of x (N, T, D), no affine terms."""
+    lib = load_library()
+    dt = x.dtype
+    ws = [w_q, w_k, w_v, w_o, w_mlp1, w_mlp2]
+    _dev(x, "x", dt)
+    for i, w in enumerate(ws):
+        _dev(w, "weight %d" % i, dt)
+    N, T, D = x.shape
+    F = w_mlp1.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    _dev(out, "out", dt)
+    with torch.cuda.device(x.device):
+        rc = lib.vit_block(_ptr(x), *[_ptr(w) for w in ws], N, T, D, F, int(H), float(eps),
+                           _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_block")
+    return out
+
+
+def vit_block_host(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln1_b=None,
+                   ln2_g=None, ln2_b=None, b1=None, b2=None, out=None, stream=None, device=0):
+    """The block on HOST tensors (pinned for full copy speed): the library copies the
+    inputs in, runs, copies `out` back and synchronises the stream."""
+    lib = load_library()
+    dt = x.dtype
+    ts = [x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, ln1_g, ln1_b, ln2_g, ln2_b, b1, b2]
+    for t in ts:
+        if t is not None and (t.is_cuda or not t.is_contiguous() or t.dtype != dt):
+            raise ValueError("vit_block_host takes contiguous host tensors of one dtype")
+    N, T, D = x.shape
+    F = w_mlp1.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(device):
+        rc = lib.vit_block_host(*[_ptr(t) for t in ts], N, T, D, F, int(H), float(eps),
+                                _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_block_host")
+    return out
+
+
+def layernorm(x, eps, gamma=None, beta=None, out_dtype=None, out=None, stream=None):
+    lib = load_library()
+    _dev(x, "x")
+    od = out_dtype or x.dtype
+    D = x.shape[-1]
+    rows = x.numel() // D
+    if out is None:
+        out = torch.empty(x.shape, dtype=od, device=x.device)
+    _dev(out, "out", od)
+    _dev(gamma, "gamma", od)
+    _dev(beta, "beta", od)
+    with torch.cuda.device(x.device):
+        rc = lib.vit_layernorm(_ptr(x), rows, D, float(eps), _ptr(gamma), _ptr(beta),
+                               _dtype_code(x.dtype), _ptr(out), _dtype_code(od), _stream(stream))
+    _check(rc, "vit_layernorm")
+    return out
+
+
+def linear(a, w, bias=None, residual=None, epilogue=EPI_STORE, out_dtype=None, out=None,
+           stream=None):
+    lib = load_library()
+    _dev(a, "a")
+    _dev(w, "w", a.dtype)
+    _dev(bias, "bias", a.dtype)
+    _dev(residual, "residual")
+    K, N = w.shape
+    M = a.numel() // K
+    od = out_dtype or a.dtype
+    if out is None:
+        out = torch.empty(a.shape[:-1] + (N,), dtype=od, device=a.device)
+    _dev(out, "out", od)
+    rdt = _dtype_code(residual.dtype) if residual is not None else 0
+    with torch.cuda.device(a.device):
+        rc = lib.vit_linear(_ptr(a), _ptr(w), _ptr(bias), _ptr(residual), M, K, N, int(epilogue),
+                            _dtype_code(a.dtype), rdt, _ptr(out), _dtype_code(od), _stream(stream))
+    _check(rc, "vit_linear")
+    return out
+
+
+def attention(qkv, H, out=None, stream=None):
+    lib = load_library()
+    _dev(qkv, "qkv")
+    N, T, D3 = qkv.shape
+    D = D3 // 3
+    if out is None:
+        out = torch.empty((N, T, D), dtype=qkv.dtype, device=qkv.device)
+    _dev(out, "out", qkv.dtype)
+    with torch.cuda.device(qkv.device):
+        rc = lib.vit_attention(_ptr(qkv), N, T, D, int(H), _dtype_code(qkv.dtype), _ptr(out),
+                               _stream(stream))
+    _check(rc, "vit_attention")
+    return out
+
+
+def device_error() -> int:
+    """Synchronise, then read and clear the device error word (0 = none)."""
+    w = ctypes.c_uint32(0)
+    rc = load_library().vit_device_error(ctypes.byref(w))
+    if rc not in (0, -4):
+        raise VitError(rc, "vit_device_error")
+    return int(w.value)
+
+
+def launch_count() -> int:
+    return int(load_library().vit_launch_count())
+
+
+def timing_enable(on: bool):
+    load_library().vit_timing_enable(1 if on else 0)
+
+
+def timing_reset():
+    load_library().vit_timing_reset()
+
+
+def timing_collect() -> dict:
+    """Synchronise pending timing records; returns {kernel: (total_ms, launches)}."""
+    lib = load_library()
+    _check(lib.vit_timing_collect(), "vit_timing_collect")
+    out = {}
+    for k in range(lib.vit_timing_kernels()):
+        ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
+        lib.vit_timing_read(k, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm))
+        out[nm.value.decode()] = (ms.value, n.value)
+    return out

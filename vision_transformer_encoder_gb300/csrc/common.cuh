@@ -1,0 +1,113 @@
+// common.cuh -- small device/host helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "vit_block.h"
+
+namespace vit {
+
+// Device error word bits (see vit_device_error).
+enum : uint32_t {
+    ERRBIT_TIMEOUT_PRODUCER = 1u << 0,
+    ERRBIT_TIMEOUT_MMA = 1u << 1,
+    ERRBIT_TIMEOUT_EPILOGUE = 1u << 2,
+    ERRBIT_TIMEOUT_TEARDOWN = 1u << 3,
+    ERRBIT_TIMEOUT_ATTENTION = 1u << 4,
+};
+
+// One bounded device-side wait gives up after this many nanoseconds.
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Hardware tanh approximation (MUFU), max relative error about 2^-11.
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Hardware base-2 exponential approximation (MUFU).
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// tanh-approximation GELU, "ViT Encoder Block" (crackedaicode), "Feed-forward stage":
+// 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). Fast form for bf16 outputs.
+__device__ __forceinline__ float gelu_tanh_fast(float z) {
+    const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+    const float k1 = 0.044715f;
+    float u = k0 * fmaf(k1 * z, z * z, z);
+    return 0.5f * z * (1.0f + tanh_approx(u));
+}
+
+// Accurate forms (library tanh) for the fp32 / fp64 paths.
+__device__ __forceinline__ float gelu_tanh_acc(float z) {
+    const float k0 = 0.7978845608028654f;
+    float u = k0 * (z + 0.044715f * z * z * z);
+    return 0.5f * z * (1.0f + tanhf(u));
+}
+__device__ __forceinline__ double gelu_tanh_acc(double z) {
+    const double k0 = 0.79788456080286535588;  // sqrt(2/pi)
+    double u = k0 * (z + 0.044715 * z * z * z);
+    return 0.5 * z * (1.0 + tanh(u));
+}
+
+// Element conversions.
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<double>(double v) { return (float)v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+    return __bfloat162float(v);
+}
+
+template <typename A, typename T> __device__ __forceinline__ A to_acc(T v) { return (A)to_f32(v); }
+template <> __device__ __forceinline__ double to_acc<double, double>(double v) { return v; }
+
+template <typename T> __device__ __forceinline__ T from_acc(float v);
+template <> __device__ __forceinline__ float from_acc<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_acc<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+template <> __device__ __forceinline__ double from_acc<double>(float v) { return v; }
+template <typename T> __device__ __forceinline__ T from_acc(double v) { return from_acc<T>((float)v); }
+template <> __device__ __forceinline__ double from_acc<double>(double v) { return v; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
+    return __bfloat1622float2(h);
+}
+
+}  // namespace vit

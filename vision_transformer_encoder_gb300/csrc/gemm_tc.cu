@@ -1,0 +1,414 @@
+// gemm_tc.cu -- persistent tcgen05 GEMM with fused epilogues, for the four dense
+// contractions of the block ("ViT Encoder Block" (crackedaicode): the Q/K/V and
+// output projections of "Multi-head attention", the two MLP matrices of
+// "Feed-forward stage"):
+//
+//   QKV : qkv = xn @ [w_q | w_k | w_v]           epilogue: store bf16
+//   Wo  : y   = x + o @ w_o                       epilogue: + residual (bf16) -> fp32
+//   W1  : h   = GELU_tanh(yn @ w_mlp1 [+ b1])     epilogue: GELU -> bf16
+//   W2  : out = y + h @ w_mlp2 [+ b2]             epilogue: + residual (fp32) -> bf16
+//
+// Design (sm_103a): one CTA per SM, persistent over 128 x 256 output tiles.
+//   warp 0      TMA producer: A tile 128 x 64 (K-major, 128B swizzle) and four
+//               64(N) x 64(K) boxes of the row-major weight (MN-major, 128B swizzle)
+//               per stage, 4-stage ring, completion counted on mbarriers.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
+//               issues tcgen05.mma (M 128, N 256, K 16) from one thread; commits
+//               free ring slots and announce finished accumulators.
+//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time (one output row per
+//               thread), fused bias / GELU / residual, vector stores.
+// The weights are read in their (in, out) storage order directly: the B operand is
+// MN-major, so no transposed copy is made. Every wait is bounded; on expiry the
+// kernel sets a bit in the device error word, lets its copies and MMAs drain, frees
+// TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace vit {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int B_BOX_BYTES = 64 * BK * 2;    // 8 KB: 64 N columns x 64 K rows
+constexpr int B_BYTES = BN * BK * 2;        // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC_COLS = BN;                // fp32 columns per accumulator
+constexpr int TMEM_COLS = 2 * ACC_COLS;     // double-buffered
+constexpr int THREADS = 192;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+
+struct Params {
+    int M, N, K;
+    int n_per_w, n_w;
+    const __nv_bfloat16* bias;
+    const void* residual;
+    int64_t ldr;
+    void* out;
+    int64_t ldo;
+    uint32_t* err;
+};
+
+__device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u = __ldg(q + i);
+        float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z),
+               d = unpack_bf16x2(u.w);
+        v[8 * i + 0] = a.x; v[8 * i + 1] = a.y; v[8 * i + 2] = b.x; v[8 * i + 3] = b.y;
+        v[8 * i + 4] = c.x; v[8 * i + 5] = c.y; v[8 * i + 6] = d.x; v[8 * i + 7] = d.y;
+    }
+}
+
+__device__ __forceinline__ void load32(const float* p, float (&v)[32]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float4 u = __ldg(q + i);
+        v[4 * i + 0] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+    }
+}
+
+__device__ __forceinline__ void store32(__nv_bfloat16* p, const float (&v)[32]) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
+        u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
+        u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
+        u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
+        q[i] = u;
+    }
+}
+
+__device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
+    float4* q = reinterpret_cast<float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+template <int EPI, typename OutT, typename ResT>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+               const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + STAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (p.M + BM - 1) / BM;
+    const int n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int kblocks = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full + s, 1);
+            ptx::mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull + a, 1);
+            ptx::mbar_init(tempty + a, 128);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB0);
+        if (p.n_w > 1) ptx::prefetch_tensormap(&tmB1);
+        if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int m0 = (tile / n_tiles) * BM;
+                const int n0 = (tile % n_tiles) * BN;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, u = it / STAGES;
+                    if (!ptx::mbar_wait_bounded(empty + s, (u & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full + s, STAGE_BYTES);
+                    ptx::tma_load_2d(sA + s * A_BYTES, &tmA, full + s, kb * BK, m0);
+#pragma unroll
+                    for (int j = 0; j < BN / 64; ++j) {
+                        const int col = n0 + 64 * j;
+                        int wi = col / p.n_per_w;
+                        if (wi > p.n_w - 1) wi = p.n_w - 1;  // past N: zero-filled box
+                        const int lc = col - wi * p.n_per_w;
+                        const CUtensorMap* tb = wi == 0 ? &tmB0 : (wi == 1 ? &tmB1 : &tmB2);
+                        ptx::tma_load_2d(sB + s * B_BYTES + j * B_BOX_BYTES, tb, full + s, lc,
+                                         kb * BK);
+                    }
+                }
+            }
+            if (!ok) {
+                set_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
+                *abort_flag = 1;
+            }
+            // Let every copy this thread issued land before the CTA can exit.
+            for (uint32_t s = 0; s < STAGES; ++s) {
+                if (it > s) {
+                    const uint32_t u_last = (it - 1 - s) / STAGES;
+                    if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
+                        set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t v = (uint32_t)(local >> 1);
+                if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % STAGES, u = it / STAGES;
+                    if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_base = ptx::smem_addr(sA + s * A_BYTES);
+                    const uint32_t b_base = ptx::smem_addr(sB + s * B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
+                        const uint64_t adesc = ptx::smem_desc_sw128(a_base + k * 32, 16, 1024);
+                        // B: MN-major, advance 16 K rows = 2 groups of 8 rows (2048 bytes);
+                        // 64-column chunks are B_BOX_BYTES apart.
+                        const uint64_t bdesc =
+                            ptx::smem_desc_sw128(b_base + k * 2048, B_BOX_BYTES, 1024);
+                        ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+                    }
+                    ptx::mma_commit(empty + s);
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull + acc);
+            }
+            if (!ok) {
+                set_error(p.err, ERRBIT_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            // Every MMA issued must finish before TMEM is released.
+            ptx::mma_commit(done);
+            if (!ptx::mbar_wait_bounded(done, 0, nullptr)) set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps 2..5
+        const int quarter = warp & 3;  // TMEM lane quarter this warp may read
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t v = (uint32_t)(local >> 1);
+            // The TMEM loads below are warp-collective: the whole warp goes on or stops.
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(tfull + acc, v & 1, abort_flag));
+            if (!ok) {
+                if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int m0 = (tile / n_tiles) * BM;
+            const int n0 = (tile % n_tiles) * BN;
+            const int row = m0 + quarter * 32 + lane;
+            const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
+                ptx::tmem_ld_wait();
+                const int col = n0 + c * 32;
+                if (row < p.M && col < p.N) {
+                    float val[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
+                    if (p.bias) {
+                        float b[32];
+                        load32(p.bias + col, b);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) val[j] += b[j];
+                    }
+                    if (EPI == TC_EPI_GELU) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
+                    } else if (EPI == TC_EPI_RESID) {
+                        float rv[32];
+                        load32(reinterpret_cast<const ResT*>(p.residual) + (int64_t)row * p.ldr + col, rv);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) val[j] += rv[j];
+                    }
+                    store32(reinterpret_cast<OutT*>(p.out) + (int64_t)row * p.ldo + col, val);
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(tempty + acc);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix (rows, cols) with row stride `ld` elements; box (box_cols, box_rows).
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld,
+              uint32_t box_cols, uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int EPI, typename OutT, typename ResT>
+cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params& p, int grid,
+                        cudaStream_t s) {
+    auto k = gemm_tc_kernel<EPI, OutT, ResT>;
+    static bool attr_set = false;  // per instantiation; idempotent, so a race is harmless
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    k<<<grid, THREADS, SMEM_BYTES, s>>>(a, b[0], b[1], b[2], p);
+    return cudaGetLastError();
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool tc_gemm_supported(const TcGemmDesc& d) {
+    if (d.M <= 0 || d.N <= 0 || d.K <= 0) return false;
+    if (d.K % BK != 0 || d.n_per_w % 64 != 0 || d.N != d.n_w * d.n_per_w) return false;
+    if (d.n_w < 1 || d.n_w > 3) return false;
+    if (d.M > 0x7fffffff || d.N > 0x7fffffff || d.K > 0x7fffffff) return false;
+    if (!aligned16(d.a) || (d.lda * 2) % 16 != 0) return false;
+    for (int i = 0; i < d.n_w; ++i)
+        if (!aligned16(d.w[i])) return false;
+    if (!aligned16(d.out) || (d.ldo * (d.out_f32 ? 4 : 2)) % 16 != 0) return false;
+    if (d.bias && !aligned16(d.bias)) return false;
+    if (d.epi == TC_EPI_RESID &&
+        (!d.residual || !aligned16(d.residual) || (d.ldr * (d.residual_f32 ? 4 : 2)) % 16 != 0))
+        return false;
+    return encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStream_t s) {
+    alignas(64) CUtensorMap ma;
+    alignas(64) CUtensorMap mb[3];
+    if (!make_map(&ma, d.a, d.M, d.K, d.lda, BK, BM)) return cudaErrorInvalidValue;
+    for (int i = 0; i < 3; ++i) {
+        const void* w = d.w[i < d.n_w ? i : 0];
+        if (!make_map(&mb[i], w, d.K, d.n_per_w, d.n_per_w, 64, BK)) return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.M = (int)d.M;
+    p.N = (int)d.N;
+    p.K = (int)d.K;
+    p.n_per_w = (int)d.n_per_w;
+    p.n_w = d.n_w;
+    p.bias = reinterpret_cast<const __nv_bfloat16*>(d.bias);
+    p.residual = d.residual;
+    p.ldr = d.ldr;
+    p.out = d.out;
+    p.ldo = d.ldo;
+    p.err = dev.err_word;
+    const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
+    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    switch (d.epi) {
+        case TC_EPI_STORE:
+            return d.out_f32 ? launch_inst<TC_EPI_STORE, float, float>(ma, mb, p, grid, s)
+                             : launch_inst<TC_EPI_STORE, __nv_bfloat16, float>(ma, mb, p, grid, s);
+        case TC_EPI_GELU:
+            return d.out_f32 ? launch_inst<TC_EPI_GELU, float, float>(ma, mb, p, grid, s)
+                             : launch_inst<TC_EPI_GELU, __nv_bfloat16, float>(ma, mb, p, grid, s);
+        case TC_EPI_RESID:
+            if (d.out_f32)
+                return d.residual_f32
+                           ? launch_inst<TC_EPI_RESID, float, float>(ma, mb, p, grid, s)
+                           : launch_inst<TC_EPI_RESID, float, __nv_bfloat16>(ma, mb, p, grid, s);
+            return d.residual_f32
+                       ? launch_inst<TC_EPI_RESID, __nv_bfloat16, float>(ma, mb, p, grid, s)
+                       : launch_inst<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(ma, mb, p, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vit

@@ -1,0 +1,205 @@
+// layernorm.cu -- per-token LayerNorm over the D features.
+// "ViT Encoder Block" (crackedaicode), "Normalize before each stage":
+//   LN(x) = (x - mean) / sqrt(variance + eps), population variance (divide by D);
+// optional gain/bias per feature: "ViT Encoder Block" (ai-engineer-exhaustive),
+// Key Equations, Step 1.
+//
+// Fast kernel (bf16 or fp32 input, bf16 output, D % 8 == 0, D <= 2048): one warp per
+// row; the row is read once with 16-byte loads into registers; mean and the centred
+// sum of squares (two passes over the registers, never E[x^2] - mean^2, so a constant
+// row normalises to exactly 0) are warp-shuffle reductions in fp32. HBM-bound:
+// D * (in + out) bytes per row.
+// Generic kernel: any supported type pair, one warp per row, strided loops.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace vit {
+namespace {
+
+constexpr int LN_THREADS = 256;  // 8 rows per CTA
+
+template <typename TIn> struct VecIO;
+template <> struct VecIO<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ static void load(const __nv_bfloat16* p, float (&v)[N]) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z),
+               d = unpack_bf16x2(u.w);
+        v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+        v[4] = c.x; v[5] = c.y; v[6] = d.x; v[7] = d.y;
+    }
+};
+template <> struct VecIO<float> {
+    static constexpr int N = 4;
+    __device__ static void load(const float* p, float (&v)[N]) {
+        float4 u = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+    }
+};
+
+template <int N> __device__ __forceinline__ void store_bf16(__nv_bfloat16* p, const float (&v)[N]);
+template <> __device__ __forceinline__ void store_bf16<8>(__nv_bfloat16* p, const float (&v)[8]) {
+    uint4 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    u.z = pack_bf16x2(v[4], v[5]);
+    u.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(p) = u;
+}
+template <> __device__ __forceinline__ void store_bf16<4>(__nv_bfloat16* p, const float (&v)[4]) {
+    uint2 u;
+    u.x = pack_bf16x2(v[0], v[1]);
+    u.y = pack_bf16x2(v[2], v[3]);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename TIn, int MAXV>
+__global__ void __launch_bounds__(LN_THREADS)
+ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
+               const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ beta,
+               int64_t rows, int D, float eps) {
+    constexpr int V = VecIO<TIn>::N;
+    const int64_t row = (int64_t)blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const int nvec = D / V;
+    const TIn* xr = x + row * D;
+    float v[MAXV][V];
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+        const int idx = lane + 32 * j;
+        if (idx < nvec) {
+            VecIO<TIn>::load(xr + idx * V, v[j]);
+#pragma unroll
+            for (int e = 0; e < V; ++e) sum += v[j][e];
+        }
+    }
+    const float mean = warp_sum(sum) / (float)D;
+    float sq = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+        const int idx = lane + 32 * j;
+        if (idx < nvec) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const float d = v[j][e] - mean;
+                sq += d * d;
+            }
+        }
+    }
+    const float var = warp_sum(sq) / (float)D;
+    const float rstd = rsqrtf(var + eps);
+    __nv_bfloat16* orow = out + row * D;
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) {
+        const int idx = lane + 32 * j;
+        if (idx < nvec) {
+            float o[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) o[e] = (v[j][e] - mean) * rstd;
+            if (gamma) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] *= __bfloat162float(gamma[idx * V + e]);
+            }
+            if (beta) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) o[e] += __bfloat162float(beta[idx * V + e]);
+            }
+            store_bf16<V>(orow + idx * V, o);
+        }
+    }
+}
+
+template <typename A>
+__device__ __forceinline__ A ld_param(const void* p, int dt, int64_t i) {
+    if (dt == DT_F32) return (A) static_cast<const float*>(p)[i];
+    if (dt == DT_BF16) return (A)__bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+    return (A) static_cast<const double*>(p)[i];
+}
+
+// Accumulation type: double for f64 input, float otherwise. gamma/beta of type gb_dt.
+template <typename TIn, typename TOut>
+__global__ void __launch_bounds__(LN_THREADS)
+ln_generic_kernel(const TIn* __restrict__ x, TOut* __restrict__ out, const void* __restrict__ gamma,
+                  const void* __restrict__ beta, int gb_dt, int64_t rows, int64_t D, double eps) {
+    using A = typename std::conditional<std::is_same<TIn, double>::value, double, float>::type;
+    const int64_t row = (int64_t)blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const TIn* xr = x + row * D;
+    A sum = 0;
+    for (int64_t j = lane; j < D; j += 32) sum += to_acc<A>(xr[j]);
+    const A mean = warp_sum(sum) / (A)D;
+    A sq = 0;
+    for (int64_t j = lane; j < D; j += 32) {
+        const A d = to_acc<A>(xr[j]) - mean;
+        sq += d * d;
+    }
+    const A var = warp_sum(sq) / (A)D;
+    const A denom = sqrt(var + (A)eps);
+    TOut* orow = out + row * D;
+    for (int64_t j = lane; j < D; j += 32) {
+        A o = (to_acc<A>(xr[j]) - mean) / denom;
+        if (gamma) o = ld_param<A>(gamma, gb_dt, j) * o;
+        if (beta) o = o + ld_param<A>(beta, gb_dt, j);
+        orow[j] = from_acc<TOut>(o);
+    }
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_generic(const void* x, void* out, const void* g, const void* b, int gb_dt,
+                           int64_t rows, int64_t D, double eps, cudaStream_t s) {
+    const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
+    ln_generic_kernel<TIn, TOut><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
+        static_cast<const TIn*>(x), static_cast<TOut*>(out), g, b, gb_dt, rows, D, eps);
+    return cudaGetLastError();
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt, const void* gamma,
+                             const void* beta, int gb_dt, int64_t rows, int64_t D, double eps,
+                             cudaStream_t s) {
+    if (rows <= 0 || D <= 0) return cudaSuccess;
+    const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    const bool vec_ok = D % 8 == 0 && D <= 2048 && aligned16(x) && aligned16(out);
+    const bool gb_bf16 = (!gamma && !beta) || gb_dt == DT_BF16;
+    if (out_dt == DT_BF16 && vec_ok && gb_bf16) {
+        auto g = static_cast<const __nv_bfloat16*>(gamma);
+        auto b = static_cast<const __nv_bfloat16*>(beta);
+        if (in_dt == DT_BF16) {
+            ln_fast_kernel<__nv_bfloat16, 8><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
+                static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(out), g, b, rows,
+                (int)D, (float)eps);
+            return cudaGetLastError();
+        }
+        if (in_dt == DT_F32) {
+            ln_fast_kernel<float, 16><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
+                static_cast<const float*>(x), static_cast<__nv_bfloat16*>(out), g, b, rows, (int)D,
+                (float)eps);
+            return cudaGetLastError();
+        }
+    }
+    if (in_dt == DT_BF16 && out_dt == DT_BF16)
+        return launch_generic<__nv_bfloat16, __nv_bfloat16>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
+    if (in_dt == DT_F32 && out_dt == DT_BF16)
+        return launch_generic<float, __nv_bfloat16>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
+    if (in_dt == DT_F32 && out_dt == DT_F32)
+        return launch_generic<float, float>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
+    if (in_dt == DT_F64 && out_dt == DT_F64)
+        return launch_generic<double, double>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
+    if (in_dt == DT_BF16 && out_dt == DT_F32)
+        return launch_generic<__nv_bfloat16, float>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vit

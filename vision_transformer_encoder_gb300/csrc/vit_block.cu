@@ -1,0 +1,576 @@
+// vit_block.cu -- the C ABI (include/vit_block.h) and the host-side dispatcher.
+//
+// vit_block enqueues, on the caller's stream, the seven steps of one pre-LN ViT
+// encoder block ("ViT Encoder Block" (crackedaicode): "Normalize before each
+// stage", "Multi-head attention", "Feed-forward stage"):
+//
+//   1 LN1        x   -> xn
+//   2 QKV GEMM   xn  -> qkv = xn @ [w_q | w_k | w_v]
+//   3 attention  qkv -> o   (per sequence and head, unmasked softmax)
+//   4 Wo GEMM    o   -> y   = x + o @ w_o
+//   5 LN2        y   -> yn
+//   6 W1 GEMM    yn  -> h   = GELU_tanh(yn @ w_mlp1 [+ b1])
+//   7 W2 GEMM    h   -> out = y + h @ w_mlp2 [+ b2]
+//
+// bf16 shapes with D and F multiples of 64 take the tensor-core kernels (GEMMs on
+// tcgen05/TMEM fed by TMA, attention on bf16 MMAs) with bf16 intermediates, except y,
+// which stays fp32 between the two residual adds. Every other case (fp32, fp64, odd
+// shapes) takes the CUDA-core kernels with intermediates in the accumulation type.
+// Scratch comes from a library-owned stream-ordered pool and is returned on the
+// same stream; nothing here synchronises unless VIT_DEBUG_SYNC=1.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "vit_block.h"
+
+namespace vit {
+namespace {
+
+__device__ uint32_t g_err_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    DeviceInfo info;
+    cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int64_t> g_launches{0};
+
+// ---- per-kernel timing -------------------------------------------------------
+enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_COUNT };
+const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
+                                         "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
+                                         "w2_gemm_residual"};
+struct Pending {
+    int kind;
+    cudaEvent_t a, b;
+};
+std::atomic<bool> g_timing{false};
+std::mutex g_tmu;
+std::vector<Pending> g_pending;
+double g_total_ms[K_COUNT];
+int64_t g_count[K_COUNT];
+
+bool debug_sync() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("VIT_DEBUG_SYNC");
+        v = (e && e[0] == '1') ? 1 : 0;
+    }
+    return v == 1;
+}
+
+int status_from(cudaError_t e) {
+    if (e == cudaSuccess) return VIT_OK;
+    if (e == cudaErrorMemoryAllocation) return VIT_ERR_NOMEM;
+    return VIT_ERR_CUDA;
+}
+
+// Sets up (once) and returns the state of the current device.
+int current_device(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VIT_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    if (!st.ready) {
+        DeviceInfo info;
+        info.device = dev;
+        if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return VIT_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return VIT_ERR_CUDA;
+        info.err_word = static_cast<uint32_t*>(p);
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return VIT_ERR_CUDA;
+        uint64_t thr = UINT64_MAX;  // keep freed scratch for the next call
+        cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+        st.info = info;
+        st.pool = pool;
+        st.ready = true;
+    }
+    *out = &st;
+    return VIT_OK;
+}
+
+// Runs one kernel launcher; counts it and, with timing on, brackets it with events.
+template <class F>
+cudaError_t run(int kind, cudaStream_t s, F&& launch) {
+    if (!g_timing.load(std::memory_order_relaxed)) {
+        cudaError_t e = launch();
+        if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+        return e;
+    }
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return cudaErrorUnknown;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+        cudaEventDestroy(a);
+        return cudaErrorUnknown;
+    }
+    cudaEventRecord(a, s);
+    cudaError_t e = launch();
+    cudaEventRecord(b, s);
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    std::lock_guard<std::mutex> lk(g_tmu);
+    g_pending.push_back({kind, a, b});
+    return e;
+}
+
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+struct BlockArgs {
+    const void *x, *w_q, *w_k, *w_v, *w_o, *w1, *w2;
+    const void *ln1_g, *ln1_b, *ln2_g, *ln2_b, *b1, *b2;
+    int64_t N, T, D, F, H;
+    double eps;
+    int dt;
+    void* out;
+};
+
+int validate(const BlockArgs& a) {
+    if (a.dt != DT_F32 && a.dt != DT_BF16 && a.dt != DT_F64) return VIT_ERR_DTYPE;
+    if (!a.x || !a.w_q || !a.w_k || !a.w_v || !a.w_o || !a.w1 || !a.w2 || !a.out) return VIT_ERR_ARG;
+    if (a.N <= 0 || a.T <= 0 || a.D <= 0 || a.F <= 0 || a.H <= 0 || a.D % a.H != 0) return VIT_ERR_ARG;
+    const int64_t lim = (int64_t)1 << 40;
+    if (a.N > lim / a.T || a.D > (1 << 20) || a.F > (1 << 22)) return VIT_ERR_ARG;
+    const size_t es = dt_size(a.dt);
+    const size_t xb = (size_t)(a.N * a.T * a.D) * es;
+    const size_t dd = (size_t)(a.D * a.D) * es, df = (size_t)(a.D * a.F) * es;
+    const void* in[] = {a.x, a.w_q, a.w_k, a.w_v, a.w_o, a.w1, a.w2,
+                        a.ln1_g, a.ln1_b, a.ln2_g, a.ln2_b, a.b1, a.b2};
+    const size_t nb[] = {xb, dd, dd, dd, dd, df, df,
+                         (size_t)a.D * es, (size_t)a.D * es, (size_t)a.D * es, (size_t)a.D * es,
+                         (size_t)a.F * es, (size_t)a.D * es};
+    for (int i = 0; i < 13; ++i)
+        if (overlaps(a.out, xb, in[i], nb[i])) return VIT_ERR_ARG;
+    return VIT_OK;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool fast_path_ok(const BlockArgs& a) {
+    if (a.dt != DT_BF16) return false;
+    if (a.D % 64 != 0 || a.F % 64 != 0 || a.D > 2048) return false;
+    if (a.N * a.T > 0x7fffffff) return false;
+    const void* ps[] = {a.x, a.w_q, a.w_k, a.w_v, a.w_o, a.w1, a.w2, a.out, a.b1, a.b2};
+    for (const void* p : ps)
+        if (p && !al16(p)) return false;
+    return true;
+}
+
+int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+    const int64_t M = a.N * a.T, D = a.D, F = a.F;
+    const bool fast = fast_path_ok(a);
+    const int acc_dt = fast ? DT_BF16 : (a.dt == DT_F64 ? DT_F64 : DT_F32);
+    const size_t ea = dt_size(acc_dt);
+    // scratch: buf (xn, then o, then yn) | qkv | y | h
+    const size_t sz_buf = round_up((size_t)(M * D) * ea, 256);
+    const size_t sz_qkv = round_up((size_t)(M * 3 * D) * ea, 256);
+    const size_t sz_y = round_up((size_t)(M * D) * (fast ? 4 : ea), 256);
+    const size_t sz_h = round_up((size_t)(M * F) * ea, 256);
+    const size_t total = sz_buf + sz_qkv + sz_y + sz_h;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    void* buf = base;
+    void* qkv = base + sz_buf;
+    void* y = base + sz_buf + sz_qkv;
+    void* h = base + sz_buf + sz_qkv + sz_y;
+
+    auto step = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+    };
+    if (fast) {
+        step(run(K_LN1, s, [&] {
+            return launch_layernorm(a.x, DT_BF16, buf, DT_BF16, a.ln1_g, a.ln1_b, DT_BF16, M, D,
+                                    a.eps, s);
+        }));
+        TcGemmDesc g;
+        std::memset(&g, 0, sizeof(g));
+        g.a = buf; g.lda = D;
+        g.w[0] = a.w_q; g.w[1] = a.w_k; g.w[2] = a.w_v; g.n_w = 3; g.n_per_w = D;
+        g.M = M; g.N = 3 * D; g.K = D;
+        g.epi = TC_EPI_STORE;
+        g.out = qkv; g.ldo = 3 * D; g.out_f32 = false;
+        const bool tc = tc_gemm_supported(g);
+        step(run(K_QKV, s, [&] {
+            if (tc) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{buf, DT_BF16, D, a.w_q, DT_BF16, D, nullptr, 0, nullptr, 0, 0,
+                            qkv, DT_BF16, 3 * D, M, D, D, TC_EPI_STORE};
+            cudaError_t r = launch_gemm_simt(sd, s);
+            sd.w = a.w_k; sd.out = static_cast<__nv_bfloat16*>(qkv) + D;
+            if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
+            sd.w = a.w_v; sd.out = static_cast<__nv_bfloat16*>(qkv) + 2 * D;
+            if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
+            return r;
+        }));
+        step(run(K_ATTN, s, [&] {
+            if (attention_fast_supported(D, a.H, qkv, buf))
+                return launch_attention_fast(qkv, buf, a.N, a.T, D, a.H, s);
+            return launch_attention_simt(qkv, DT_BF16, buf, a.N, a.T, D, a.H, s);
+        }));
+        g.a = buf; g.w[0] = a.w_o; g.n_w = 1; g.n_per_w = D; g.N = D; g.K = D;
+        g.epi = TC_EPI_RESID; g.residual = a.x; g.ldr = D; g.residual_f32 = false;
+        g.out = y; g.ldo = D; g.out_f32 = true;
+        step(run(K_WO, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{buf, DT_BF16, D, a.w_o, DT_BF16, D, nullptr, 0, a.x, DT_BF16, D,
+                            y, DT_F32, D, M, D, D, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(run(K_LN2, s, [&] {
+            return launch_layernorm(y, DT_F32, buf, DT_BF16, a.ln2_g, a.ln2_b, DT_BF16, M, D, a.eps, s);
+        }));
+        g.a = buf; g.w[0] = a.w1; g.n_w = 1; g.n_per_w = F; g.N = F; g.K = D;
+        g.epi = TC_EPI_GELU; g.bias = a.b1; g.residual = nullptr;
+        g.out = h; g.ldo = F; g.out_f32 = false;
+        step(run(K_W1, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{buf, DT_BF16, D, a.w1, DT_BF16, F, a.b1, DT_BF16, nullptr, 0, 0,
+                            h, DT_BF16, F, M, F, D, TC_EPI_GELU};
+            return launch_gemm_simt(sd, s);
+        }));
+        g.a = h; g.lda = F; g.w[0] = a.w2; g.n_w = 1; g.n_per_w = D; g.N = D; g.K = F;
+        g.epi = TC_EPI_RESID; g.bias = a.b2; g.residual = y; g.ldr = D; g.residual_f32 = true;
+        g.out = a.out; g.ldo = D; g.out_f32 = false;
+        step(run(K_W2, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{h, DT_BF16, F, a.w2, DT_BF16, D, a.b2, DT_BF16, y, DT_F32, D,
+                            a.out, DT_BF16, D, M, D, F, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+    } else {
+        const int dt = a.dt;
+        step(run(K_LN1, s, [&] {
+            return launch_layernorm(a.x, dt, buf, acc_dt, a.ln1_g, a.ln1_b, dt, M, D, a.eps, s);
+        }));
+        SimtGemmDesc sd{buf, acc_dt, D, a.w_q, dt, D, nullptr, 0, nullptr, 0, 0, qkv, acc_dt, 3 * D,
+                        M, D, D, TC_EPI_STORE};
+        step(run(K_QKV, s, [&] {
+            cudaError_t r = launch_gemm_simt(sd, s);
+            SimtGemmDesc k2 = sd;
+            k2.w = a.w_k;
+            k2.out = static_cast<uint8_t*>(qkv) + D * ea;
+            if (r == cudaSuccess) r = launch_gemm_simt(k2, s);
+            k2.w = a.w_v;
+            k2.out = static_cast<uint8_t*>(qkv) + 2 * D * ea;
+            if (r == cudaSuccess) r = launch_gemm_simt(k2, s);
+            return r;
+        }));
+        step(run(K_ATTN, s, [&] { return launch_attention_simt(qkv, acc_dt, buf, a.N, a.T, D, a.H, s); }));
+        step(run(K_WO, s, [&] {
+            SimtGemmDesc w{buf, acc_dt, D, a.w_o, dt, D, nullptr, 0, a.x, dt, D, y, acc_dt, D,
+                           M, D, D, TC_EPI_RESID};
+            return launch_gemm_simt(w, s);
+        }));
+        step(run(K_LN2, s, [&] {
+            return launch_layernorm(y, acc_dt, buf, acc_dt, a.ln2_g, a.ln2_b, dt, M, D, a.eps, s);
+        }));
+        step(run(K_W1, s, [&] {
+            SimtGemmDesc w{buf, acc_dt, D, a.w1, dt, F, a.b1, dt, nullptr, 0, 0, h, acc_dt, F,
+                           M, F, D, TC_EPI_GELU};
+            return launch_gemm_simt(w, s);
+        }));
+        step(run(K_W2, s, [&] {
+            SimtGemmDesc w{h, acc_dt, F, a.w2, dt, D, a.b2, dt, y, acc_dt, D, a.out, dt, D,
+                           M, D, F, TC_EPI_RESID};
+            return launch_gemm_simt(w, s);
+        }));
+    }
+    cudaError_t fe = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = fe;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+        uint32_t w = 0;
+        if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
+        if (w) return VIT_ERR_TIMEOUT;
+    }
+    return VIT_OK;
+}
+
+}  // namespace
+}  // namespace vit
+
+using namespace vit;
+
+extern "C" {
+
+int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_v, const void* w_o,
+                 const void* w_mlp1, const void* w_mlp2, const void* ln1_g, const void* ln1_b,
+                 const void* ln2_g, const void* ln2_b, const void* b1, const void* b2, int64_t N,
+                 int64_t T, int64_t D, int64_t F, int64_t H, double eps, int dtype, void* out,
+                 void* stream) {
+    BlockArgs a{x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, ln1_g, ln1_b, ln2_g, ln2_b, b1, b2,
+                N, T, D, F, H, eps, dtype, out};
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    DeviceState* st = nullptr;
+    rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    return enqueue_block(a, st->info, static_cast<cudaStream_t>(stream));
+}
+
+int vit_block(const void* x, const void* w_q, const void* w_k, const void* w_v, const void* w_o,
+              const void* w_mlp1, const void* w_mlp2, int64_t N, int64_t T, int64_t D, int64_t F,
+              int64_t H, double eps, int dtype, void* out, void* stream) {
+    return vit_block_ex(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, nullptr, nullptr, nullptr, nullptr,
+                        nullptr, nullptr, N, T, D, F, H, eps, dtype, out, stream);
+}
+
+int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_host,
+                   const void* w_v_host, const void* w_o_host, const void* w_mlp1_host,
+                   const void* w_mlp2_host, const void* ln1_g_host, const void* ln1_b_host,
+                   const void* ln2_g_host, const void* ln2_b_host, const void* b1_host,
+                   const void* b2_host, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+                   double eps, int dtype, void* out_host, void* stream) {
+    BlockArgs a{x_host, w_q_host, w_k_host, w_v_host, w_o_host, w_mlp1_host, w_mlp2_host,
+                ln1_g_host, ln1_b_host, ln2_g_host, ln2_b_host, b1_host, b2_host,
+                N, T, D, F, H, eps, dtype, out_host};
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    DeviceState* st = nullptr;
+    rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = dt_size(dtype);
+    const size_t xb = (size_t)(N * T * D) * es;
+    const size_t sizes[14] = {xb, (size_t)(D * D) * es, (size_t)(D * D) * es, (size_t)(D * D) * es,
+                              (size_t)(D * D) * es, (size_t)(D * F) * es, (size_t)(D * F) * es,
+                              (size_t)D * es, (size_t)D * es, (size_t)D * es, (size_t)D * es,
+                              (size_t)F * es, (size_t)D * es, xb};
+    const void* src[13] = {x_host, w_q_host, w_k_host, w_v_host, w_o_host, w_mlp1_host, w_mlp2_host,
+                           ln1_g_host, ln1_b_host, ln2_g_host, ln2_b_host, b1_host, b2_host};
+    size_t off[14], total = 0;
+    for (int i = 0; i < 14; ++i) {
+        off[i] = total;
+        if (i < 13 && !src[i]) continue;
+        total += round_up(sizes[i], 256);
+    }
+    void* dmem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&dmem, total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    uint8_t* base = static_cast<uint8_t*>(dmem);
+    const void* dev_in[13];
+    for (int i = 0; i < 13; ++i) {
+        dev_in[i] = src[i] ? base + off[i] : nullptr;
+        if (src[i] && e == cudaSuccess)
+            e = cudaMemcpyAsync(base + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, s);
+    }
+    void* dev_out = base + off[13];
+    if (e == cudaSuccess) {
+        BlockArgs d{dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], dev_in[6],
+                    dev_in[7], dev_in[8], dev_in[9], dev_in[10], dev_in[11], dev_in[12],
+                    N, T, D, F, H, eps, dtype, dev_out};
+        rc = enqueue_block(d, st->info, s);
+        if (rc == VIT_OK) e = cudaMemcpyAsync(out_host, dev_out, xb, cudaMemcpyDeviceToHost, s);
+    }
+    cudaError_t fe = cudaFreeAsync(dmem, s);
+    cudaError_t se = cudaStreamSynchronize(s);
+    if (rc != VIT_OK) return rc;
+    if (e == cudaSuccess) e = fe;
+    if (e == cudaSuccess) e = se;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    return VIT_OK;
+}
+
+int vit_layernorm(const void* x, int64_t rows, int64_t D, double eps, const void* gamma,
+                  const void* beta, int in_dtype, void* out, int out_dtype, void* stream) {
+    if (!x || !out || rows <= 0 || D <= 0) return VIT_ERR_ARG;
+    const bool ok = (in_dtype == DT_BF16 && out_dtype == DT_BF16) ||
+                    (in_dtype == DT_F32 && (out_dtype == DT_BF16 || out_dtype == DT_F32)) ||
+                    (in_dtype == DT_F64 && out_dtype == DT_F64);
+    if (!ok) return VIT_ERR_DTYPE;
+    if (overlaps(out, (size_t)(rows * D) * dt_size(out_dtype), x, (size_t)(rows * D) * dt_size(in_dtype)))
+        return VIT_ERR_ARG;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = run(K_LN1, s, [&] {
+        return launch_layernorm(x, in_dtype, out, out_dtype, gamma, beta, out_dtype, rows, D, eps, s);
+    });
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    return VIT_OK;
+}
+
+int vit_linear(const void* a, const void* w, const void* bias, const void* residual, int64_t M,
+               int64_t K, int64_t N, int epilogue, int dtype, int residual_dtype, void* out,
+               int out_dtype, void* stream) {
+    if (!a || !w || !out || M <= 0 || K <= 0 || N <= 0) return VIT_ERR_ARG;
+    if (epilogue < VIT_EPI_STORE || epilogue > VIT_EPI_RESIDUAL) return VIT_ERR_ARG;
+    if ((epilogue == VIT_EPI_RESIDUAL) != (residual != nullptr)) return VIT_ERR_ARG;
+    if (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F64) return VIT_ERR_DTYPE;
+    if (dtype == DT_BF16) {
+        if (out_dtype != DT_BF16 && out_dtype != DT_F32) return VIT_ERR_DTYPE;
+        if (residual && residual_dtype != DT_BF16 && residual_dtype != DT_F32) return VIT_ERR_DTYPE;
+    } else {
+        if (out_dtype != dtype || (residual && residual_dtype != dtype)) return VIT_ERR_DTYPE;
+    }
+    const size_t ob = (size_t)(M * N) * dt_size(out_dtype);
+    if (overlaps(out, ob, a, (size_t)(M * K) * dt_size(dtype)) ||
+        overlaps(out, ob, w, (size_t)(K * N) * dt_size(dtype)) ||
+        overlaps(out, ob, bias, (size_t)N * dt_size(dtype)))
+        return VIT_ERR_ARG;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int kind = epilogue == VIT_EPI_GELU ? K_W1 : (epilogue == VIT_EPI_RESIDUAL ? K_W2 : K_QKV);
+    cudaError_t e = run(kind, s, [&] {
+        if (dtype == DT_BF16) {
+            TcGemmDesc g;
+            std::memset(&g, 0, sizeof(g));
+            g.a = a; g.lda = K; g.w[0] = w; g.n_w = 1; g.n_per_w = N; g.M = M; g.N = N; g.K = K;
+            g.epi = epilogue; g.bias = bias; g.residual = residual; g.ldr = N;
+            g.residual_f32 = residual_dtype == DT_F32; g.out = out; g.ldo = N;
+            g.out_f32 = out_dtype == DT_F32;
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, st->info, s);
+        }
+        SimtGemmDesc sd{a, dtype, K, w, dtype, N, bias, dtype, residual, residual_dtype, N,
+                        out, out_dtype, N, M, N, K, epilogue};
+        return launch_gemm_simt(sd, s);
+    });
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    return VIT_OK;
+}
+
+int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, int dtype, void* o,
+                  void* stream) {
+    if (!qkv || !o || N <= 0 || T <= 0 || D <= 0 || H <= 0 || D % H != 0) return VIT_ERR_ARG;
+    if (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F64) return VIT_ERR_DTYPE;
+    const size_t es = dt_size(dtype);
+    if (overlaps(o, (size_t)(N * T * D) * es, qkv, (size_t)(N * T * 3 * D) * es)) return VIT_ERR_ARG;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = run(K_ATTN, s, [&] {
+        if (dtype == DT_BF16 && attention_fast_supported(D, H, qkv, o) && (D * 2) % 16 == 0)
+            return launch_attention_fast(qkv, o, N, T, D, H, s);
+        return launch_attention_simt(qkv, dtype, o, N, T, D, H, s);
+    });
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    return VIT_OK;
+}
+
+const char* vit_status_string(int status) {
+    switch (status) {
+        case VIT_OK: return "success";
+        case VIT_ERR_ARG: return "invalid argument (null pointer, size, H not dividing D, or aliasing)";
+        case VIT_ERR_DTYPE: return "unsupported dtype";
+        case VIT_ERR_CUDA: return "CUDA call or kernel launch failed";
+        case VIT_ERR_TIMEOUT: return "a device-side wait timed out";
+        case VIT_ERR_NOMEM: return "scratch allocation failed";
+        case VIT_ERR_UNSUPPORTED: return "shape or alignment not supported by this entry point";
+    }
+    return "unknown status";
+}
+
+const char* vit_version(void) { return "vit_block 0.1 (sm_103a)"; }
+
+int64_t vit_launch_count(void) { return g_launches.load(); }
+
+int vit_device_error(uint32_t* word) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return VIT_ERR_CUDA;
+    uint32_t w = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return VIT_ERR_CUDA;
+    if (word) *word = w;
+    return w ? VIT_ERR_TIMEOUT : VIT_OK;
+}
+
+int vit_timing_enable(int enable) {
+    g_timing.store(enable != 0);
+    return VIT_OK;
+}
+
+int vit_timing_collect(void) {
+    std::vector<Pending> p;
+    {
+        std::lock_guard<std::mutex> lk(g_tmu);
+        p.swap(g_pending);
+    }
+    int rc = VIT_OK;
+    for (const Pending& q : p) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(q.b) != cudaSuccess || cudaEventElapsedTime(&ms, q.a, q.b) != cudaSuccess)
+            rc = VIT_ERR_CUDA;
+        else {
+            g_total_ms[q.kind] += ms;
+            g_count[q.kind] += 1;
+        }
+        cudaEventDestroy(q.a);
+        cudaEventDestroy(q.b);
+    }
+    return rc;
+}
+
+int vit_timing_kernels(void) { return K_COUNT; }
+
+int vit_timing_read(int k, double* total_ms, int64_t* launches, const char** name) {
+    if (k < 0 || k >= K_COUNT) return VIT_ERR_ARG;
+    if (total_ms) *total_ms = g_total_ms[k];
+    if (launches) *launches = g_count[k];
+    if (name) *name = kKernNames[k];
+    return VIT_OK;
+}
+
+int vit_timing_reset(void) {
+    for (int k = 0; k < K_COUNT; ++k) {
+        g_total_ms[k] = 0;
+        g_count[k] = 0;
+    }
+    return VIT_OK;
+}
+
+}  // extern "C"
