@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Throughput of the pre-LN ViT encoder block forward on GB300.
+
+One step = one vit_block call over one batch: every stage of the block (LN1, QKV
+GEMM, attention, Wo GEMM + residual, LN2, W1 GEMM + GELU, W2 GEMM + residual) on
+N sequences of the chosen block shape. Default workload: the ViT-B/16-shaped block
+(N 256, T 197, D 768, H 12, F 3072) in bf16 with fp32 accumulation.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config vit_b16]
+  python bench.py --impl reference ...   # the float64 CPU oracle, as the reference arm
+
+Prints one JSON line (rank 0). For N > 1 (torchrun, one process per GPU) each rank
+runs the whole workload on its own GPU with its own seed (independent sequences, no
+collective on the data path); value = all ranks' tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from vision_transformer_encoder_gb300 import api  # noqa: E402
+from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs  # noqa: E402
+
+METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf16, 1 GPU"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 512 << 20  # > 126 MB L2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def workload_name(name, c):
+    label = {"vit_b16": "ViT-B/16", "vit_ti16": "ViT-Ti/16", "vit_l16_384": "ViT-L/16@384",
+             "vit_h14_448": "ViT-H/14@448", "tiny": "tiny"}[name]
+    return ("%s-shaped pre-LN encoder block forward: N=%d sequences x T=%d tokens, D=%d, H=%d "
+            "(d_h=%d), F=%d, eps=%g" % (label, c["N"], c["T"], c["D"], c["H"], c["D"] // c["H"],
+                                        c["F"], c["eps"]))
+
+
+def flops_per_step(c):
+    N, T, D, F = c["N"], c["T"], c["D"], c["F"]
+    return 2 * N * T * (4 * D * D + 2 * D * F) + 4 * N * T * T * D
+
+
+def kernel_work(c):
+    """Algorithmic work per launch of each kernel: (bound, amount, unit)."""
+    N, T, D, F = c["N"], c["T"], c["D"], c["F"]
+    M = N * T
+    return {
+        "ln1": ("hbm", M * D * (2 + 2), "bytes"),          # read x bf16, write xn bf16
+        "qkv_gemm": ("tensor", 2 * M * D * 3 * D, "flops"),
+        "attention": ("tensor", 4 * N * T * T * D, "flops"),
+        "wo_gemm_residual": ("tensor", 2 * M * D * D, "flops"),
+        "ln2": ("hbm", M * D * (4 + 2), "bytes"),          # read y fp32, write yn bf16
+        "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),
+        "w2_gemm_residual": ("tensor", 2 * M * F * D, "flops"),
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic():
+    """DRAM bytes per launch from a committed ncu summary, keyed by kernel; an entry is
+    used only while the source file it was measured on is unchanged (same sha256)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic_vit_b16.txt")
+    out = {}
+    if not os.path.exists(p):
+        return out
+    for line in open(p):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if len(parts) != 4:
+            continue
+        kern, nbytes, src, sha = parts
+        path = os.path.join(ROOT, src)
+        if os.path.exists(path) and hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] == sha:
+            out[kern] = int(float(nbytes))
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 20 ms in the background."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        window = [r for r in rows if t0 <= r[0] <= t1]
+        note = "sampled every 20 ms during the timed region"
+        if len(window) < 3:
+            window = rows
+            note = "timed region shorter than 3 samples: warm-up and timed region together"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window),
+                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+                "samples": len(window), "note": note}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def reduce_max(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_baseline(name, c):
+    """The float64 oracle on the host cores, on a bounded sample of the workload."""
+    import oracle
+    cores = oracle.max_threads()
+    n = max(1, min(cores, c["N"]))
+    inp = make_config_inputs(name, dtype=torch.bfloat16, N=n)
+    t = time.perf_counter()
+    oracle.vit_block(inp.x, *inp.weights(), c["H"], c["eps"], nthreads=cores)
+    dt = time.perf_counter() - t
+    return {"value": n * c["T"] / dt, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
+            "sample": "%d of the %d sequences (%d tokens each), float64 straight loops, OpenMP "
+                      "over sequences, %.1f s wall" % (n, c["N"], c["T"], dt)}
+
+
+def run_reference(args):
+    """Reference arm: the float64 CPU oracle as it stands, on the host cores."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import oracle
+    name = args.config
+    c = CONFIGS[name]
+    cores = oracle.max_threads()
+    K, W = args.steps, args.warmup
+    # one sequence per host core: a step costs about one sequence's time on one core
+    n = max(1, min(cores, c["N"]))
+    inp = make_config_inputs(name, dtype=torch.bfloat16, N=n)
+    x = inp.x[:n]
+    ws = inp.weights()
+    for _ in range(W):
+        oracle.vit_block(x, *ws, c["H"], c["eps"], nthreads=cores)
+    times = []
+    for _ in range(K):
+        t = time.perf_counter()
+        oracle.vit_block(x, *ws, c["H"], c["eps"], nthreads=cores)
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = K * n * c["T"] / total
+    sample = ("each step: %d of the %d sequences (%d tokens each) of the workload, float64 "
+              "straight loops, OpenMP over sequences" % (n, c["N"], c["T"]))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": K, "warmup": W, "ms_per_step": 1e3 * total / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_name(name, c), "tokens_per_step": n * c["T"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(cores, n), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="vit_b16", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10,
+                    help="steps of the host-buffer end-to-end measurement (0: skip it)")
+    ap.add_argument("--n-seq", type=int, default=None,
+                    help="override the number of sequences N (profiling of a smaller case)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local = dist_setup()
+    name = args.config
+    c = dict(CONFIGS[name])
+    if args.n_seq:
+        c["N"] = args.n_seq
+    H, eps = c["H"], c["eps"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    inp = make_config_inputs(name, seed=rank, dtype=torch.bfloat16, N=c["N"])
+    d = inp.to(device=dev)
+    out = torch.empty_like(d.x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.vit_block(d.x, *d.weights(), H, eps, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    gpu_id = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[local] \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else None
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.2)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    api.timing_reset()
+    api.timing_enable(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = api.launch_count()
+    t0 = time.time()
+    for k in range(K):
+        flush.zero_()                 # evict L2 between steps (outside the events)
+        starts[k].record(stream)
+        step()
+        ends[k].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    launches = api.launch_count() - launches0
+    api.timing_enable(False)
+    time.sleep(0.1)
+    sampler.stop()
+    per_kernel = api.timing_collect()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = reduce_max(sum(step_ms), world)
+    tokens = c["N"] * c["T"]
+    value = world * tokens * K / (total_ms / 1e3)
+    ms_per_step = total_ms / K
+
+    # end to end through the host-buffer entry point (pinned host memory)
+    e2e = None
+    if args.e2e_steps > 0:
+        pinned = [t.pin_memory() for t in [inp.x] + inp.weights()]
+        hout = torch.empty_like(pinned[0]).pin_memory()
+        api.vit_block_host(*pinned, H, eps, out=hout, device=dev.index)
+        barrier(world)
+        te = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            api.vit_block_host(*pinned, H, eps, out=hout, device=dev.index)
+        e2e_s = reduce_max(time.perf_counter() - te, world)
+        h2d = sum(t.numel() * t.element_size() for t in pinned)
+        d2h = hout.numel() * hout.element_size()
+        e2e = {"value": world * tokens * args.e2e_steps / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": args.e2e_steps, "api": "vit_block_host (C ABI, pinned host buffers)"}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    work = kernel_work(c)
+    dom = max(per_kernel, key=lambda k: per_kernel[k][0])
+    kms, kn = per_kernel[dom]
+    bound, amount, _unit = work[dom]
+    avg_s = kms / kn / 1e3
+    traffic = load_traffic().get(dom)
+    if bound == "tensor":
+        peak = peaks["bf16_tflops"]
+        achieved = amount / avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    else:
+        peak = peaks["hbm_gbs"]
+        achieved = amount / avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak}
+    roof.update({"traffic": traffic, "kernel": dom, "launches": kn,
+                 "avg_launch_us": avg_s * 1e6,
+                 "algorithmic_per_launch": amount,
+                 "peak_source": "%s (%s)" % (peak_src, "bf16 burst" if bound == "tensor" else "copy"),
+                 "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                                       if bound == "tensor" else None)})
+    step_tflops = flops_per_step(c) / (ms_per_step / 1e3) / 1e12
+    kernels = {k: {"avg_us": 1e3 * v[0] / v[1] if v[1] else None, "launches": v[1],
+                   "share": v[0] / sum(x[0] for x in per_kernel.values())}
+               for k, v in per_kernel.items()}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(name, c),
+                   "tokens_per_step_per_gpu": tokens,
+                   "inputs": "seeded synthetic: x ~ N(0,1), weights ~ N(0, 1/fan_in), bf16",
+                   "l2": "512 MiB written between timed steps (flush); per-step working set "
+                         "about 0.9 GB, larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "tflops": step_tflops,
+        "frac_of_peak": step_tflops / peaks["bf16_tflops"],
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "e2e": e2e,
+        "clocks": sampler.summary(t0, t1),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(name, c)
+    if args.n_seq:
+        line["config"]["note"] = "N overridden on the command line (not the headline workload)"
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -99,6 +100,41 @@ __device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
     if (err) atomicOr(err, bit);
+}
+
+
+// Epilogue of one 128 x 256 accumulator: this thread owns output row `row` and reads
+// its 256 fp32 columns from TMEM (lane row, columns from t_row) 32 at a time.
+template <int EPI, typename OutT, typename ResT>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, int row, int n0) {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
+        ptx::tmem_ld_wait();
+        const int col = n0 + c * 32;
+        if (row < p.M && col < p.N) {
+            float val[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
+            if (p.bias) {
+                float b[32];
+                load32(p.bias + col, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] += b[j];
+            }
+            if (EPI == TC_EPI_GELU) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
+            } else if (EPI == TC_EPI_RESID) {
+                float rv[32];
+                load32(reinterpret_cast<const ResT*>(p.residual) + (int64_t)row * p.ldr + col, rv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] += rv[j];
+            }
+            store32(reinterpret_cast<OutT*>(p.out) + (int64_t)row * p.ldo + col, val);
+        }
+    }
 }
 
 template <int EPI, typename OutT, typename ResT>
@@ -261,34 +297,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int n0 = (tile % n_tiles) * BN;
             const int row = m0 + quarter * 32 + lane;
             const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
-                ptx::tmem_ld_wait();
-                const int col = n0 + c * 32;
-                if (row < p.M && col < p.N) {
-                    float val[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
-                    if (p.bias) {
-                        float b[32];
-                        load32(p.bias + col, b);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) val[j] += b[j];
-                    }
-                    if (EPI == TC_EPI_GELU) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
-                    } else if (EPI == TC_EPI_RESID) {
-                        float rv[32];
-                        load32(reinterpret_cast<const ResT*>(p.residual) + (int64_t)row * p.ldr + col, rv);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) val[j] += rv[j];
-                    }
-                    store32(reinterpret_cast<OutT*>(p.out) + (int64_t)row * p.ldo + col, val);
-                }
-            }
+            epilogue_tile<EPI, OutT, ResT>(p, t_row, row, n0);
             ptx::tc_fence_before();
             ptx::mbar_arrive(tempty + acc);
         }
@@ -298,6 +307,200 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+
+// ------------------------------------------------------------------ CTA-pair kernel
+// Two CTAs of a cluster (ranks 0 and 1, on a TPC's two SMs) compute one 256 x 256 output
+// tile with tcgen05.mma.cta_group::2 (M 256 = 128 rows per CTA, N 256): each CTA loads
+// its own 128 rows of A and its own half (128 columns) of the weight tile, 32 KB per
+// 64-deep k block, so each SM moves two thirds of the operand bytes per flop that the
+// single-CTA 128 x 256 tile needs, and six stages fit in shared memory.
+//   rank 0 (leader): arms the stage barrier for both CTAs' bytes, issues the pair MMAs
+//   from one thread and multicasts its commits (ring slot free / accumulator ready) to
+//   both CTAs. Both ranks: a TMA warp for their own operand halves (completion counted on
+//   the leader's barrier), and four epilogue warps reading their own TMEM rows; the
+//   epilogue threads of both CTAs release an accumulator on the leader's barrier.
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
+constexpr int P_B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's 128 weight columns
+constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024;
+
+template <int EPI, typename OutT, typename ResT>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                    const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + P_STAGES * P_A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint64_t* empty = full + P_STAGES;
+    uint64_t* tfull = empty + P_STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int m_tiles = (p.M + 2 * BM - 1) / (2 * BM);
+    const int n_tiles = (p.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int kblocks = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P_STAGES; ++s) {
+            ptx::mbar_init(full + s, 1);
+            ptx::mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull + a, 1);
+            ptx::mbar_init(tempty + a, 2 * 128);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB0);
+        if (p.n_w > 1) ptx::prefetch_tensormap(&tmB1);
+        if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    ptx::cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // -------------------------------------------- TMA producer (both ranks)
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(full), 0);  // leader's
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+                const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
+                const int n0 = (tile % n_tiles) * BN + (int)rank * (BN / 2);
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % P_STAGES, u = it / P_STAGES;
+                    if (!ptx::mbar_wait_bounded(empty + s, (u & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(full + s, 2 * P_STAGE_BYTES);
+                    const uint32_t fb = full0 + s * 8;
+                    ptx::tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, fb, kb * BK, m0);
+#pragma unroll
+                    for (int j = 0; j < BN / 128; ++j) {
+                        const int col = n0 + 64 * j;
+                        int wi = col / p.n_per_w;
+                        if (wi > p.n_w - 1) wi = p.n_w - 1;  // past N: zero-filled box
+                        const int lc = col - wi * p.n_per_w;
+                        const CUtensorMap* tb = wi == 0 ? &tmB0 : (wi == 1 ? &tmB1 : &tmB2);
+                        ptx::tma_load_2d_pair(sB + s * P_B_BYTES + j * B_BOX_BYTES, tb, fb, lc,
+                                              kb * BK);
+                    }
+                }
+            }
+            if (!ok) {
+                set_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
+                *abort_flag = 1;
+            }
+            if (rank == 0) {
+                // both CTAs' copies complete on these barriers: let them land
+                for (uint32_t s = 0; s < P_STAGES; ++s) {
+                    if (it > s) {
+                        const uint32_t u_last = (it - 1 - s) / P_STAGES;
+                        if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
+                            set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // -------------------------------------------- pair MMA issuer (leader)
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(2 * BM, BN, false, true);
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+                const int acc = local & 1;
+                const uint32_t v = (uint32_t)(local >> 1);
+                if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % P_STAGES, u = it / P_STAGES;
+                    if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_base = ptx::smem_addr(sA + s * P_A_BYTES);
+                    const uint32_t b_base = ptx::smem_addr(sB + s * P_B_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t adesc = ptx::smem_desc_sw128(a_base + k * 32, 16, 1024);
+                        const uint64_t bdesc =
+                            ptx::smem_desc_sw128(b_base + k * 2048, B_BOX_BYTES, 1024);
+                        ptx::mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+                    }
+                    ptx::mma_commit_pair_mc(empty + s, 0x3);
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair_mc(tfull + acc, 0x3);
+            }
+            if (!ok) {
+                set_error(p.err, ERRBIT_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            ptx::mma_commit_pair(done);
+            if (!ptx::mbar_wait_bounded(done, 0, nullptr)) set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else {
+        // ---------------------------------------------- epilogue warps 2..5 (both ranks)
+        const int quarter = warp & 3;
+        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);  // leader's
+        int local = 0;
+        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+            const int acc = local & 1;
+            const uint32_t v = (uint32_t)(local >> 1);
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(tfull + acc, v & 1, abort_flag));
+            if (!ok) {
+                if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
+            const int n0 = (tile % n_tiles) * BN;
+            const int row = m0 + quarter * 32 + lane;
+            const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+            epilogue_tile<EPI, OutT, ResT>(p, t_row, row, n0);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive_cluster(tempty0 + acc * 8);
+        }
+    }
+
+    __syncthreads();
+    ptx::cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -350,6 +553,37 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params
     return cudaGetLastError();
 }
 
+template <int EPI, typename OutT, typename ResT>
+cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const Params& p, int grid,
+                             cudaStream_t s) {
+    auto k = gemm_tc_pair_kernel<EPI, OutT, ResT>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    k<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], p);
+    return cudaGetLastError();
+}
+
+template <int EPI, typename OutT, typename ResT>
+cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const Params& p,
+                       int grid, cudaStream_t s) {
+    return pair ? launch_inst_pair<EPI, OutT, ResT>(a, b, p, grid, s)
+                : launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
+}
+
+// The CTA-pair kernel is the default; VIT_GEMM_PAIR=0 selects the single-CTA kernel.
+bool use_pair_kernel() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("VIT_GEMM_PAIR");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
@@ -390,23 +624,31 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     p.out = d.out;
     p.ldo = d.ldo;
     p.err = dev.err_word;
-    const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
-    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    const bool pair = use_pair_kernel() && dev.num_sms >= 2;
+    int grid;
+    if (pair) {
+        const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN);
+        const int64_t clusters = tiles < dev.num_sms / 2 ? tiles : dev.num_sms / 2;
+        grid = (int)(2 * clusters);
+    } else {
+        const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
+        grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    }
     switch (d.epi) {
         case TC_EPI_STORE:
-            return d.out_f32 ? launch_inst<TC_EPI_STORE, float, float>(ma, mb, p, grid, s)
-                             : launch_inst<TC_EPI_STORE, __nv_bfloat16, float>(ma, mb, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, p, grid, s)
+                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, p, grid, s);
         case TC_EPI_GELU:
-            return d.out_f32 ? launch_inst<TC_EPI_GELU, float, float>(ma, mb, p, grid, s)
-                             : launch_inst<TC_EPI_GELU, __nv_bfloat16, float>(ma, mb, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, p, grid, s)
+                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, p, grid, s);
         case TC_EPI_RESID:
             if (d.out_f32)
                 return d.residual_f32
-                           ? launch_inst<TC_EPI_RESID, float, float>(ma, mb, p, grid, s)
-                           : launch_inst<TC_EPI_RESID, float, __nv_bfloat16>(ma, mb, p, grid, s);
+                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, p, grid, s)
+                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, p, grid, s);
             return d.residual_f32
-                       ? launch_inst<TC_EPI_RESID, __nv_bfloat16, float>(ma, mb, p, grid, s)
-                       : launch_inst<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(ma, mb, p, grid, s);
+                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, p, grid, s)
+                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -163,6 +163,37 @@ cudaError_t launch_generic(const void* x, void* out, const void* g, const void* 
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+template <typename TIn, int MAXV>
+cudaError_t launch_fast_v(const void* x, void* out, const void* g, const void* b, int64_t rows,
+                          int64_t D, double eps, cudaStream_t s) {
+    const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
+    ln_fast_kernel<TIn, MAXV><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
+        static_cast<const TIn*>(x), static_cast<__nv_bfloat16*>(out),
+        static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), rows, (int)D,
+        (float)eps);
+    return cudaGetLastError();
+}
+
+template <typename TIn>
+cudaError_t launch_fast(const void* x, void* out, const void* g, const void* b, int64_t rows,
+                        int64_t D, double eps, int per_lane, cudaStream_t s) {
+    switch (per_lane) {
+        case 1: return launch_fast_v<TIn, 1>(x, out, g, b, rows, D, eps, s);
+        case 2: return launch_fast_v<TIn, 2>(x, out, g, b, rows, D, eps, s);
+        case 3: return launch_fast_v<TIn, 3>(x, out, g, b, rows, D, eps, s);
+        case 4: return launch_fast_v<TIn, 4>(x, out, g, b, rows, D, eps, s);
+        case 5: return launch_fast_v<TIn, 5>(x, out, g, b, rows, D, eps, s);
+        case 6: return launch_fast_v<TIn, 6>(x, out, g, b, rows, D, eps, s);
+        case 7:
+        case 8: return launch_fast_v<TIn, 8>(x, out, g, b, rows, D, eps, s);
+        case 9:
+        case 10: return launch_fast_v<TIn, 10>(x, out, g, b, rows, D, eps, s);
+        case 11:
+        case 12: return launch_fast_v<TIn, 12>(x, out, g, b, rows, D, eps, s);
+        default: return launch_fast_v<TIn, 16>(x, out, g, b, rows, D, eps, s);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt, const void* gamma,
@@ -173,21 +204,11 @@ cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt, co
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     const bool vec_ok = D % 8 == 0 && D <= 2048 && aligned16(x) && aligned16(out);
     const bool gb_bf16 = (!gamma && !beta) || gb_dt == DT_BF16;
-    if (out_dt == DT_BF16 && vec_ok && gb_bf16) {
-        auto g = static_cast<const __nv_bfloat16*>(gamma);
-        auto b = static_cast<const __nv_bfloat16*>(beta);
-        if (in_dt == DT_BF16) {
-            ln_fast_kernel<__nv_bfloat16, 8><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
-                static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(out), g, b, rows,
-                (int)D, (float)eps);
-            return cudaGetLastError();
-        }
-        if (in_dt == DT_F32) {
-            ln_fast_kernel<float, 16><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
-                static_cast<const float*>(x), static_cast<__nv_bfloat16*>(out), g, b, rows, (int)D,
-                (float)eps);
-            return cudaGetLastError();
-        }
+    if (out_dt == DT_BF16 && vec_ok && gb_bf16 && (in_dt == DT_BF16 || in_dt == DT_F32)) {
+        // registers hold ceil(D / (32 lanes * vector width)) vectors per lane
+        const int per_lane = (int)((D / (in_dt == DT_BF16 ? 8 : 4) + 31) / 32);
+        return in_dt == DT_BF16 ? launch_fast<__nv_bfloat16>(x, out, gamma, beta, rows, D, eps, per_lane, s)
+                                : launch_fast<float>(x, out, gamma, beta, rows, D, eps, per_lane, s);
     }
     if (in_dt == DT_BF16 && out_dt == DT_BF16)
         return launch_generic<__nv_bfloat16, __nv_bfloat16>(x, out, gamma, beta, gb_dt, rows, D, eps, s);
