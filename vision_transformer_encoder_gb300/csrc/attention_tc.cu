@@ -1,0 +1,460 @@
+// attention_tc.cu -- bidirectional multi-head attention on the sm_103a tensor cores
+// (tcgen05 / TMEM / TMA), bf16 in and out, fp32 softmax.
+//
+// "ViT Encoder Block" (crackedaicode), "Multi-head attention": per sequence n and head
+// h, out_h = softmax(Q_h K_h^T / sqrt(D/H)) V_h with every key visible (no mask);
+// heads written side by side in order. Q, K and V are read in place from the fused
+// (N, T, 3D) buffer [Q | K | V] (head h at columns h*dh of each block, as in
+// "vision1 reference transcript" (nipunbatra.github.io), Page 106).
+//
+// Persistent kernel, one CTA per SM. A work item is (sequence, head, pair of 128-row
+// query tiles), so one pass over the keys serves 256 queries (T = 197 is one item).
+//   warp 0      TMA: the item's query tiles, then 128-key K and V tiles into a 2-stage
+//               ring. A 3-D tensor map (column, token, sequence) zero-fills tokens past
+//               T, so tiles never read the next sequence. Boxes are 16 columns wide with
+//               a 32-byte swizzle, which covers head widths 64 and 80 exactly.
+//   warp 1      MMA: S_g = Q_g K^T (M 128, N 128, K dh) into TMEM, then O_g += P_g V
+//               (M 128, N dh, K 128) with P from shared memory and V read MN-major.
+//               S and O live in TMEM (2 x 128 + 2 x dh columns of 512).
+//   warps 2-5   softmax group 0 (query tile 0), warps 6-9 group 1 (query tile 1): one
+//               query row per thread. Pass 1 takes the row maximum of the valid keys,
+//               pass 2 writes P = exp2(S*log2(e)/sqrt(dh) - m) in bf16 to a 128B-swizzled
+//               K-major tile, keys past T get P = 0. When the running maximum grows, the
+//               thread rescales its O row in TMEM first (online softmax). At the end it
+//               divides by the row sum and stores bf16.
+// The two groups are released independently (S for one group is issued right after
+// that group's P.V), so one group's softmax overlaps the other's MMAs.
+// Every wait is bounded; on expiry the kernel records an error bit and unwinds.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace vit {
+namespace {
+
+constexpr int AT_ROWS = 128;       // query rows per tile (TMEM lanes)
+constexpr int AT_KEYS = 128;       // keys per K/V tile
+constexpr int AT_KV_STAGES = 2;
+constexpr int AT_THREADS = 320;    // 10 warps
+constexpr int AT_BOX = AT_ROWS * 32;  // one 16-column box of 128 rows: 4 KB
+
+template <int DH>
+struct AtLayout {
+    static constexpr int NB = DH / 16;
+    static constexpr int TILE = NB * AT_BOX;        // one Q, K or V tile
+    static constexpr int P_BYTES = AT_ROWS * AT_KEYS * 2;
+    static constexpr int OFF_Q = 0;                 // 2 query tiles
+    static constexpr int OFF_K = OFF_Q + 2 * TILE;
+    static constexpr int OFF_V = OFF_K + AT_KV_STAGES * TILE;
+    static constexpr int OFF_P = OFF_V + AT_KV_STAGES * TILE;   // 2 groups
+    static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+};
+
+struct AtParams {
+    int N, T, D, H;
+    int npairs;      // query-tile pairs per (sequence, head)
+    int nkt;         // key tiles per sequence
+    int items;
+    float scale_log2;
+    __nv_bfloat16* o;
+    uint32_t* err;
+};
+
+struct AtBars {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[AT_KV_STAGES], kv_empty[AT_KV_STAGES];
+    uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
+    uint64_t done;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void at_error(uint32_t* err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ void item_decode(const AtParams& p, int item, int& n, int& h, int& q0,
+                                            int& nact) {
+    const int pair = item % p.npairs;
+    h = (item / p.npairs) % p.H;
+    n = item / (p.npairs * p.H);
+    q0 = pair * 2 * AT_ROWS;
+    nact = (q0 + AT_ROWS < p.T) ? 2 : 1;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(AT_THREADS, 1)
+attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
+    using L = AtLayout<DH>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem + L::OFF_Q;
+    uint8_t* sK = smem + L::OFF_K;
+    uint8_t* sV = smem + L::OFF_V;
+    uint8_t* sP = smem + L::OFF_P;
+    AtBars* bars = reinterpret_cast<AtBars*>(smem + L::OFF_BAR);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bars->q_full, 1);
+        ptx::mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < AT_KV_STAGES; ++s) {
+            ptx::mbar_init(&bars->kv_full[s], 1);
+            ptx::mbar_init(&bars->kv_empty[s], 1);
+        }
+        for (int g = 0; g < 2; ++g) {
+            ptx::mbar_init(&bars->s_full[g], 1);
+            ptx::mbar_init(&bars->s_free[g], 128);
+            ptx::mbar_init(&bars->p_full[g], 128);
+            ptx::mbar_init(&bars->o_done[g], 1);
+            ptx::mbar_init(&bars->o_free[g], 128);
+        }
+        ptx::mbar_init(&bars->done, 1);
+        bars->abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&tm);
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_slot, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+    // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+DH), O_1 [384,384+DH)
+    const int D = p.D;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            uint32_t kv_it = 0, ii = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ii) {
+                int n, h, q0, nact;
+                item_decode(p, item, n, h, q0, nact);
+                if (!ptx::mbar_wait_bounded(&bars->q_empty, (ii & 1) ^ 1, abort_flag)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&bars->q_full, nact * L::TILE);
+                for (int g = 0; g < nact; ++g)
+                    for (int b = 0; b < L::NB; ++b)
+                        ptx::tma_load_3d(sQ + g * L::TILE + b * AT_BOX, &tm, &bars->q_full,
+                                         h * DH + 16 * b, q0 + g * AT_ROWS, n);
+                for (int j = 0; j < p.nkt; ++j, ++kv_it) {
+                    const uint32_t st = kv_it % AT_KV_STAGES, u = kv_it / AT_KV_STAGES;
+                    if (!ptx::mbar_wait_bounded(&bars->kv_empty[st], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::TILE);
+                    for (int b = 0; b < L::NB; ++b) {
+                        ptx::tma_load_3d(sK + st * L::TILE + b * AT_BOX, &tm, &bars->kv_full[st],
+                                         D + h * DH + 16 * b, j * AT_KEYS, n);
+                        ptx::tma_load_3d(sV + st * L::TILE + b * AT_BOX, &tm, &bars->kv_full[st],
+                                         2 * D + h * DH + 16 * b, j * AT_KEYS, n);
+                    }
+                }
+            }
+            if (!ok) {
+                at_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
+                *abort_flag = 1;
+            }
+            // let in-flight copies land before the CTA can exit
+            if (ii > 0 && !ptx::mbar_wait_bounded(&bars->q_full, (ii - 1) & 1, nullptr))
+                at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            for (uint32_t s = 0; s < AT_KV_STAGES; ++s)
+                if (kv_it > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((kv_it - 1 - s) / AT_KV_STAGES) & 1, nullptr))
+                    at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            constexpr uint32_t idS = ptx::idesc_bf16_f32(AT_ROWS, AT_KEYS, false, false);
+            constexpr uint32_t idO = ptx::idesc_bf16_f32(AT_ROWS, DH, false, true);
+            uint32_t kv_base = 0, ii = 0;
+            uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};
+            bool ok = true;
+            auto issue_S = [&](int g, int j) -> bool {
+                const uint32_t kv = kv_base + j;
+                const uint32_t st = kv % AT_KV_STAGES, u = kv / AT_KV_STAGES;
+                if (g == 0 && !ptx::mbar_wait_bounded(&bars->kv_full[st], u & 1, abort_flag)) return false;
+                if (sc[g] > 0 && !ptx::mbar_wait_bounded(&bars->s_free[g], (sc[g] - 1) & 1, abort_flag)) return false;
+                ptx::tc_fence_after();
+                const uint32_t qa = ptx::smem_addr(sQ + g * L::TILE);
+                const uint32_t ka = ptx::smem_addr(sK + st * L::TILE);
+#pragma unroll
+                for (int kk = 0; kk < L::NB; ++kk) {
+                    const uint64_t ad = ptx::smem_desc(qa + kk * AT_BOX, 16, 256, ptx::kLayoutSw32);
+                    const uint64_t bd = ptx::smem_desc(ka + kk * AT_BOX, 16, 256, ptx::kLayoutSw32);
+                    ptx::mma_bf16_ss(tmem + g * AT_KEYS, ad, bd, idS, kk > 0);
+                }
+                ptx::mma_commit(&bars->s_full[g]);
+                ++sc[g];
+                return true;
+            };
+            for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ii) {
+                int n, h, q0, nact;
+                item_decode(p, item, n, h, q0, nact);
+                if (!ptx::mbar_wait_bounded(&bars->q_full, ii & 1, abort_flag)) { ok = false; break; }
+                for (int g = 0; g < nact && ok; ++g) ok = issue_S(g, 0);
+                if (p.nkt == 1 && ok) ptx::mma_commit(&bars->q_empty);
+                for (int j = 0; j < p.nkt && ok; ++j) {
+                    const uint32_t st = (kv_base + j) % AT_KV_STAGES;
+                    for (int g = 0; g < nact; ++g) {
+                        if (!ptx::mbar_wait_bounded(&bars->p_full[g], pc[g] & 1, abort_flag)) { ok = false; break; }
+                        if (j == 0 && ic[g] > 0 &&
+                            !ptx::mbar_wait_bounded(&bars->o_free[g], (ic[g] - 1) & 1, abort_flag)) { ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t pa = ptx::smem_addr(sP + g * L::P_BYTES);
+                        const uint32_t va = ptx::smem_addr(sV + st * L::TILE);
+#pragma unroll
+                        for (int kk = 0; kk < AT_KEYS / 16; ++kk) {
+                            const uint64_t ad = ptx::smem_desc(pa + (kk >> 2) * (AT_ROWS * 128) + (kk & 3) * 32,
+                                                               16, 1024, ptx::kLayoutSw128);
+                            const uint64_t bd = ptx::smem_desc(va + kk * 512, AT_BOX, 256, ptx::kLayoutSw32);
+                            ptx::mma_bf16_ss(tmem + 256 + g * 128, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        ptx::mma_commit(&bars->o_done[g]);
+                        ++pc[g];
+                        if (g == nact - 1) ptx::mma_commit(&bars->kv_empty[st]);
+                        if (j + 1 < p.nkt) {
+                            if (!issue_S(g, j + 1)) { ok = false; break; }
+                            if (j + 1 == p.nkt - 1 && g == nact - 1) ptx::mma_commit(&bars->q_empty);
+                        }
+                    }
+                }
+                for (int g = 0; g < nact; ++g) ++ic[g];
+                kv_base += p.nkt;
+            }
+            if (!ok) {
+                at_error(p.err, ERRBIT_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            ptx::mma_commit(&bars->done);
+            if (!ptx::mbar_wait_bounded(&bars->done, 0, nullptr)) at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else {
+        // -------------------------------------------------------- softmax groups
+        const int g = (warp - 2) >> 2;          // 0: warps 2-5, 1: warps 6-9
+        const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+        const int r = quarter * 32 + lane;      // query row within the tile
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + g * AT_KEYS + lane_off;
+        const uint32_t tO = tmem + 256 + g * 128 + lane_off;
+        uint8_t* prow = sP + g * L::P_BYTES + r * 128;   // + chunk * 16 KB
+        const float sl2 = p.scale_log2;
+        uint32_t tt = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x) {
+            int n, h, q0, nact;
+            item_decode(p, item, n, h, q0, nact);
+            if (g >= nact) continue;
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < p.nkt; ++j, ++tt) {
+                ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->s_full[g], tt & 1, abort_flag));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const int valid = min(AT_KEYS, p.T - j * AT_KEYS);
+                // pass 1: maximum over the valid keys of this row
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < AT_KEYS / 32; ++c) {
+                    if (c * 32 < valid) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e)
+                            if (c * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(v[e]));
+                    }
+                }
+                const float m_new = fmaxf(m, mx * sl2);
+                const float alpha = exp2_approx(m - m_new);
+                if (j > 0) {
+                    // P.V of the previous tile must be done: it reads P, and O is rescaled
+                    ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll
+                        for (int c = 0; c < DH / 16; ++c) {
+                            uint32_t v[16];
+                            ptx::tmem_ld_32x32b_x16(tO + c * 16, v);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                            ptx::tmem_st_32x32b_x16(tO + c * 16, v);
+                        }
+                        ptx::tmem_st_wait();
+                    }
+                }
+                l *= alpha;
+                m = m_new;
+                // pass 2: P = exp2(s * scale - m) in bf16, 0 past the valid keys
+#pragma unroll
+                for (int c = 0; c < AT_KEYS / 32; ++c) {
+                    uint32_t pk[16];
+                    if (c * 32 < valid) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float p0 = (c * 32 + e < valid)
+                                                 ? exp2_approx(fmaf(__uint_as_float(v[e]), sl2, -m)) : 0.f;
+                            const float p1 = (c * 32 + e + 1 < valid)
+                                                 ? exp2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m)) : 0.f;
+                            l += p0 + p1;
+                            pk[e >> 1] = pack_bf16x2(p0, p1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                    }
+                    // 32 keys = four 16-byte units of this row in chunk c/2 (64 keys per
+                    // 128-byte row), placed with the 128-byte swizzle (unit ^ row % 8)
+                    uint8_t* base = prow + (c >> 1) * (AT_ROWS * 128);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int unit = (c & 1) * 4 + q;
+                        uint4 w = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                        *reinterpret_cast<uint4*>(base + ((unit ^ (r & 7)) << 4)) = w;
+                    }
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&bars->s_free[g]);
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bars->p_full[g]);
+            }
+            if (!ok) break;
+            // epilogue: O / l -> bf16
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const float inv = 1.f / l;
+            const int t = q0 + g * AT_ROWS + r;
+            __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * DH;
+#pragma unroll
+            for (int c = 0; c < DH / 16; ++c) {
+                uint32_t v[16];
+                ptx::tmem_ld_32x32b_x16(tO + c * 16, v);
+                ptx::tmem_ld_wait();
+                if (t < p.T) {
+                    uint4 w0, w1;
+                    w0.x = pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
+                    w0.y = pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
+                    w0.z = pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
+                    w0.w = pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
+                    w1.x = pack_bf16x2(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
+                    w1.y = pack_bf16x2(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
+                    w1.z = pack_bf16x2(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
+                    w1.w = pack_bf16x2(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
+                    *reinterpret_cast<uint4*>(orow + c * 16) = w0;
+                    *reinterpret_cast<uint4*>(orow + c * 16 + 8) = w1;
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bars->o_free[g]);
+        }
+        if (!ok) {
+            if (lane == 0) at_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
+            *abort_flag = 1;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn at_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault,
+                                             &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    });
+    return fn;
+}
+
+template <int DH>
+cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
+                         const DeviceInfo& dev, cudaStream_t s) {
+    using L = AtLayout<DH>;
+    EncodeTiledFn fn = at_encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    alignas(64) CUtensorMap tm;
+    cuuint64_t dims[3] = {(cuuint64_t)(3 * D), (cuuint64_t)T, (cuuint64_t)N};
+    cuuint64_t strides[2] = {(cuuint64_t)(3 * D * 2), (cuuint64_t)(T * 3 * D * 2)};
+    cuuint32_t box[3] = {16, AT_ROWS, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    AtParams p;
+    p.N = (int)N;
+    p.T = (int)T;
+    p.D = (int)D;
+    p.H = (int)H;
+    const int qt = (int)((T + AT_ROWS - 1) / AT_ROWS);
+    p.npairs = (qt + 1) / 2;
+    p.nkt = (int)((T + AT_KEYS - 1) / AT_KEYS);
+    p.items = (int)(N * H * p.npairs);
+    p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.err = dev.err_word;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<DH>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
+    attention_tc_kernel<DH><<<grid, AT_THREADS, L::SMEM, s>>>(tm, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attention_tc_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o) {
+    if (H <= 0 || D % H != 0) return false;
+    const int64_t dh = D / H;
+    if (dh != 64 && dh != 80) return false;
+    if ((reinterpret_cast<uintptr_t>(qkv) & 15) || (reinterpret_cast<uintptr_t>(o) & 15)) return false;
+    if ((3 * D * 2) % 16 != 0 || N * H * ((T + 255) / 256) > 0x7fffffff || T > (1 << 20)) return false;
+    const char* e = std::getenv("VIT_ATTN_TC");
+    if (e && e[0] == '0') return false;
+    return at_encode_fn() != nullptr;
+}
+
+cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
+                                const DeviceInfo& dev, cudaStream_t s) {
+    if (N <= 0 || T <= 0) return cudaSuccess;
+    switch (D / H) {
+        case 64: return launch_tc_dh<64>(qkv, o, N, T, D, H, dev, s);
+        case 80: return launch_tc_dh<80>(qkv, o, N, T, D, H, dev, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vit

@@ -70,6 +70,12 @@ cudaError_t launch_gemm_simt(const SimtGemmDesc& d, cudaStream_t s);
 bool attention_fast_supported(int64_t D, int64_t H, const void* qkv, const void* o);
 cudaError_t launch_attention_fast(const void* qkv, void* o, int64_t N, int64_t T, int64_t D,
                                   int64_t H, cudaStream_t s);
+// tcgen05 flash attention (attention_tc.cu): head widths 64 and 80, bf16, 16-byte
+// aligned buffers. VIT_ATTN_TC=0 disables it (then the kernel above is used).
+bool attention_tc_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv,
+                            const void* o);
+cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, int64_t D,
+                                int64_t H, const DeviceInfo& dev, cudaStream_t s);
 // Any dtype (f32/bf16/f64 in and out, same type), any head width.
 cudaError_t launch_attention_simt(const void* qkv, int dt, void* o, int64_t N, int64_t T,
                                   int64_t D, int64_t H, cudaStream_t s);

@@ -236,6 +236,8 @@ int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
             return r;
         }));
         step(run(K_ATTN, s, [&] {
+            if (attention_tc_supported(a.N, a.T, D, a.H, qkv, buf))
+                return launch_attention_tc(qkv, buf, a.N, a.T, D, a.H, dev, s);
             if (attention_fast_supported(D, a.H, qkv, buf))
                 return launch_attention_fast(qkv, buf, a.N, a.T, D, a.H, s);
             return launch_attention_simt(qkv, DT_BF16, buf, a.N, a.T, D, a.H, s);
@@ -492,6 +494,8 @@ int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, i
     if (rc != VIT_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = run(K_ATTN, s, [&] {
+        if (dtype == DT_BF16 && attention_tc_supported(N, T, D, H, qkv, o))
+            return launch_attention_tc(qkv, o, N, T, D, H, st->info, s);
         if (dtype == DT_BF16 && attention_fast_supported(D, H, qkv, o) && (D * 2) % 16 == 0)
             return launch_attention_fast(qkv, o, N, T, D, H, s);
         return launch_attention_simt(qkv, dtype, o, N, T, D, H, s);
