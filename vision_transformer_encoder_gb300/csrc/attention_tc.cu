@@ -11,15 +11,19 @@
 // query tiles), so one pass over the keys serves 256 queries (T = 197 is one item).
 //   warp 0      TMA: the item's query tiles, then 128-key K and V tiles into a 2-stage
 //               ring. A 3-D tensor map (column, token, sequence) zero-fills tokens past
-//               T, so tiles never read the next sequence. Boxes are 16 columns wide with
-//               a 32-byte swizzle, which covers head widths 64 and 80 exactly.
+//               T, so tiles never read the next sequence. A head slice is one 64-column
+//               box with the 128-byte swizzle, plus, for dh = 80, one 16-column box with
+//               the 32-byte swizzle (the MMAs for that part use a second descriptor).
 //   warp 1      MMA: S_g = Q_g K^T (M 128, N 128, K dh) into TMEM, then O_g += P_g V
-//               (M 128, N dh, K 128) with P from shared memory and V read MN-major.
-//               S and O live in TMEM (2 x 128 + 2 x dh columns of 512).
+//               (M 128, N dh, K 128) with V read MN-major. S and O live in TMEM. For
+//               dh = 64, P also lives in TMEM (the MMA reads A from tensor memory), which
+//               frees shared memory for two query buffers and four K/V stages, so the
+//               loads run a whole work item ahead; for dh = 80, P is staged in shared
+//               memory and the ring is one query buffer and two K/V stages.
 //   warps 2-5   softmax group 0 (query tile 0), warps 6-9 group 1 (query tile 1): one
 //               query row per thread. Pass 1 takes the row maximum of the valid keys,
-//               pass 2 writes P = exp2(S*log2(e)/sqrt(dh) - m) in bf16 to a 128B-swizzled
-//               K-major tile, keys past T get P = 0. When the running maximum grows, the
+//               pass 2 writes P = exp2(S*log2(e)/sqrt(dh) - m) in bf16 (to TMEM, or to a
+//               128B-swizzled K-major shared tile), keys past T get P = 0. When the running maximum grows, the
 //               thread rescales its O row in TMEM first (online softmax). At the end it
 //               divides by the row sum and stores bf16.
 // The two groups are released independently (S for one group is issued right after
@@ -41,24 +45,32 @@ namespace {
 
 constexpr int AT_ROWS = 128;       // query rows per tile (TMEM lanes)
 constexpr int AT_KEYS = 128;       // keys per K/V tile
-constexpr int AT_KV_STAGES = 2;
+constexpr int AT_MAX_KV = 4;
 constexpr int AT_THREADS = 320;    // 10 warps
-constexpr int AT_BOX = AT_ROWS * 32;  // one 16-column box of 128 rows: 4 KB
+constexpr int AT_BOX64 = AT_ROWS * 128;  // 64 columns x 128 rows, 128B swizzle: 16 KB
+constexpr int AT_BOX16 = AT_ROWS * 32;   // 16 columns x 128 rows, 32B swizzle: 4 KB
 
-template <int DH>
+// PT: P kept in TMEM (dh = 64). Otherwise P is staged in shared memory.
+template <int DH, bool PT>
 struct AtLayout {
-    static constexpr int NB = DH / 16;
-    static constexpr int TILE = NB * AT_BOX;        // one Q, K or V tile
-    static constexpr int P_BYTES = AT_ROWS * AT_KEYS * 2;
-    static constexpr int OFF_Q = 0;                 // 2 query tiles
-    static constexpr int OFF_K = OFF_Q + 2 * TILE;
-    static constexpr int OFF_V = OFF_K + AT_KV_STAGES * TILE;
-    static constexpr int OFF_P = OFF_V + AT_KV_STAGES * TILE;   // 2 groups
+    static_assert(DH == 64 || DH == 80, "head width 64 or 80");
+    static constexpr bool TAIL = DH == 80;          // a 16-column second box
+    static constexpr int TILE = AT_BOX64 + (TAIL ? AT_BOX16 : 0);   // one Q, K or V tile
+    static constexpr int QBUF = PT ? 2 : 1;         // query-pair buffers
+    static constexpr int KVS = PT ? 4 : 2;          // K/V ring stages
+    static constexpr int P_BYTES = PT ? 0 : AT_ROWS * AT_KEYS * 2;
+    static constexpr int OFF_Q = 0;                 // QBUF x 2 query tiles
+    static constexpr int OFF_K = OFF_Q + QBUF * 2 * TILE;
+    static constexpr int OFF_V = OFF_K + KVS * TILE;
+    static constexpr int OFF_P = OFF_V + KVS * TILE;   // 2 groups (if staged)
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-    static constexpr int SMEM = OFF_BAR + 256 + 1024;
+    static constexpr int SMEM = OFF_BAR + 512 + 1024;
+    static_assert(KVS <= AT_MAX_KV, "ring too deep");
+    static_assert(!PT || DH <= 64, "O and P share a 128-column TMEM slot");
 };
 
 struct AtParams {
+    int tail_maps;   // 1 when the 16-column map is used (dh = 80)
     int N, T, D, H;
     int npairs;      // query-tile pairs per (sequence, head)
     int nkt;         // key tiles per sequence
@@ -69,8 +81,8 @@ struct AtParams {
 };
 
 struct AtBars {
-    uint64_t q_full, q_empty;
-    uint64_t kv_full[AT_KV_STAGES], kv_empty[AT_KV_STAGES];
+    uint64_t q_full[2], q_empty[2];
+    uint64_t kv_full[AT_MAX_KV], kv_empty[AT_MAX_KV];
     uint64_t s_full[2], s_free[2], p_full[2], o_done[2], o_free[2];
     uint64_t done;
     uint32_t tmem_slot;
@@ -90,10 +102,12 @@ __device__ __forceinline__ void item_decode(const AtParams& p, int item, int& n,
     nact = (q0 + AT_ROWS < p.T) ? 2 : 1;
 }
 
-template <int DH>
+template <int DH, bool PT>
 __global__ void __launch_bounds__(AT_THREADS, 1)
-attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
-    using L = AtLayout<DH>;
+attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm16,
+                    const AtParams p) {
+    using L = AtLayout<DH, PT>;
+    constexpr int KVS = L::KVS, QB = L::QBUF;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -107,9 +121,11 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bars->q_full, 1);
-        ptx::mbar_init(&bars->q_empty, 1);
-        for (int s = 0; s < AT_KV_STAGES; ++s) {
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bars->q_full[b], 1);
+            ptx::mbar_init(&bars->q_empty[b], 1);
+        }
+        for (int s = 0; s < AT_MAX_KV; ++s) {
             ptx::mbar_init(&bars->kv_full[s], 1);
             ptx::mbar_init(&bars->kv_empty[s], 1);
         }
@@ -124,7 +140,10 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&tm);
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm);
+        if (L::TAIL) ptx::prefetch_tensormap(&tm16);
+    }
     if (warp == 1) {
         ptx::tmem_alloc(&bars->tmem_slot, 512);
         ptx::tmem_relinquish();
@@ -133,7 +152,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
-    // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+DH), O_1 [384,384+DH)
+    // TMEM columns: S_g at [128 g, 128 g + 128); O_g at 256 + 128 g; with PT, P_g (64
+    // columns of bf16 pairs) right after O_g at 256 + 128 g + 64.
     const int D = p.D;
 
     if (warp == 0) {
@@ -144,21 +164,26 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
             for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ii) {
                 int n, h, q0, nact;
                 item_decode(p, item, n, h, q0, nact);
-                if (!ptx::mbar_wait_bounded(&bars->q_empty, (ii & 1) ^ 1, abort_flag)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(&bars->q_full, nact * L::TILE);
-                for (int g = 0; g < nact; ++g)
-                    for (int b = 0; b < L::NB; ++b)
-                        ptx::tma_load_3d(sQ + g * L::TILE + b * AT_BOX, &tm, &bars->q_full,
-                                         h * DH + 16 * b, q0 + g * AT_ROWS, n);
+                const uint32_t qb = ii % QB, qu = ii / QB;
+                if (!ptx::mbar_wait_bounded(&bars->q_empty[qb], (qu & 1) ^ 1, abort_flag)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&bars->q_full[qb], nact * L::TILE);
+                for (int g = 0; g < nact; ++g) {
+                    uint8_t* dq = sQ + (qb * 2 + g) * L::TILE;
+                    ptx::tma_load_3d(dq, &tm, &bars->q_full[qb], h * DH, q0 + g * AT_ROWS, n);
+                    if (L::TAIL)
+                        ptx::tma_load_3d(dq + AT_BOX64, &tm16, &bars->q_full[qb], h * DH + 64, q0 + g * AT_ROWS, n);
+                }
                 for (int j = 0; j < p.nkt; ++j, ++kv_it) {
-                    const uint32_t st = kv_it % AT_KV_STAGES, u = kv_it / AT_KV_STAGES;
+                    const uint32_t st = kv_it % KVS, u = kv_it / KVS;
                     if (!ptx::mbar_wait_bounded(&bars->kv_empty[st], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
                     ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::TILE);
-                    for (int b = 0; b < L::NB; ++b) {
-                        ptx::tma_load_3d(sK + st * L::TILE + b * AT_BOX, &tm, &bars->kv_full[st],
-                                         D + h * DH + 16 * b, j * AT_KEYS, n);
-                        ptx::tma_load_3d(sV + st * L::TILE + b * AT_BOX, &tm, &bars->kv_full[st],
-                                         2 * D + h * DH + 16 * b, j * AT_KEYS, n);
+                    uint8_t* dk = sK + st * L::TILE;
+                    uint8_t* dv = sV + st * L::TILE;
+                    ptx::tma_load_3d(dk, &tm, &bars->kv_full[st], D + h * DH, j * AT_KEYS, n);
+                    ptx::tma_load_3d(dv, &tm, &bars->kv_full[st], 2 * D + h * DH, j * AT_KEYS, n);
+                    if (L::TAIL) {
+                        ptx::tma_load_3d(dk + AT_BOX64, &tm16, &bars->kv_full[st], D + h * DH + 64, j * AT_KEYS, n);
+                        ptx::tma_load_3d(dv + AT_BOX64, &tm16, &bars->kv_full[st], 2 * D + h * DH + 64, j * AT_KEYS, n);
                     }
                 }
             }
@@ -167,33 +192,41 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
                 *abort_flag = 1;
             }
             // let in-flight copies land before the CTA can exit
-            if (ii > 0 && !ptx::mbar_wait_bounded(&bars->q_full, (ii - 1) & 1, nullptr))
-                at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-            for (uint32_t s = 0; s < AT_KV_STAGES; ++s)
-                if (kv_it > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((kv_it - 1 - s) / AT_KV_STAGES) & 1, nullptr))
+            for (uint32_t b = 0; b < (uint32_t)QB; ++b)
+                if (ii > b && !ptx::mbar_wait_bounded(&bars->q_full[b], ((ii - 1 - b) / QB) & 1, nullptr))
+                    at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            for (uint32_t s = 0; s < (uint32_t)KVS; ++s)
+                if (kv_it > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((kv_it - 1 - s) / KVS) & 1, nullptr))
                     at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t idS = ptx::idesc_bf16_f32(AT_ROWS, AT_KEYS, false, false);
-            constexpr uint32_t idO = ptx::idesc_bf16_f32(AT_ROWS, DH, false, true);
+            constexpr uint32_t idO64 = ptx::idesc_bf16_f32(AT_ROWS, 64, false, true);
+            constexpr uint32_t idO16 = ptx::idesc_bf16_f32(AT_ROWS, 16, false, true);
             uint32_t kv_base = 0, ii = 0;
             uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};
             bool ok = true;
+            uint32_t qb = 0;
             auto issue_S = [&](int g, int j) -> bool {
                 const uint32_t kv = kv_base + j;
-                const uint32_t st = kv % AT_KV_STAGES, u = kv / AT_KV_STAGES;
+                const uint32_t st = kv % KVS, u = kv / KVS;
                 if (g == 0 && !ptx::mbar_wait_bounded(&bars->kv_full[st], u & 1, abort_flag)) return false;
                 if (sc[g] > 0 && !ptx::mbar_wait_bounded(&bars->s_free[g], (sc[g] - 1) & 1, abort_flag)) return false;
                 ptx::tc_fence_after();
-                const uint32_t qa = ptx::smem_addr(sQ + g * L::TILE);
+                const uint32_t qa = ptx::smem_addr(sQ + (qb * 2 + g) * L::TILE);
                 const uint32_t ka = ptx::smem_addr(sK + st * L::TILE);
 #pragma unroll
-                for (int kk = 0; kk < L::NB; ++kk) {
-                    const uint64_t ad = ptx::smem_desc(qa + kk * AT_BOX, 16, 256, ptx::kLayoutSw32);
-                    const uint64_t bd = ptx::smem_desc(ka + kk * AT_BOX, 16, 256, ptx::kLayoutSw32);
+                for (int kk = 0; kk < 4; ++kk) {   // 64 columns: 128-byte rows, 32 bytes per step
+                    const uint64_t ad = ptx::smem_desc(qa + kk * 32, 16, 1024, ptx::kLayoutSw128);
+                    const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 1024, ptx::kLayoutSw128);
                     ptx::mma_bf16_ss(tmem + g * AT_KEYS, ad, bd, idS, kk > 0);
+                }
+                if (L::TAIL) {                     // columns 64..79: one 32-byte-row step
+                    const uint64_t ad = ptx::smem_desc(qa + AT_BOX64, 16, 256, ptx::kLayoutSw32);
+                    const uint64_t bd = ptx::smem_desc(ka + AT_BOX64, 16, 256, ptx::kLayoutSw32);
+                    ptx::mma_bf16_ss(tmem + g * AT_KEYS, ad, bd, idS, 1u);
                 }
                 ptx::mma_commit(&bars->s_full[g]);
                 ++sc[g];
@@ -202,31 +235,47 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
             for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ii) {
                 int n, h, q0, nact;
                 item_decode(p, item, n, h, q0, nact);
-                if (!ptx::mbar_wait_bounded(&bars->q_full, ii & 1, abort_flag)) { ok = false; break; }
+                qb = ii % QB;
+                if (!ptx::mbar_wait_bounded(&bars->q_full[qb], (ii / QB) & 1, abort_flag)) { ok = false; break; }
                 for (int g = 0; g < nact && ok; ++g) ok = issue_S(g, 0);
-                if (p.nkt == 1 && ok) ptx::mma_commit(&bars->q_empty);
+                if (p.nkt == 1 && ok) ptx::mma_commit(&bars->q_empty[qb]);
                 for (int j = 0; j < p.nkt && ok; ++j) {
-                    const uint32_t st = (kv_base + j) % AT_KV_STAGES;
+                    const uint32_t st = (kv_base + j) % KVS;
                     for (int g = 0; g < nact; ++g) {
                         if (!ptx::mbar_wait_bounded(&bars->p_full[g], pc[g] & 1, abort_flag)) { ok = false; break; }
                         if (j == 0 && ic[g] > 0 &&
                             !ptx::mbar_wait_bounded(&bars->o_free[g], (ic[g] - 1) & 1, abort_flag)) { ok = false; break; }
                         ptx::tc_fence_after();
-                        const uint32_t pa = ptx::smem_addr(sP + g * L::P_BYTES);
                         const uint32_t va = ptx::smem_addr(sV + st * L::TILE);
+                        const uint32_t tO = tmem + 256 + g * 128;
 #pragma unroll
                         for (int kk = 0; kk < AT_KEYS / 16; ++kk) {
-                            const uint64_t ad = ptx::smem_desc(pa + (kk >> 2) * (AT_ROWS * 128) + (kk & 3) * 32,
-                                                               16, 1024, ptx::kLayoutSw128);
-                            const uint64_t bd = ptx::smem_desc(va + kk * 512, AT_BOX, 256, ptx::kLayoutSw32);
-                            ptx::mma_bf16_ss(tmem + 256 + g * 128, ad, bd, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                            // V: keys are the K dimension (rows), head columns the N dimension
+                            // (MN-major); 16 keys = 16 rows of 128 bytes
+                            const uint64_t bd = ptx::smem_desc(va + kk * 2048, 16, 1024, ptx::kLayoutSw128);
+                            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                            if (PT) {
+                                // P: 16 keys = 8 columns of bf16 pairs per k step
+                                ptx::mma_bf16_ts(tO, tO + 64 + kk * 8, bd, idO64, acc);
+                            } else {
+                                const uint32_t pa = ptx::smem_addr(sP + g * L::P_BYTES);
+                                const uint64_t ad = ptx::smem_desc(pa + (kk >> 2) * (AT_ROWS * 128) + (kk & 3) * 32,
+                                                                   16, 1024, ptx::kLayoutSw128);
+                                ptx::mma_bf16_ss(tO, ad, bd, idO64, acc);
+                                if (L::TAIL) {
+                                    // head columns 64..79 from the 16-column box (32-byte rows)
+                                    const uint64_t bt = ptx::smem_desc(va + AT_BOX64 + kk * 512, 16, 256,
+                                                                       ptx::kLayoutSw32);
+                                    ptx::mma_bf16_ss(tO + 64, ad, bt, idO16, acc);
+                                }
+                            }
                         }
                         ptx::mma_commit(&bars->o_done[g]);
                         ++pc[g];
                         if (g == nact - 1) ptx::mma_commit(&bars->kv_empty[st]);
                         if (j + 1 < p.nkt) {
                             if (!issue_S(g, j + 1)) { ok = false; break; }
-                            if (j + 1 == p.nkt - 1 && g == nact - 1) ptx::mma_commit(&bars->q_empty);
+                            if (j + 1 == p.nkt - 1 && g == nact - 1) ptx::mma_commit(&bars->q_empty[qb]);
                         }
                     }
                 }
@@ -248,7 +297,8 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + g * AT_KEYS + lane_off;
         const uint32_t tO = tmem + 256 + g * 128 + lane_off;
-        uint8_t* prow = sP + g * L::P_BYTES + r * 128;   // + chunk * 16 KB
+        const uint32_t tP = tO + 64;
+        uint8_t* prow = sP + g * L::P_BYTES + r * 128;   // + chunk * 16 KB (staged P)
         const float sl2 = p.scale_log2;
         uint32_t tt = 0;
         bool ok = true;
@@ -256,81 +306,85 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
             int n, h, q0, nact;
             item_decode(p, item, n, h, q0, nact);
             if (g >= nact) continue;
+            // a warp whose 32 query rows all lie past T has no output: it only keeps the
+            // barrier protocol (its rows of P and O are never read back)
+            const bool live = q0 + g * AT_ROWS + quarter * 32 < p.T;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < p.nkt; ++j, ++tt) {
                 ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->s_full[g], tt & 1, abort_flag));
                 if (!ok) break;
-                ptx::tc_fence_after();
-                const int valid = min(AT_KEYS, p.T - j * AT_KEYS);
-                // pass 1: maximum over the valid keys of this row
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < AT_KEYS / 32; ++c) {
-                    if (c * 32 < valid) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            if (c * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(v[e]));
-                    }
-                }
-                const float m_new = fmaxf(m, mx * sl2);
-                const float alpha = exp2_approx(m - m_new);
                 if (j > 0) {
                     // P.V of the previous tile must be done: it reads P, and O is rescaled
                     ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
                     if (!ok) break;
-                    ptx::tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha < 1.f)) {
+                }
+                ptx::tc_fence_after();
+                if (live) {
+                    const int valid = min(AT_KEYS, p.T - j * AT_KEYS);
+                    uint32_t sv[AT_KEYS];
+#pragma unroll
+                    for (int c = 0; c < AT_KEYS / 32; ++c)
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+                    ptx::tmem_ld_wait();
+                    if (valid < AT_KEYS) {
+#pragma unroll
+                        for (int e = 0; e < AT_KEYS; ++e)
+                            if (e >= valid) sv[e] = __float_as_uint(-INFINITY);
+                    }
+                    // row maximum, eight independent chains
+                    float mx[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[e]);
+#pragma unroll
+                    for (int e = 8; e < AT_KEYS; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[e]));
+                    const float mrow = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    const float m_new = fmaxf(m, mrow * sl2);
+                    const float alpha = exp2_approx(m - m_new);
+                    if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+                        // rescale this row of O, 16 columns at a time (S is still live)
 #pragma unroll
                         for (int c = 0; c < DH / 16; ++c) {
-                            uint32_t v[16];
-                            ptx::tmem_ld_32x32b_x16(tO + c * 16, v);
+                            uint32_t ov[16];
+                            ptx::tmem_ld_32x32b_x16(tO + c * 16, ov);
                             ptx::tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-                            ptx::tmem_st_32x32b_x16(tO + c * 16, v);
+                            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                            ptx::tmem_st_32x32b_x16(tO + c * 16, ov);
                         }
-                        ptx::tmem_st_wait();
                     }
-                }
-                l *= alpha;
-                m = m_new;
-                // pass 2: P = exp2(s * scale - m) in bf16, 0 past the valid keys
+                    m = m_new;
+                    // P = exp2(s * scale - m) (masked keys give exp2(-inf) = 0) in bf16
+                    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < AT_KEYS / 32; ++c) {
-                    uint32_t pk[16];
-                    if (c * 32 < valid) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v);
-                        ptx::tmem_ld_wait();
+                    for (int c = 0; c < AT_KEYS / 32; ++c) {
+                        uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 32; e += 2) {
-                            const float p0 = (c * 32 + e < valid)
-                                                 ? exp2_approx(fmaf(__uint_as_float(v[e]), sl2, -m)) : 0.f;
-                            const float p1 = (c * 32 + e + 1 < valid)
-                                                 ? exp2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m)) : 0.f;
-                            l += p0 + p1;
+                            const float p0 = exp2_approx(fmaf(__uint_as_float(sv[c * 32 + e]), sl2, -m));
+                            const float p1 = exp2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 1]), sl2, -m));
+                            ls[(e >> 1) & 7] += p0 + p1;
                             pk[e >> 1] = pack_bf16x2(p0, p1);
                         }
-                    } else {
+                        if (PT) {
+                            ptx::tmem_st_32x32b_x16(tP + c * 16, pk);
+                        } else {
+                            // four 16-byte units of the 128B-swizzled row (64 keys per row)
+                            uint8_t* base = prow + (c >> 1) * (AT_ROWS * 128);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                            for (int q = 0; q < 4; ++q) {
+                                const int unit = (c & 1) * 4 + q;
+                                *reinterpret_cast<uint4*>(base + ((unit ^ (r & 7)) << 4)) =
+                                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                            }
+                        }
                     }
-                    // 32 keys = four 16-byte units of this row in chunk c/2 (64 keys per
-                    // 128-byte row), placed with the 128-byte swizzle (unit ^ row % 8)
-                    uint8_t* base = prow + (c >> 1) * (AT_ROWS * 128);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int unit = (c & 1) * 4 + q;
-                        uint4 w = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        *reinterpret_cast<uint4*>(base + ((unit ^ (r & 7)) << 4)) = w;
-                    }
+                    l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
+                    ptx::tmem_st_wait();
                 }
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bars->s_free[g]);
-                ptx::fence_proxy_async_smem();
+                if (!PT) ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bars->p_full[g]);
             }
             if (!ok) break;
@@ -338,26 +392,25 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const AtParams p) {
             ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
             if (!ok) break;
             ptx::tc_fence_after();
-            const float inv = 1.f / l;
-            const int t = q0 + g * AT_ROWS + r;
-            __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * DH;
+            if (live) {
+                uint32_t ov[DH];
 #pragma unroll
-            for (int c = 0; c < DH / 16; ++c) {
-                uint32_t v[16];
-                ptx::tmem_ld_32x32b_x16(tO + c * 16, v);
+                for (int c = 0; c < DH / 16; ++c)
+                    ptx::tmem_ld_32x32b_x16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[c * 16]));
                 ptx::tmem_ld_wait();
+                const float inv = 1.f / l;
+                const int t = q0 + g * AT_ROWS + r;
                 if (t < p.T) {
-                    uint4 w0, w1;
-                    w0.x = pack_bf16x2(__uint_as_float(v[0]) * inv, __uint_as_float(v[1]) * inv);
-                    w0.y = pack_bf16x2(__uint_as_float(v[2]) * inv, __uint_as_float(v[3]) * inv);
-                    w0.z = pack_bf16x2(__uint_as_float(v[4]) * inv, __uint_as_float(v[5]) * inv);
-                    w0.w = pack_bf16x2(__uint_as_float(v[6]) * inv, __uint_as_float(v[7]) * inv);
-                    w1.x = pack_bf16x2(__uint_as_float(v[8]) * inv, __uint_as_float(v[9]) * inv);
-                    w1.y = pack_bf16x2(__uint_as_float(v[10]) * inv, __uint_as_float(v[11]) * inv);
-                    w1.z = pack_bf16x2(__uint_as_float(v[12]) * inv, __uint_as_float(v[13]) * inv);
-                    w1.w = pack_bf16x2(__uint_as_float(v[14]) * inv, __uint_as_float(v[15]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c * 16) = w0;
-                    *reinterpret_cast<uint4*>(orow + c * 16 + 8) = w1;
+                    __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * DH;
+#pragma unroll
+                    for (int c = 0; c < DH / 8; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c * 8) = w;
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -395,22 +448,28 @@ EncodeTiledFn at_encode_fn() {
     return fn;
 }
 
-template <int DH>
+template <int DH, bool PT>
 cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
                          const DeviceInfo& dev, cudaStream_t s) {
-    using L = AtLayout<DH>;
+    using L = AtLayout<DH, PT>;
     EncodeTiledFn fn = at_encode_fn();
     if (!fn) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap tm;
+    alignas(64) CUtensorMap tm, tm16;
     cuuint64_t dims[3] = {(cuuint64_t)(3 * D), (cuuint64_t)T, (cuuint64_t)N};
     cuuint64_t strides[2] = {(cuuint64_t)(3 * D * 2), (cuuint64_t)(T * 3 * D * 2)};
-    cuuint32_t box[3] = {16, AT_ROWS, 1};
+    cuuint32_t box[3] = {64, AT_ROWS, 1};
+    cuuint32_t box16[3] = {16, AT_ROWS, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (fn(&tm16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box16, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     AtParams p;
+    p.tail_maps = DH == 80;
     p.N = (int)N;
     p.T = (int)T;
     p.D = (int)D;
@@ -424,13 +483,13 @@ cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t
     p.err = dev.err_word;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<DH>,
+        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<DH, PT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
-    attention_tc_kernel<DH><<<grid, AT_THREADS, L::SMEM, s>>>(tm, p);
+    attention_tc_kernel<DH, PT><<<grid, AT_THREADS, L::SMEM, s>>>(tm, tm16, p);
     return cudaGetLastError();
 }
 
@@ -451,8 +510,8 @@ cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, 
                                 const DeviceInfo& dev, cudaStream_t s) {
     if (N <= 0 || T <= 0) return cudaSuccess;
     switch (D / H) {
-        case 64: return launch_tc_dh<64>(qkv, o, N, T, D, H, dev, s);
-        case 80: return launch_tc_dh<80>(qkv, o, N, T, D, H, dev, s);
+        case 64: return launch_tc_dh<64, true>(qkv, o, N, T, D, H, dev, s);
+        case 80: return launch_tc_dh<80, false>(qkv, o, N, T, D, H, dev, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -18,8 +18,9 @@ enum : uint32_t {
     ERRBIT_TIMEOUT_ATTENTION = 1u << 4,
 };
 
-// One bounded device-side wait gives up after this many nanoseconds.
-constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+// One bounded device-side wait gives up after this many SM clock cycles (about two
+// seconds at 2 GHz; longer at lower clocks).
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
