@@ -311,6 +311,103 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 }
 
 
+
+// Residual values of 32 columns of one row (nothing for other epilogues or past M/N).
+template <int EPI, typename ResT>
+__device__ __forceinline__ void epilogue_prefetch(const Params& p, int row, int col, float (&rv)[32]) {
+    if (EPI == TC_EPI_RESID && row < p.M && col < p.N)
+        load32(reinterpret_cast<const ResT*>(p.residual) + (int64_t)row * p.ldr + col, rv);
+}
+
+// 32 values of one output row inside a 32-row staging tile that a TMA store writes
+// out. fp32: 128-byte rows with the 128-byte swizzle (16-byte unit u of row r at
+// u ^ (r % 8)); bf16: 64-byte rows with the 64-byte swizzle (unit u at u ^ (r / 2 % 4)).
+// Each group of eight rows touches eight distinct 16-byte bank groups: no conflicts.
+template <typename T> struct StageIO;
+template <> struct StageIO<float> {
+    static constexpr int ROW_BYTES = 128;
+    __device__ static void write(uint8_t* buf, int r, const float (&v)[32]) {
+        uint8_t* row = buf + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(row + ((u ^ (r & 7)) << 4)) =
+                make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+    }
+};
+template <> struct StageIO<__nv_bfloat16> {
+    static constexpr int ROW_BYTES = 64;
+    __device__ static void write(uint8_t* buf, int r, const float (&v)[32]) {
+        uint8_t* row = buf + r * 64;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * u + 0], v[8 * u + 1]);
+            w.y = pack_bf16x2(v[8 * u + 2], v[8 * u + 3]);
+            w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
+            w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
+            *reinterpret_cast<uint4*>(row + ((u ^ ((r >> 1) & 3)) << 4)) = w;
+        }
+    }
+};
+
+constexpr int EPI_STAGE_BYTES = 32 * 128;   // one 32 x 32 staging tile (fp32 size)
+
+// Epilogue of this warp's 32 rows x 256 columns: TMEM -> registers (bias, GELU or
+// residual) -> swizzled shared staging -> TMA store, 32 columns at a time, two staging
+// tiles per warp so a store drains while the next chunk is computed. The residual
+// of the next chunk is loaded into registers while the current one is processed.
+template <int EPI, typename OutT, typename ResT>
+__device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
+                                                  uint8_t* stage, uint32_t t_row, int row, int row0,
+                                                  int n0, int lane) {
+    float rv[32];
+    epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
+        const int col = n0 + c * 32;
+        float rnext[32];
+        if (c + 1 < BN / 32) epilogue_prefetch<EPI, ResT>(p, row, col + 32, rnext);
+        ptx::tmem_ld_wait();
+        float val[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
+        if (col < p.N) {
+            if (p.bias) {
+                float b[32];
+                load32(p.bias + col, b);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] += b[j];
+            }
+            if (EPI == TC_EPI_GELU) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
+            } else if (EPI == TC_EPI_RESID) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] += rv[j];
+            }
+        }
+        if (EPI == TC_EPI_RESID && c + 1 < BN / 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) rv[j] = rnext[j];
+        }
+        if (col < p.N) {
+            uint8_t* buf = stage + (c & 1) * EPI_STAGE_BYTES;
+            // the store issued from this buffer two chunks ago must have read it
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+            StageIO<OutT>::write(buf, lane, val);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::tma_store_2d(tmOut, buf, col, row0);
+                ptx::bulk_commit_group();
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ CTA-pair kernel
 // Two CTAs of a cluster (ranks 0 and 1, on a TPC's two SMs) compute one 256 x 256 output
 // tile with tcgen05.mma.cta_group::2 (M 256 = 128 rows per CTA, N 256): each CTA loads
@@ -323,22 +420,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 //   the leader's barrier), and four epilogue warps reading their own TMEM rows; the
 //   epilogue threads of both CTAs release an accumulator on the leader's barrier.
 constexpr int P_STAGES = 6;
+constexpr int P_THREADS = 288;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
+                                // warp 1: MMA; warps 5-8: epilogue
 constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's 128 weight columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int P_EPI_BYTES = 4 * 2 * EPI_STAGE_BYTES;   // 4 epilogue warps x 2 staging tiles
+constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_EPI_BYTES + BAR_BYTES + 1024;
 
 template <int EPI, typename OutT, typename ResT>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmOut, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + P_STAGES * P_A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P_STAGES * P_STAGE_BYTES);
+    uint8_t* sEpi = smem + P_STAGES * P_STAGE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + P_EPI_BYTES);
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -372,6 +473,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         ptx::prefetch_tensormap(&tmB0);
         if (p.n_w > 1) ptx::prefetch_tensormap(&tmB1);
         if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
+        ptx::prefetch_tensormap(&tmOut);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -382,9 +484,13 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    if (warp == 0) {
+    // TMA issue from one thread is serialised (roughly one box at a time), so four warps
+    // each issue one 64-row box per stage: A rows 0-63, A rows 64-127, weight columns
+    // 0-63 and 64-127 of this CTA's half.
+    const int prod = warp == 0 ? 0 : (warp >= 2 && warp <= 4) ? warp - 1 : -1;
+    if (prod >= 0) {
         if (lane == 0) {
-            // -------------------------------------------- TMA producer (both ranks)
+            // -------------------------------------------- TMA producers (both ranks)
             const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(full), 0);  // leader's
             uint32_t it = 0;
             bool ok = true;
@@ -397,18 +503,19 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ok = false;
                         break;
                     }
-                    if (rank == 0) ptx::mbar_arrive_expect_tx(full + s, 2 * P_STAGE_BYTES);
+                    if (prod == 0 && rank == 0) ptx::mbar_arrive_expect_tx(full + s, 2 * P_STAGE_BYTES);
                     const uint32_t fb = full0 + s * 8;
-                    ptx::tma_load_2d_pair(sA + s * P_A_BYTES, &tmA, fb, kb * BK, m0);
-#pragma unroll
-                    for (int j = 0; j < BN / 128; ++j) {
+                    if (prod < 2) {
+                        ptx::tma_load_2d_pair(sA + s * P_A_BYTES + prod * (P_A_BYTES / 2), &tmA, fb, kb * BK,
+                                              m0 + prod * (BM / 2));
+                    } else {
+                        const int j = prod - 2;
                         const int col = n0 + 64 * j;
                         int wi = col / p.n_per_w;
                         if (wi > p.n_w - 1) wi = p.n_w - 1;  // past N: zero-filled box
                         const int lc = col - wi * p.n_per_w;
                         const CUtensorMap* tb = wi == 0 ? &tmB0 : (wi == 1 ? &tmB1 : &tmB2);
-                        ptx::tma_load_2d_pair(sB + s * P_B_BYTES + j * B_BOX_BYTES, tb, fb, lc,
-                                              kb * BK);
+                        ptx::tma_load_2d_pair(sB + s * P_B_BYTES + j * B_BOX_BYTES, tb, fb, lc, kb * BK);
                     }
                 }
             }
@@ -416,8 +523,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 set_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
                 *abort_flag = 1;
             }
-            if (rank == 0) {
-                // both CTAs' copies complete on these barriers: let them land
+            if (prod == 0 && rank == 0) {
+                // every copy of both CTAs completes on these barriers: let them land
                 for (uint32_t s = 0; s < P_STAGES; ++s) {
                     if (it > s) {
                         const uint32_t u_last = (it - 1 - s) / P_STAGES;
@@ -472,7 +579,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!ptx::mbar_wait_bounded(done, 0, nullptr)) set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
     } else {
-        // ---------------------------------------------- epilogue warps 2..5 (both ranks)
+        // ---------------------------------------------- epilogue warps 5..8 (both ranks)
         const int quarter = warp & 3;
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);  // leader's
         int local = 0;
@@ -488,12 +595,14 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::tc_fence_after();
             const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
             const int n0 = (tile % n_tiles) * BN;
-            const int row = m0 + quarter * 32 + lane;
+            const int row0 = m0 + quarter * 32;
             const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile<EPI, OutT, ResT>(p, t_row, row, n0);
+            epilogue_tile_tma<EPI, OutT, ResT>(p, &tmOut, sEpi + (warp - 5) * 2 * EPI_STAGE_BYTES, t_row,
+                                               row0 + lane, row0, n0, lane);
             ptx::tc_fence_before();
             ptx::mbar_arrive_cluster(tempty0 + acc * 8);
         }
+        if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }
 
     __syncthreads();
@@ -539,6 +648,23 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int6
     return r == CUDA_SUCCESS;
 }
 
+// Output (rows, cols) of fp32 or bf16, row stride ld elements; 32 x 32 boxes with the
+// swizzle matching StageIO (128B for fp32 rows of 128 bytes, 64B for bf16).
+bool make_map_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld, bool f32) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int es = f32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int EPI, typename OutT, typename ResT>
 cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params& p, int grid,
                         cudaStream_t s) {
@@ -554,8 +680,8 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params
 }
 
 template <int EPI, typename OutT, typename ResT>
-cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const Params& p, int grid,
-                             cudaStream_t s) {
+cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
+                             const Params& p, int grid, cudaStream_t s) {
     auto k = gemm_tc_pair_kernel<EPI, OutT, ResT>;
     static bool attr_set = false;
     if (!attr_set) {
@@ -563,14 +689,14 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const P
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], p);
+    k<<<grid, P_THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], out, p);
     return cudaGetLastError();
 }
 
 template <int EPI, typename OutT, typename ResT>
-cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const Params& p,
-                       int grid, cudaStream_t s) {
-    return pair ? launch_inst_pair<EPI, OutT, ResT>(a, b, p, grid, s)
+cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
+                       const Params& p, int grid, cudaStream_t s) {
+    return pair ? launch_inst_pair<EPI, OutT, ResT>(a, b, out, p, grid, s)
                 : launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
 }
 
@@ -607,11 +733,15 @@ bool tc_gemm_supported(const TcGemmDesc& d) {
 cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStream_t s) {
     alignas(64) CUtensorMap ma;
     alignas(64) CUtensorMap mb[3];
-    if (!make_map(&ma, d.a, d.M, d.K, d.lda, BK, BM)) return cudaErrorInvalidValue;
+    const bool pair = use_pair_kernel() && dev.num_sms >= 2;
+    // the pair kernel loads A as two 64-row boxes from two warps
+    if (!make_map(&ma, d.a, d.M, d.K, d.lda, BK, pair ? BM / 2 : BM)) return cudaErrorInvalidValue;
     for (int i = 0; i < 3; ++i) {
         const void* w = d.w[i < d.n_w ? i : 0];
         if (!make_map(&mb[i], w, d.K, d.n_per_w, d.n_per_w, 64, BK)) return cudaErrorInvalidValue;
     }
+    alignas(64) CUtensorMap mo;
+    if (!make_map_out(&mo, d.out, d.M, d.N, d.ldo, d.out_f32)) return cudaErrorInvalidValue;
     Params p;
     p.M = (int)d.M;
     p.N = (int)d.N;
@@ -624,7 +754,6 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     p.out = d.out;
     p.ldo = d.ldo;
     p.err = dev.err_word;
-    const bool pair = use_pair_kernel() && dev.num_sms >= 2;
     int grid;
     if (pair) {
         const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN);
@@ -636,19 +765,19 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     }
     switch (d.epi) {
         case TC_EPI_STORE:
-            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, p, grid, s)
-                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, p, grid, s)
+                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s);
         case TC_EPI_GELU:
-            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, p, grid, s)
-                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, p, grid, s)
+                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s);
         case TC_EPI_RESID:
             if (d.out_f32)
                 return d.residual_f32
-                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, p, grid, s)
-                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, p, grid, s);
+                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, p, grid, s)
+                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, p, grid, s);
             return d.residual_f32
-                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, p, grid, s)
-                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, p, grid, s);
+                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s)
+                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
