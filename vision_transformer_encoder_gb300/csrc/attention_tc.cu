@@ -9,8 +9,9 @@
 //
 // Persistent kernel, one CTA per SM. A work item is (sequence, head, pair of 128-row
 // query tiles), so one pass over the keys serves 256 queries (T = 197 is one item).
-//   warp 0      TMA: the item's query tiles, then 128-key K and V tiles into a 2-stage
-//               ring. A 3-D tensor map (column, token, sequence) zero-fills tokens past
+//   warps 0,10,11  TMA: the item's query tiles (warp 0), then 128-key K (warp 10) and
+//               V (warp 11) tiles into a ring; one thread issues its copies one at a time,
+//               so the three streams come from three warps. A 3-D tensor map (column, token, sequence) zero-fills tokens past
 //               T, so tiles never read the next sequence. A head slice is one 64-column
 //               box with the 128-byte swizzle, plus, for dh = 80, one 16-column box with
 //               the 32-byte swizzle (the MMAs for that part use a second descriptor).
@@ -46,7 +47,7 @@ namespace {
 constexpr int AT_ROWS = 128;       // query rows per tile (TMEM lanes)
 constexpr int AT_KEYS = 128;       // keys per K/V tile
 constexpr int AT_MAX_KV = 4;
-constexpr int AT_THREADS = 320;    // 10 warps
+constexpr int AT_THREADS = 384;    // 12 warps: 0 Q loads, 1 MMA, 2-9 softmax, 10 K loads, 11 V loads
 constexpr int AT_BOX64 = AT_ROWS * 128;  // 64 columns x 128 rows, 128B swizzle: 16 KB
 constexpr int AT_BOX16 = AT_ROWS * 32;   // 16 columns x 128 rows, 32B swizzle: 4 KB
 
@@ -156,35 +157,37 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
     // columns of bf16 pairs) right after O_g at 256 + 128 g + 64.
     const int D = p.D;
 
-    if (warp == 0) {
+    if (warp == 0 || warp >= 10) {
         if (lane == 0) {
-            // ------------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producers: one thread
+            // issues its boxes one after another, so Q, K and V come from three warps
+            const int role = warp == 0 ? 0 : warp - 9;   // 0 Q, 1 K, 2 V
             uint32_t kv_it = 0, ii = 0;
             bool ok = true;
             for (int item = blockIdx.x; item < p.items && ok; item += gridDim.x, ++ii) {
                 int n, h, q0, nact;
                 item_decode(p, item, n, h, q0, nact);
-                const uint32_t qb = ii % QB, qu = ii / QB;
-                if (!ptx::mbar_wait_bounded(&bars->q_empty[qb], (qu & 1) ^ 1, abort_flag)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(&bars->q_full[qb], nact * L::TILE);
-                for (int g = 0; g < nact; ++g) {
-                    uint8_t* dq = sQ + (qb * 2 + g) * L::TILE;
-                    ptx::tma_load_3d(dq, &tm, &bars->q_full[qb], h * DH, q0 + g * AT_ROWS, n);
-                    if (L::TAIL)
-                        ptx::tma_load_3d(dq + AT_BOX64, &tm16, &bars->q_full[qb], h * DH + 64, q0 + g * AT_ROWS, n);
+                if (role == 0) {
+                    const uint32_t qb = ii % QB, qu = ii / QB;
+                    if (!ptx::mbar_wait_bounded(&bars->q_empty[qb], (qu & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&bars->q_full[qb], nact * L::TILE);
+                    for (int g = 0; g < nact; ++g) {
+                        uint8_t* dq = sQ + (qb * 2 + g) * L::TILE;
+                        ptx::tma_load_3d(dq, &tm, &bars->q_full[qb], h * DH, q0 + g * AT_ROWS, n);
+                        if (L::TAIL)
+                            ptx::tma_load_3d(dq + AT_BOX64, &tm16, &bars->q_full[qb], h * DH + 64, q0 + g * AT_ROWS, n);
+                    }
+                    continue;
                 }
+                const int col = (role == 1 ? D : 2 * D) + h * DH;
+                uint8_t* ring = role == 1 ? sK : sV;
                 for (int j = 0; j < p.nkt; ++j, ++kv_it) {
                     const uint32_t st = kv_it % KVS, u = kv_it / KVS;
                     if (!ptx::mbar_wait_bounded(&bars->kv_empty[st], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
-                    ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::TILE);
-                    uint8_t* dk = sK + st * L::TILE;
-                    uint8_t* dv = sV + st * L::TILE;
-                    ptx::tma_load_3d(dk, &tm, &bars->kv_full[st], D + h * DH, j * AT_KEYS, n);
-                    ptx::tma_load_3d(dv, &tm, &bars->kv_full[st], 2 * D + h * DH, j * AT_KEYS, n);
-                    if (L::TAIL) {
-                        ptx::tma_load_3d(dk + AT_BOX64, &tm16, &bars->kv_full[st], D + h * DH + 64, j * AT_KEYS, n);
-                        ptx::tma_load_3d(dv + AT_BOX64, &tm16, &bars->kv_full[st], 2 * D + h * DH + 64, j * AT_KEYS, n);
-                    }
+                    if (role == 1) ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::TILE);
+                    uint8_t* dst = ring + st * L::TILE;
+                    ptx::tma_load_3d(dst, &tm, &bars->kv_full[st], col, j * AT_KEYS, n);
+                    if (L::TAIL) ptx::tma_load_3d(dst + AT_BOX64, &tm16, &bars->kv_full[st], col + 64, j * AT_KEYS, n);
                 }
             }
             if (!ok) {
@@ -192,12 +195,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
                 *abort_flag = 1;
             }
             // let in-flight copies land before the CTA can exit
-            for (uint32_t b = 0; b < (uint32_t)QB; ++b)
-                if (ii > b && !ptx::mbar_wait_bounded(&bars->q_full[b], ((ii - 1 - b) / QB) & 1, nullptr))
-                    at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-            for (uint32_t s = 0; s < (uint32_t)KVS; ++s)
-                if (kv_it > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((kv_it - 1 - s) / KVS) & 1, nullptr))
-                    at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            if (role == 0) {
+                for (uint32_t b = 0; b < (uint32_t)QB; ++b)
+                    if (ii > b && !ptx::mbar_wait_bounded(&bars->q_full[b], ((ii - 1 - b) / QB) & 1, nullptr))
+                        at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            } else {
+                for (uint32_t s = 0; s < (uint32_t)KVS; ++s)
+                    if (kv_it > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((kv_it - 1 - s) / KVS) & 1, nullptr))
+                        at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -289,7 +295,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
             ptx::mma_commit(&bars->done);
             if (!ptx::mbar_wait_bounded(&bars->done, 0, nullptr)) at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 9) {
         // -------------------------------------------------------- softmax groups
         const int g = (warp - 2) >> 2;          // 0: warps 2-5, 1: warps 6-9
         const int quarter = warp & 3;           // TMEM lane quarter this warp may access
