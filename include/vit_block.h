@@ -106,6 +106,37 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
                    const void* b2_host, int64_t N, int64_t T, int64_t D, int64_t F,
                    int64_t H, double eps, int dtype, void* out_host, void* stream);
 
+/*
+ * vit_block_noalloc -- vit_block_ex that allocates no device memory.
+ *
+ * No counterpart on the pages this library follows: it exists for callers that cannot
+ * call cudaMalloc or use a memory pool while the block runs -- for example a host
+ * application that reserves all device memory up front under a fixed budget, or code
+ * running where allocation calls are not allowed. Arguments, layouts, results and
+ * errors are those of vit_block_ex; inputs and `out` are still the caller's.
+ *
+ * Scratch: instead of the stream-ordered pool, the call uses one fixed array of
+ * 64 MiB (67,108,864 bytes) that the library keeps in device memory on every GPU that
+ * loads it, until the process exits. A call whose scratch would exceed 64 MiB returns
+ * VIT_ERR_UNSUPPORTED before launching anything. (Scratch per token: 12 D + 2 F bytes
+ * on the bf16 tensor-core path, e.g. 15,360 bytes for D 768 / F 3072, so 4,369
+ * tokens; (5 D + F) times the element size on the other paths.) The call makes no
+ * cudaMalloc, cudaFree or other allocating call, and nothing in the array needs to be
+ * cleared: every scratch byte is written before it is read.
+ *
+ * The first call on a device looks up the array's device address (a one-time set-up
+ * per device, made with that device current); make that first call before any stream
+ * capture. All calls share the one array: calls that may overlap on the GPU (on
+ * different streams, or from several host threads) race on it and must be ordered by
+ * the caller.
+ */
+int vit_block_noalloc(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                      const void* w_o, const void* w_mlp1, const void* w_mlp2,
+                      const void* ln1_g, const void* ln1_b, const void* ln2_g,
+                      const void* ln2_b, const void* b1, const void* b2,
+                      int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+                      double eps, int dtype, void* out, void* stream);
+
 /* ------------------------------------------------------------------------------
  * Step-level entry points: each runs one stage of the block on its own. They use
  * the same kernels as vit_block and exist for stage-by-stage checking and for

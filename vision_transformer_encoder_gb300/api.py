@@ -27,6 +27,7 @@ SIGNATURES = {
     "vit_block": (_int, [_vp] * 7 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_block_ex": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_block_host": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
+    "vit_block_noalloc": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
     "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
     "vit_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _vp, _vp]),

@@ -182,26 +182,38 @@ bool fast_path_ok(const BlockArgs& a) {
     return true;
 }
 
-int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+// Scratch layout of one block call: buf (xn, then o, then yn) | qkv | y | h, each
+// rounded up to 256 bytes. Every byte is written before it is read.
+struct Workspace {
+    bool fast;
+    int acc_dt;
+    size_t sz_buf, sz_qkv, sz_y, sz_h, total;
+};
+
+Workspace workspace_layout(const BlockArgs& a) {
+    Workspace w;
     const int64_t M = a.N * a.T, D = a.D, F = a.F;
-    const bool fast = fast_path_ok(a);
-    const int acc_dt = fast ? DT_BF16 : (a.dt == DT_F64 ? DT_F64 : DT_F32);
+    w.fast = fast_path_ok(a);
+    w.acc_dt = w.fast ? DT_BF16 : (a.dt == DT_F64 ? DT_F64 : DT_F32);
+    const size_t ea = dt_size(w.acc_dt);
+    w.sz_buf = round_up((size_t)(M * D) * ea, 256);
+    w.sz_qkv = round_up((size_t)(M * 3 * D) * ea, 256);
+    w.sz_y = round_up((size_t)(M * D) * (w.fast ? 4 : ea), 256);
+    w.sz_h = round_up((size_t)(M * F) * ea, 256);
+    w.total = w.sz_buf + w.sz_qkv + w.sz_y + w.sz_h;
+    return w;
+}
+
+// Enqueues the seven steps of the block on `s`, using `ws` (at least w.total bytes)
+// as scratch.
+cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s,
+                               const Workspace& w, void* ws) {
+    const int64_t M = a.N * a.T, D = a.D, F = a.F;
+    const bool fast = w.fast;
+    const int acc_dt = w.acc_dt;
     const size_t ea = dt_size(acc_dt);
-    // scratch: buf (xn, then o, then yn) | qkv | y | h
-    const size_t sz_buf = round_up((size_t)(M * D) * ea, 256);
-    const size_t sz_qkv = round_up((size_t)(M * 3 * D) * ea, 256);
-    const size_t sz_y = round_up((size_t)(M * D) * (fast ? 4 : ea), 256);
-    const size_t sz_h = round_up((size_t)(M * F) * ea, 256);
-    const size_t total = sz_buf + sz_qkv + sz_y + sz_h;
-    DeviceState* st = nullptr;
-    int rc = current_device(&st);
-    if (rc != VIT_OK) return rc;
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, st->pool, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
-    }
+    const size_t sz_buf = w.sz_buf, sz_qkv = w.sz_qkv, sz_y = w.sz_y;
+    cudaError_t e = cudaSuccess;
     uint8_t* base = static_cast<uint8_t*>(ws);
     void* buf = base;
     void* qkv = base + sz_buf;
@@ -310,6 +322,21 @@ int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
             return launch_gemm_simt(w, s);
         }));
     }
+    return e;
+}
+
+int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+    const Workspace w = workspace_layout(a);
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, w.total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
+    }
+    e = launch_block_steps(a, dev, s, w, ws);
     cudaError_t fe = cudaFreeAsync(ws, s);
     if (e == cudaSuccess) e = fe;
     if (e != cudaSuccess) {
@@ -322,6 +349,50 @@ int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
         if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
         if (w) return VIT_ERR_TIMEOUT;
     }
+    return VIT_OK;
+}
+
+// ---- scratch for vit_block_noalloc ---------------------------------------------
+// For callers that cannot allocate device memory, vit_block_noalloc runs the block with
+// its scratch in this fixed, library-owned array instead of the stream-ordered pool.
+// Every device that loads the library holds it until the process exits. Kernels never
+// read a byte of it before writing it, so nothing needs clearing between calls.
+constexpr size_t kNoAllocScratchBytes = (size_t)64 << 20;
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocState {
+    bool ready = false;
+    DeviceInfo info;
+    void* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+// Per-device set-up, on the first call with that device current: device attributes and
+// the device addresses of the scratch array and the error word (in host code the
+// array's name is only a host-side stand-in, so its address must be looked up).
+// Nothing here allocates.
+int noalloc_device(NoAllocState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return VIT_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    NoAllocState& st = g_noalloc[dev];
+    if (!st.ready) {
+        DeviceInfo info;
+        info.device = dev;
+        if (cudaDeviceGetAttribute(&info.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&info.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return VIT_ERR_CUDA;
+        void* err = nullptr;
+        if (cudaGetSymbolAddress(&err, g_err_word) != cudaSuccess) return VIT_ERR_CUDA;
+        info.err_word = static_cast<uint32_t*>(err);
+        void* scratch = nullptr;
+        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) return VIT_ERR_CUDA;
+        st.info = info;
+        st.scratch = scratch;
+        st.ready = true;
+    }
+    *out = &st;
     return VIT_OK;
 }
 
@@ -503,6 +574,35 @@ int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, i
     if (e != cudaSuccess) {
         cudaGetLastError();
         return status_from(e);
+    }
+    return VIT_OK;
+}
+
+int vit_block_noalloc(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                      const void* w_o, const void* w_mlp1, const void* w_mlp2, const void* ln1_g,
+                      const void* ln1_b, const void* ln2_g, const void* ln2_b, const void* b1,
+                      const void* b2, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+                      double eps, int dtype, void* out, void* stream) {
+    BlockArgs a{x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, ln1_g, ln1_b, ln2_g, ln2_b, b1, b2,
+                N, T, D, F, H, eps, dtype, out};
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    const Workspace w = workspace_layout(a);
+    if (w.total > kNoAllocScratchBytes) return VIT_ERR_UNSUPPORTED;
+    NoAllocState* st = nullptr;
+    rc = noalloc_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_block_steps(a, st->info, s, w, st->scratch);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return VIT_ERR_CUDA;
+    }
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+        uint32_t word = 0;
+        if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return VIT_ERR_CUDA;
+        if (word) return VIT_ERR_TIMEOUT;
     }
     return VIT_OK;
 }
