@@ -356,19 +356,19 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;   // one 32 x 32 staging tile (fp32 si
 // residual) -> swizzled shared staging -> TMA store, 32 columns at a time, two staging
 // tiles per warp so a store drains while the next chunk is computed. The residual
 // of the next chunk is loaded into registers while the current one is processed.
-template <int EPI, typename OutT, typename ResT>
+template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS>
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
                                                   uint8_t* stage, uint32_t t_row, int row, int row0,
                                                   int n0, int lane) {
     float rv[32];
     epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    for (int c = 0; c < CHUNKS; ++c) {
         uint32_t r[32];
         ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
         const int col = n0 + c * 32;
         float rnext[32];
-        if (c + 1 < BN / 32) epilogue_prefetch<EPI, ResT>(p, row, col + 32, rnext);
+        if (c + 1 < CHUNKS) epilogue_prefetch<EPI, ResT>(p, row, col + 32, rnext);
         ptx::tmem_ld_wait();
         float val[32];
 #pragma unroll
@@ -388,14 +388,14 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
                 for (int j = 0; j < 32; ++j) val[j] += rv[j];
             }
         }
-        if (EPI == TC_EPI_RESID && c + 1 < BN / 32) {
+        if (EPI == TC_EPI_RESID && c + 1 < CHUNKS) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = rnext[j];
         }
         if (col < p.N) {
-            uint8_t* buf = stage + (c & 1) * EPI_STAGE_BYTES;
-            // the store issued from this buffer two chunks ago must have read it
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            uint8_t* buf = stage + (c % BUFS) * EPI_STAGE_BYTES;
+            // the store issued from this buffer BUFS chunks ago must have read it
+            if (lane == 0) ptx::bulk_wait_group_read<BUFS - 1>();
             __syncwarp();
             StageIO<OutT>::write(buf, lane, val);
             ptx::fence_proxy_async_smem();
@@ -420,12 +420,14 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
 //   the leader's barrier), and four epilogue warps reading their own TMEM rows; the
 //   epilogue threads of both CTAs release an accumulator on the leader's barrier.
 constexpr int P_STAGES = 6;
-constexpr int P_THREADS = 288;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
-                                // warp 1: MMA; warps 5-8: epilogue
+constexpr int P_EPI_WARPS = 8;
+constexpr int P_THREADS = 416;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
+                                // warp 1: MMA; warps 5-12: epilogue
 constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's 128 weight columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
-constexpr int P_EPI_BYTES = 4 * 2 * EPI_STAGE_BYTES;   // 4 epilogue warps x 2 staging tiles
+constexpr int P_EPI_BUFS = 1;   // staging tiles per epilogue warp
+constexpr int P_EPI_BYTES = P_EPI_WARPS * P_EPI_BUFS * EPI_STAGE_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_EPI_BYTES + BAR_BYTES + 1024;
 
 template <int EPI, typename OutT, typename ResT>
@@ -462,7 +464,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(tfull + a, 1);
-            ptx::mbar_init(tempty + a, 2 * 128);
+            ptx::mbar_init(tempty + a, 2 * P_EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
@@ -579,8 +581,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!ptx::mbar_wait_bounded(done, 0, nullptr)) set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
     } else {
-        // ---------------------------------------------- epilogue warps 5..8 (both ranks)
-        const int quarter = warp & 3;
+        // ---------------------------------------------- epilogue warps 5..12 (both ranks)
+        const int quarter = warp & 3;               // TMEM lane quarter this warp may read
+        const int half = (warp - 5) >> 2;           // which 128 of the 256 columns
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);  // leader's
         int local = 0;
         for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
@@ -596,11 +599,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
             const int n0 = (tile % n_tiles) * BN;
             const int row0 = m0 + quarter * 32;
-            const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile_tma<EPI, OutT, ResT>(p, &tmOut, sEpi + (warp - 5) * 2 * EPI_STAGE_BYTES, t_row,
-                                               row0 + lane, row0, n0, lane);
+            const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
+            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS>(p, &tmOut, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row,
+                                                  row0 + lane, row0, n0 + half * 128, lane);
             ptx::tc_fence_before();
-            ptx::mbar_arrive_cluster(tempty0 + acc * 8);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
         }
         if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }
