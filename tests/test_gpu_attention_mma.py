@@ -24,3 +24,16 @@ def test_attention_stages_on_mma_sync_kernel():
                         os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "attention"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_attention_stages_on_cta_pair_kernel():
+    """Head width 64 runs on the single-CTA tcgen05 kernel by default; VIT_ATTN_PAIR=1
+    selects the CTA-pair kernel."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, VIT_ATTN_PAIR="1")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "attention"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
