@@ -64,6 +64,10 @@ def kernel_work(c):
         "ln2": ("hbm", M * D * (4 + 2), "bytes"),          # read y fp32, write yn bf16
         "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),
         "w2_gemm_residual": ("tensor", 2 * M * F * D, "flops"),
+        # LayerNorm folded into the GEMMs (default bf16 path): LN1 reduces to row
+        # statistics of x; the fold's column terms are computed once per call
+        "ln1_row_stats": ("hbm", M * D * 2 + M * 8, "bytes"),
+        "ln_fold_prep": ("hbm", (3 * D * D + D * F) * 2 + (3 * D + F) * 8, "bytes"),
     }
 
 
@@ -337,6 +341,7 @@ def main():
 
     peaks, peak_src = load_peaks()
     work = kernel_work(c)
+    per_kernel = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(per_kernel, key=lambda k: per_kernel[k][0])
     kms, kn = per_kernel[dom]
     bound, amount, _unit = work[dom]

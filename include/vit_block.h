@@ -120,7 +120,8 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
  * loads it, until the process exits. A call whose scratch would exceed 64 MiB returns
  * VIT_ERR_UNSUPPORTED before launching anything. (Scratch per token: 12 D + 2 F bytes
  * on the bf16 tensor-core path, e.g. 15,360 bytes for D 768 / F 3072, so 4,369
- * tokens; (5 D + F) times the element size on the other paths.) The call makes no
+ * tokens; (5 D + F) times the element size on the other paths; more when VIT_LN_FOLD=1
+ * selects the LayerNorm-folded path.) The call makes no
  * cudaMalloc, cudaFree or other allocating call, and nothing in the array needs to be
  * cleared: every scratch byte is written before it is read.
  *

@@ -56,6 +56,9 @@ struct Params {
     void* out;
     int64_t ldo;
     uint32_t* err;
+    TcLnFold fold;
+    float2* parts_out;   // extra outputs: row partials (mean, M2), 2 per 256-column tile
+    int parts_stride;
 };
 
 __device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
@@ -356,12 +359,48 @@ constexpr int EPI_STAGE_BYTES = 32 * 128;   // one 32 x 32 staging tile (fp32 si
 // residual) -> swizzled shared staging -> TMA store, 32 columns at a time, two staging
 // tiles per warp so a store drains while the next chunk is computed. The residual
 // of the next chunk is loaded into registers while the current one is processed.
-template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS>
+template <typename T> __device__ __forceinline__ void load32f(const float* p, float (&v)[32]) {
+    const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 u = __ldg(q + i);
+        v[4 * i + 0] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
+    }
+}
+
+// Mean and 1/sqrt(var + eps) of one row from its partials (mean_k, M2_k) over column
+// ranges of part_cols (the last one may be shorter), merged with Chan's formula.
+__device__ __forceinline__ float2 merge_row_stats(const TcLnFold& f, int row) {
+    float n = 0.f, mean = 0.f, m2 = 0.f;
+    for (int k = 0; k < f.nparts; ++k) {
+        const int rest = f.D - k * f.part_cols;
+        if (rest <= 0) break;
+        const float nb = (float)(rest < f.part_cols ? rest : f.part_cols);
+        const float2 pb = f.parts[(int64_t)row * f.nparts + k];
+        const float nt = n + nb;
+        const float delta = pb.x - mean;
+        mean += delta * (nb / nt);
+        m2 += pb.y + delta * delta * (n * nb / nt);
+        n = nt;
+    }
+    return make_float2(mean, rsqrtf(m2 / (float)f.D + f.eps));
+}
+
+// Epilogue of this warp's 32 rows x (32 * CHUNKS) columns: TMEM -> registers (folded
+// LayerNorm or bias, GELU or residual) -> swizzled shared staging -> TMA store, 32
+// columns at a time. The residual of the next chunk is loaded into registers while the
+// current one is processed. With EXTRA, the same values are also stored as bf16 through
+// tmOut2 and the row's (mean, M2) over these columns is written to p.parts_out.
+template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS, bool FOLD, bool EXTRA>
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
-                                                  uint8_t* stage, uint32_t t_row, int row, int row0,
-                                                  int n0, int lane) {
+                                                  const CUtensorMap* tmOut2, uint8_t* stage,
+                                                  uint32_t t_row, int row, int row0, int n0,
+                                                  int lane, int part_index) {
     float rv[32];
     epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
+    float2 st = make_float2(0.f, 1.f);
+    if (FOLD && row < p.M) st = merge_row_stats(p.fold, row);
+    float cnt = 0.f, cmean = 0.f, cm2 = 0.f;   // EXTRA: running statistics of this row
 #pragma unroll 1
     for (int c = 0; c < CHUNKS; ++c) {
         uint32_t r[32];
@@ -374,7 +413,13 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
 #pragma unroll
         for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
         if (col < p.N) {
-            if (p.bias) {
+            if (FOLD) {
+                float cs[32], cb[32];
+                load32f<float>(p.fold.colsum + col, cs);
+                load32f<float>(p.fold.colbias + col, cb);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) val[j] = fmaf(st.y, fmaf(-st.x, cs[j], val[j]), cb[j]);
+            } else if (p.bias) {
                 float b[32];
                 load32(p.bias + col, b);
 #pragma unroll
@@ -404,21 +449,40 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
                 ptx::tma_store_2d(tmOut, buf, col, row0);
                 ptx::bulk_commit_group();
             }
+            if (EXTRA) {
+                // chunk statistics, merged into this row's running (count, mean, M2)
+                float sm = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sm += val[j];
+                const float mb = sm * (1.f / 32.f);
+                float qb = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float d = val[j] - mb;
+                    qb = fmaf(d, d, qb);
+                }
+                const float nt = cnt + 32.f;
+                const float delta = mb - cmean;
+                cmean += delta * (32.f / nt);
+                cm2 += qb + delta * delta * (cnt * 32.f / nt);
+                cnt = nt;
+                // bf16 copy through the same staging tile once the fp32 store has read it
+                if (lane == 0) ptx::bulk_wait_group_read<0>();
+                __syncwarp();
+                StageIO<__nv_bfloat16>::write(buf, lane, val);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(tmOut2, buf, col, row0);
+                    ptx::bulk_commit_group();
+                }
+            }
         }
     }
+    if (EXTRA && row < p.M && cnt > 0.f)
+        p.parts_out[(int64_t)row * p.parts_stride + part_index] = make_float2(cmean, cm2);
 }
 
-// ------------------------------------------------------------------ CTA-pair kernel
-// Two CTAs of a cluster (ranks 0 and 1, on a TPC's two SMs) compute one 256 x 256 output
-// tile with tcgen05.mma.cta_group::2 (M 256 = 128 rows per CTA, N 256): each CTA loads
-// its own 128 rows of A and its own half (128 columns) of the weight tile, 32 KB per
-// 64-deep k block, so each SM moves two thirds of the operand bytes per flop that the
-// single-CTA 128 x 256 tile needs, and six stages fit in shared memory.
-//   rank 0 (leader): arms the stage barrier for both CTAs' bytes, issues the pair MMAs
-//   from one thread and multicasts its commits (ring slot free / accumulator ready) to
-//   both CTAs. Both ranks: a TMA warp for their own operand halves (completion counted on
-//   the leader's barrier), and four epilogue warps reading their own TMEM rows; the
-//   epilogue threads of both CTAs release an accumulator on the leader's barrier.
 constexpr int P_STAGES = 6;
 constexpr int P_EPI_WARPS = 8;
 constexpr int P_THREADS = 416;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
@@ -430,11 +494,12 @@ constexpr int P_EPI_BUFS = 1;   // staging tiles per epilogue warp
 constexpr int P_EPI_BYTES = P_EPI_WARPS * P_EPI_BUFS * EPI_STAGE_BYTES;
 constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_EPI_BYTES + BAR_BYTES + 1024;
 
-template <int EPI, typename OutT, typename ResT>
+template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                    const __grid_constant__ CUtensorMap tmOut, const Params p) {
+                    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOut2,
+                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -476,6 +541,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (p.n_w > 1) ptx::prefetch_tensormap(&tmB1);
         if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmOut);
+        if (EXTRA) ptx::prefetch_tensormap(&tmOut2);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -600,8 +666,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int n0 = (tile % n_tiles) * BN;
             const int row0 = m0 + quarter * 32;
             const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS>(p, &tmOut, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row,
-                                                  row0 + lane, row0, n0 + half * 128, lane);
+            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA>(
+                p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row, row0 + lane, row0,
+                n0 + half * 128, lane, (n0 / BN) * 2 + half);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
@@ -683,25 +750,29 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params
     return cudaGetLastError();
 }
 
-template <int EPI, typename OutT, typename ResT>
+template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
 cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
-                             const Params& p, int grid, cudaStream_t s) {
-    auto k = gemm_tc_pair_kernel<EPI, OutT, ResT>;
+                             const CUtensorMap& out2, const Params& p, int grid, cudaStream_t s) {
+    auto k = gemm_tc_pair_kernel<EPI, OutT, ResT, FOLD, EXTRA>;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, P_THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], out, p);
+    k<<<grid, P_THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], out, out2, p);
     return cudaGetLastError();
 }
 
 template <int EPI, typename OutT, typename ResT>
 cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
-                       const Params& p, int grid, cudaStream_t s) {
-    return pair ? launch_inst_pair<EPI, OutT, ResT>(a, b, out, p, grid, s)
-                : launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
+                       const CUtensorMap& out2, const Params& p, int grid, cudaStream_t s) {
+    if (!pair) return launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
+    if (p.fold.parts)
+        return launch_inst_pair<EPI, OutT, ResT, true, false>(a, b, out, out2, p, grid, s);
+    if (p.parts_out)
+        return launch_inst_pair<EPI, OutT, ResT, false, true>(a, b, out, out2, p, grid, s);
+    return launch_inst_pair<EPI, OutT, ResT, false, false>(a, b, out, out2, p, grid, s);
 }
 
 // The CTA-pair kernel is the default; VIT_GEMM_PAIR=0 selects the single-CTA kernel.
@@ -717,6 +788,8 @@ bool use_pair_kernel() {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
+
+bool tc_pair_enabled(const DeviceInfo& dev) { return use_pair_kernel() && dev.num_sms >= 2; }
 
 bool tc_gemm_supported(const TcGemmDesc& d) {
     if (d.M <= 0 || d.N <= 0 || d.K <= 0) return false;
@@ -744,8 +817,13 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
         const void* w = d.w[i < d.n_w ? i : 0];
         if (!make_map(&mb[i], w, d.K, d.n_per_w, d.n_per_w, 64, BK)) return cudaErrorInvalidValue;
     }
-    alignas(64) CUtensorMap mo;
+    alignas(64) CUtensorMap mo, mo2;
     if (!make_map_out(&mo, d.out, d.M, d.N, d.ldo, d.out_f32)) return cudaErrorInvalidValue;
+    if (d.extra.parts) {
+        if (!make_map_out(&mo2, d.extra.out_bf16, d.M, d.N, d.N, false)) return cudaErrorInvalidValue;
+    } else {
+        mo2 = mo;
+    }
     Params p;
     p.M = (int)d.M;
     p.N = (int)d.N;
@@ -758,6 +836,9 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     p.out = d.out;
     p.ldo = d.ldo;
     p.err = dev.err_word;
+    p.fold = d.fold;
+    p.parts_out = d.extra.parts;
+    p.parts_stride = (int)(2 * ((d.N + BN - 1) / BN));
     int grid;
     if (pair) {
         const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN);
@@ -769,19 +850,19 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     }
     switch (d.epi) {
         case TC_EPI_STORE:
-            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, p, grid, s)
-                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
+                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s);
         case TC_EPI_GELU:
-            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, p, grid, s)
-                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
+                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s);
         case TC_EPI_RESID:
             if (d.out_f32)
                 return d.residual_f32
-                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, p, grid, s)
-                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, p, grid, s);
+                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
+                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, mo2, p, grid, s);
             return d.residual_f32
-                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, p, grid, s)
-                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, p, grid, s);
+                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s)
+                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, mo2, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }

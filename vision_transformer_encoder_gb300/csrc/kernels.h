@@ -29,6 +29,25 @@ cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt,
 // ---- Tensor-core GEMM (gemm_tc.cu) --------------------------------------------
 enum TcEpi : int { TC_EPI_STORE = 0, TC_EPI_GELU = 1, TC_EPI_RESID = 2 };
 
+// LayerNorm folded into the GEMM (pair kernel only): A holds un-normalised rows; the
+// epilogue computes rstd * (acc - mean * colsum_j) + colbias_j with mean and rstd merged
+// from per-row partials (mean, M2) over ln_part_cols columns each.
+struct TcLnFold {
+    const float2* parts = nullptr;   // (M, nparts)
+    int nparts = 0, part_cols = 0, D = 0;
+    float eps = 0.f;
+    const float* colsum = nullptr;   // (N)
+    const float* colbias = nullptr;  // (N), includes the layer's own bias
+};
+
+// Extra outputs of the Wo epilogue (pair kernel only): a bf16 copy of the output and
+// the output rows' partial statistics (mean, M2) per 128 columns.
+struct TcExtraOut {
+    void* out_bf16 = nullptr;        // (M, N) bf16, row stride N
+    float2* parts = nullptr;         // (M, 2 * ceil(N / 256))
+};
+
+
 struct TcGemmDesc {
     const void* a;         // (M, K) bf16, row stride lda elements
     int64_t lda;
@@ -44,7 +63,34 @@ struct TcGemmDesc {
     void* out;             // (M, N) out_f32 ? f32 : bf16, row stride ldo
     int64_t ldo;
     bool out_f32;
+    TcLnFold fold;         // fold.parts != nullptr: LayerNorm folded (pair kernel)
+    TcExtraOut extra;      // extra.parts != nullptr: extra outputs (pair kernel)
 };
+
+// True when the pair kernel is in use (the fused LayerNorm needs it).
+bool tc_pair_enabled(const DeviceInfo& dev);
+
+// ---- LayerNorm folding (fold.cu) ------------------------------------------------
+// Row partials of x (bf16, D % 8 == 0, D <= 2048): one (mean, M2) per row.
+bool row_parts_supported(int64_t D, const void* x);
+cudaError_t launch_row_parts(const void* x, float2* parts, int64_t rows, int64_t D, cudaStream_t s);
+
+// Column terms of a folded LayerNorm for weights (K, n_per_w) x n_w (concatenated
+// columns, N = n_w * n_per_w): colsum_j = sum_i W'_ij, colbias_j = sum_i beta_i W_ij
+// + bias_j, W' = diag(gamma) W written to w_scaled when gamma is given.
+struct FoldPrep {
+    const void* w[3];
+    void* w_scaled[3];
+    int64_t n_per_w, N, K;
+    const void* gamma;
+    const void* beta;
+    const void* bias;
+    float* colsum;
+    float* colbias;
+};
+// scratch: fold_prep_scratch_bytes(N, K) bytes of per-chunk partial sums.
+size_t fold_prep_scratch_bytes(int64_t N, int64_t K);
+cudaError_t launch_fold_prep(const FoldPrep& d, float* scratch, cudaStream_t s);
 
 // True when the tensor-core GEMM takes this shape and these pointers.
 bool tc_gemm_supported(const TcGemmDesc& d);

@@ -49,10 +49,10 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<int64_t> g_launches{0};
 
 // ---- per-kernel timing -------------------------------------------------------
-enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_COUNT };
+enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_COUNT };
 const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
                                          "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
-                                         "w2_gemm_residual"};
+                                         "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep"};
 struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -182,32 +182,151 @@ bool fast_path_ok(const BlockArgs& a) {
     return true;
 }
 
-// Scratch layout of one block call: buf (xn, then o, then yn) | qkv | y | h, each
-// rounded up to 256 bytes. Every byte is written before it is read.
+// Scratch layout of one block call, each piece rounded up to 256 bytes; every byte is
+// written before it is read.
+//  unfused paths: buf (xn, then o, then yn) | qkv | y | h
+//  fused bf16 path (LayerNorm folded into the GEMMs): buf (o) | qkv | y | yb (bf16 copy
+//  of y) | h | LN1 row partials | LN2 row partials | column terms of both folds |
+//  gain-scaled weights when LN gains are given.
 struct Workspace {
-    bool fast;
+    bool fast, fused;
     int acc_dt;
-    size_t sz_buf, sz_qkv, sz_y, sz_h, total;
+    size_t sz_buf, sz_qkv, sz_y, sz_h;
+    size_t sz_yb, sz_p1, sz_p2, sz_cols, sz_wq, sz_w1, sz_prep;
+    int p2;   // LN2 partials per row
+    size_t total;
 };
 
-Workspace workspace_layout(const BlockArgs& a) {
+Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     Workspace w;
     const int64_t M = a.N * a.T, D = a.D, F = a.F;
     w.fast = fast_path_ok(a);
+    w.fused = w.fast && fused_ok;
     w.acc_dt = w.fast ? DT_BF16 : (a.dt == DT_F64 ? DT_F64 : DT_F32);
     const size_t ea = dt_size(w.acc_dt);
     w.sz_buf = round_up((size_t)(M * D) * ea, 256);
     w.sz_qkv = round_up((size_t)(M * 3 * D) * ea, 256);
     w.sz_y = round_up((size_t)(M * D) * (w.fast ? 4 : ea), 256);
     w.sz_h = round_up((size_t)(M * F) * ea, 256);
-    w.total = w.sz_buf + w.sz_qkv + w.sz_y + w.sz_h;
+    w.p2 = (int)(2 * ((D + 255) / 256));
+    w.sz_yb = w.sz_p1 = w.sz_p2 = w.sz_cols = w.sz_wq = w.sz_w1 = w.sz_prep = 0;
+    if (w.fused) {
+        w.sz_yb = round_up((size_t)(M * D) * 2, 256);
+        w.sz_p1 = round_up((size_t)M * 8, 256);
+        w.sz_p2 = round_up((size_t)M * 8 * w.p2, 256);
+        w.sz_cols = round_up((size_t)(2 * 3 * D + 2 * F) * 4, 256);
+        if (a.ln1_g) w.sz_wq = round_up((size_t)(3 * D * D) * 2, 256);
+        if (a.ln2_g) w.sz_w1 = round_up((size_t)(D * F) * 2, 256);
+        const size_t p1 = fold_prep_scratch_bytes(3 * D, D), p2 = fold_prep_scratch_bytes(F, D);
+        w.sz_prep = round_up(p1 > p2 ? p1 : p2, 256);
+    }
+    w.total = w.sz_buf + w.sz_qkv + w.sz_y + w.sz_h + w.sz_yb + w.sz_p1 + w.sz_p2 + w.sz_cols + w.sz_wq +
+              w.sz_w1 + w.sz_prep;
     return w;
+}
+
+// The bf16 path with LayerNorm folded into the GEMMs (VIT_LN_FOLD=1, with the CTA-pair
+// GEMM):
+//   prep      column terms of both folds (+ gain-scaled weights)
+//   LN1 stats row (mean, M2) of x
+//   QKV GEMM  qkv = rstd (x @ W' - mean colsum) + colbias          (A = x itself)
+//   attention o
+//   Wo GEMM   y = x + o @ w_o (fp32), plus a bf16 copy of y and y's row partials
+//   W1 GEMM   h = GELU(rstd (yb @ W1' - mean colsum) + colbias)    (colbias holds b1)
+//   W2 GEMM   out = y + h @ w_mlp2 [+ b2]
+cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s,
+                               const Workspace& w, void* ws) {
+    const int64_t M = a.N * a.T, D = a.D, F = a.F;
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    void* o = p;                 p += w.sz_buf;
+    void* qkv = p;               p += w.sz_qkv;
+    void* y = p;                 p += w.sz_y;
+    void* h = p;                 p += w.sz_h;
+    void* yb = p;                p += w.sz_yb;
+    float2* parts1 = reinterpret_cast<float2*>(p);  p += w.sz_p1;
+    float2* parts2 = reinterpret_cast<float2*>(p);  p += w.sz_p2;
+    float* cols = reinterpret_cast<float*>(p);      p += w.sz_cols;
+    __nv_bfloat16* wq_scaled = a.ln1_g ? reinterpret_cast<__nv_bfloat16*>(p) : nullptr;  p += w.sz_wq;
+    __nv_bfloat16* w1_scaled = a.ln2_g ? reinterpret_cast<__nv_bfloat16*>(p) : nullptr;  p += w.sz_w1;
+    float* prep_scratch = reinterpret_cast<float*>(p);
+    float* colsum1 = cols;
+    float* colbias1 = cols + 3 * D;
+    float* colsum2 = cols + 6 * D;
+    float* colbias2 = cols + 6 * D + F;
+    cudaError_t e = cudaSuccess;
+    auto step = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+    };
+    const void* wqkv[3] = {a.w_q, a.w_k, a.w_v};
+    const void* wqkv_used[3] = {a.w_q, a.w_k, a.w_v};
+    if (wq_scaled)
+        for (int i = 0; i < 3; ++i) wqkv_used[i] = wq_scaled + (size_t)i * D * D;
+    step(run(K_FOLD_PREP, s, [&] {
+        FoldPrep f1;
+        std::memset(&f1, 0, sizeof(f1));
+        for (int i = 0; i < 3; ++i) {
+            f1.w[i] = wqkv[i];
+            f1.w_scaled[i] = wq_scaled ? (void*)(wq_scaled + (size_t)i * D * D) : nullptr;
+        }
+        f1.n_per_w = D; f1.N = 3 * D; f1.K = D;
+        f1.gamma = a.ln1_g; f1.beta = a.ln1_b; f1.bias = nullptr;
+        f1.colsum = colsum1; f1.colbias = colbias1;
+        cudaError_t r = launch_fold_prep(f1, prep_scratch, s);
+        if (r != cudaSuccess) return r;
+        FoldPrep f2;
+        std::memset(&f2, 0, sizeof(f2));
+        f2.w[0] = f2.w[1] = f2.w[2] = a.w1;
+        f2.w_scaled[0] = f2.w_scaled[1] = f2.w_scaled[2] = w1_scaled;
+        f2.n_per_w = F; f2.N = F; f2.K = D;
+        f2.gamma = a.ln2_g; f2.beta = a.ln2_b; f2.bias = a.b1;
+        f2.colsum = colsum2; f2.colbias = colbias2;
+        return launch_fold_prep(f2, prep_scratch, s);
+    }));
+    step(run(K_LN1_STATS, s, [&] { return launch_row_parts(a.x, parts1, M, D, s); }));
+    TcGemmDesc g;
+    std::memset(&g, 0, sizeof(g));
+    g.a = a.x; g.lda = D;
+    g.w[0] = wqkv_used[0]; g.w[1] = wqkv_used[1]; g.w[2] = wqkv_used[2]; g.n_w = 3; g.n_per_w = D;
+    g.M = M; g.N = 3 * D; g.K = D;
+    g.epi = TC_EPI_STORE;
+    g.out = qkv; g.ldo = 3 * D; g.out_f32 = false;
+    g.fold.parts = parts1; g.fold.nparts = 1; g.fold.part_cols = (int)D; g.fold.D = (int)D;
+    g.fold.eps = (float)a.eps; g.fold.colsum = colsum1; g.fold.colbias = colbias1;
+    step(run(K_QKV, s, [&] { return launch_gemm_tc(g, dev, s); }));
+    step(run(K_ATTN, s, [&] {
+        if (attention_tc_supported(a.N, a.T, D, a.H, qkv, o)) return launch_attention_tc(qkv, o, a.N, a.T, D, a.H, dev, s);
+        if (attention_fast_supported(D, a.H, qkv, o)) return launch_attention_fast(qkv, o, a.N, a.T, D, a.H, s);
+        return launch_attention_simt(qkv, DT_BF16, o, a.N, a.T, D, a.H, s);
+    }));
+    std::memset(&g, 0, sizeof(g));
+    g.a = o; g.lda = D; g.w[0] = a.w_o; g.n_w = 1; g.n_per_w = D;
+    g.M = M; g.N = D; g.K = D;
+    g.epi = TC_EPI_RESID; g.residual = a.x; g.ldr = D; g.residual_f32 = false;
+    g.out = y; g.ldo = D; g.out_f32 = true;
+    g.extra.out_bf16 = yb; g.extra.parts = parts2;
+    step(run(K_WO, s, [&] { return launch_gemm_tc(g, dev, s); }));
+    std::memset(&g, 0, sizeof(g));
+    g.a = yb; g.lda = D; g.w[0] = w1_scaled ? (const void*)w1_scaled : a.w1; g.n_w = 1; g.n_per_w = F;
+    g.M = M; g.N = F; g.K = D;
+    g.epi = TC_EPI_GELU;
+    g.out = h; g.ldo = F; g.out_f32 = false;
+    g.fold.parts = parts2; g.fold.nparts = w.p2; g.fold.part_cols = 128; g.fold.D = (int)D;
+    g.fold.eps = (float)a.eps; g.fold.colsum = colsum2; g.fold.colbias = colbias2;
+    step(run(K_W1, s, [&] { return launch_gemm_tc(g, dev, s); }));
+    std::memset(&g, 0, sizeof(g));
+    g.a = h; g.lda = F; g.w[0] = a.w2; g.n_w = 1; g.n_per_w = D;
+    g.M = M; g.N = D; g.K = F;
+    g.epi = TC_EPI_RESID; g.bias = a.b2; g.residual = y; g.ldr = D; g.residual_f32 = true;
+    g.out = a.out; g.ldo = D; g.out_f32 = false;
+    step(run(K_W2, s, [&] { return launch_gemm_tc(g, dev, s); }));
+    return e;
 }
 
 // Enqueues the seven steps of the block on `s`, using `ws` (at least w.total bytes)
 // as scratch.
 cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s,
                                const Workspace& w, void* ws) {
+    if (w.fused) return launch_block_fused(a, dev, s, w, ws);
     const int64_t M = a.N * a.T, D = a.D, F = a.F;
     const bool fast = w.fast;
     const int acc_dt = w.acc_dt;
@@ -325,8 +444,23 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     return e;
 }
 
+// LayerNorm folded into the GEMMs is opt-in (VIT_LN_FOLD=1): it removes the LN2 pass
+// and LN1's normalised copy, but the extra epilogue work in the Wo and W1 GEMMs
+// currently costs as much as it saves.
+bool ln_fold_requested() {
+    static const bool on = [] {
+        const char* e = std::getenv("VIT_LN_FOLD");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+
+bool fused_ok(const BlockArgs& a, const DeviceInfo& dev) {
+    return ln_fold_requested() && tc_pair_enabled(dev) && row_parts_supported(a.D, a.x);
+}
+
 int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-    const Workspace w = workspace_layout(a);
+    const Workspace w = workspace_layout(a, fused_ok(a, dev));
     DeviceState* st = nullptr;
     int rc = current_device(&st);
     if (rc != VIT_OK) return rc;
@@ -587,11 +721,11 @@ int vit_block_noalloc(const void* x, const void* w_q, const void* w_k, const voi
                 N, T, D, F, H, eps, dtype, out};
     int rc = validate(a);
     if (rc != VIT_OK) return rc;
-    const Workspace w = workspace_layout(a);
-    if (w.total > kNoAllocScratchBytes) return VIT_ERR_UNSUPPORTED;
     NoAllocState* st = nullptr;
     rc = noalloc_device(&st);
     if (rc != VIT_OK) return rc;
+    const Workspace w = workspace_layout(a, fused_ok(a, st->info));
+    if (w.total > kNoAllocScratchBytes) return VIT_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_block_steps(a, st->info, s, w, st->scratch);
     if (e != cudaSuccess) {
