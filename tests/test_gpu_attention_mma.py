@@ -1,8 +1,11 @@
-"""The attention parity tests again, on the bf16 mma.sync kernel.
+"""The attention parity tests again, on the kernels that are not the default.
 
-Head widths 64 and 80 run on the tcgen05 kernel by default; VIT_ATTN_TC=0 makes the
-library use the mma.sync flash kernel for them instead. The choice is read per call
-from the environment, so the stage tests are re-run in a child process with it set.
+Head widths 64 and 80 run on tcgen05 kernels by default: for head width 64 and at most
+224 tokens the whole-row kernel (all keys in one S tile), otherwise the key-streaming
+kernel. VIT_ATTN_TC=0 selects the mma.sync flash kernel, VIT_ATTN_WHOLE=0 the streaming
+kernel at every length, and VIT_ATTN_PAIR=1 (with VIT_ATTN_WHOLE=0) the CTA-pair kernel.
+The switches are read once per process, so the stage tests are re-run in a child
+process with them set.
 """
 import os
 import subprocess
@@ -32,7 +35,18 @@ def test_attention_stages_on_cta_pair_kernel():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    env = dict(os.environ, VIT_ATTN_PAIR="1")
+    env = dict(os.environ, VIT_ATTN_PAIR="1", VIT_ATTN_WHOLE="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "attention"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_attention_stages_on_key_streaming_kernel():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, VIT_ATTN_WHOLE="0")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "attention"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)

@@ -134,7 +134,9 @@ def test_layernorm_wide_types(dtype):
 @pytest.mark.parametrize("N,T,D,H", [(2, 197, 128, 2), (1, 65, 64, 1), (3, 77, 160, 2),
                                      (1, 1, 64, 1), (2, 129, 256, 4), (1, 300, 96, 3),
                                      (2, 577, 128, 2), (1, 1025, 160, 2), (3, 256, 64, 1),
-                                     (1, 385, 80, 1)])
+                                     (1, 385, 80, 1), (2, 224, 128, 2), (1, 128, 64, 1),
+                                     (3, 208, 64, 1), (2, 16, 128, 2), (1, 225, 64, 1),
+                                     (5, 100, 192, 3)])
 def test_attention_bf16(N, T, D, H):
     d = _dev()
     qkv = _rand((N, T, 3 * D), 20 + T, std=1.5)

@@ -1,0 +1,468 @@
+// attention_whole.cu -- bidirectional multi-head attention for head width 64 and at most
+// 224 tokens per sequence, on the sm_103a tensor cores (tcgen05 / TMEM / TMA).
+//
+// "ViT Encoder Block" (crackedaicode), "Multi-head attention": per sequence n and head
+// h, out_h = softmax(Q_h K_h^T / sqrt(D/H)) V_h with every key visible; heads written
+// side by side in order, Q, K and V read in place from the fused (N, T, 3D) buffer.
+//
+// With T <= 224, all keys of a query row fit in one S tile: S = Q K^T for 128 query
+// rows is a single M 128 x N ns MMA chain (ns = T rounded up to 16), so the row maximum
+// is known before any exponent is taken. The softmax is one exact pass per row -- no
+// running maximum, no rescaling of O -- and O = P V is one MMA chain over ns keys.
+//
+// A unit is (sequence, head, 128-row query tile); the units of one (sequence, head)
+// item share its K and V. Persistent kernel, one CTA per SM, 16 warps:
+//   warps 0, 10, 11  TMA loads of Q, K and V (one issuing thread per stream, as a
+//                    thread's TMA copies are issued one after another). Each is
+//                    double-buffered per item; a 3-D tensor map (column, token,
+//                    sequence) zero-fills tokens past T.
+//   warp 1           TMEM owner and MMA issuer. MMA stream: S(0), S(1), PV(0), S(2),
+//                    PV(1), S(3), PV(2), ...: S of the next unit runs while the softmax
+//                    of the current one works, and PV(u) follows as soon as P(u) is in.
+//   warps 2-5 / 6-9  softmax of even / odd units, one query row per thread. Pass 1: row
+//                    maximum over the valid keys. Pass 2: P = exp2(S log2(e)/sqrt(dh) - max)
+//                    in bf16, written into the S columns already consumed (32 keys fill
+//                    16 columns), and the row sum l to shared memory.
+//   warps 12-15      epilogue, one per TMEM lane quarter: O into registers, O's slot
+//                    released at once, then O / l in bf16 to global memory.
+// TMEM, 512 columns: S / P of even units at [0, 224), of odd units at [224, 448), O at
+// [448, 512). S(u + 2) overwrites P(u) only after PV(u) in the same in-order MMA stream.
+// Every wait is bounded; on expiry the kernel records an error bit and unwinds.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace vit {
+namespace {
+
+constexpr int AW_DH = 64;
+constexpr int AW_ROWS = 128;               // query rows per unit (TMEM lanes)
+constexpr int AW_MAX_KEYS = 224;           // S columns per unit
+constexpr int AW_THREADS = 512;            // 16 warps
+constexpr int AW_BOX = AW_ROWS * 128;      // 128 rows x 64 bf16 columns, 128B swizzle: 16 KB
+constexpr int AW_OFF_Q = 0;                        // [buffer][query tile]
+constexpr int AW_OFF_K = AW_OFF_Q + 4 * AW_BOX;    // [buffer][128-key box]
+constexpr int AW_OFF_V = AW_OFF_K + 4 * AW_BOX;    // [buffer][128-key box]
+constexpr int AW_OFF_L = AW_OFF_V + 4 * AW_BOX;    // row sums [unit % 4][row]
+constexpr int AW_OFF_BAR = AW_OFF_L + 4 * AW_ROWS * 4;
+constexpr int AW_SMEM = AW_OFF_BAR + 256 + 1024;   // + alignment slack
+constexpr uint32_t AW_TMEM_O = 448;
+
+struct AwParams {
+    int T, D, H;
+    int nq;        // query tiles per item: 1 or 2
+    int nkb;       // 128-key boxes per item: 1 or 2
+    int ns;        // S columns: T rounded up to 16
+    int items;     // N * H
+    float scale_log2;
+    __nv_bfloat16* o;
+    uint32_t* err;
+};
+
+struct AwBars {
+    uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[2], p_full[2], l_full[4];
+    uint64_t o_done, o_free, done;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+static_assert(sizeof(AwBars) <= 256, "barrier block");
+static_assert(AW_SMEM <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ void aw_error(uint32_t* err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+// Masks keys at or past `lim` (chunk-relative) to -inf.
+template <int W>
+__device__ __forceinline__ void mask_tail(uint32_t (&v)[W], int lim) {
+    if (lim < W) {
+#pragma unroll
+        for (int e = 0; e < W; ++e)
+            if (e >= lim) v[e] = __float_as_uint(-INFINITY);
+    }
+}
+
+template <int W>
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[W], float m) {
+    float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
+#pragma unroll
+    for (int e = 2; e < W; e += 2) {
+        a = fmaxf(a, __uint_as_float(v[e]));
+        b = fmaxf(b, __uint_as_float(v[e + 1]));
+    }
+    return fmaxf(m, fmaxf(a, b));
+}
+
+// P for W keys: W / 2 packed bf16 pairs; returns the partial row sum.
+template <int W>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&v)[W], float sl2, float m,
+                                           uint32_t (&pk)[W / 2]) {
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < W; e += 2) {
+        const float p0 = exp2_approx(fmaf(__uint_as_float(v[e]), sl2, -m));
+        const float p1 = exp2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m));
+        s0 += p0;
+        s1 += p1;
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+    }
+    return s0 + s1;
+}
+
+__global__ void __launch_bounds__(AW_THREADS, 1)
+attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* sQ = smem + AW_OFF_Q;
+    uint8_t* sK = smem + AW_OFF_K;
+    uint8_t* sV = smem + AW_OFF_V;
+    float* sL = reinterpret_cast<float*>(smem + AW_OFF_L);
+    AwBars* bars = reinterpret_cast<AwBars*>(smem + AW_OFF_BAR);
+    volatile int* abort_flag = &bars->abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = p.nq;
+    const int n_items = p.items > (int)blockIdx.x ? (p.items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int units = n_items * nq;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&bars->q_full[b], 1);
+            ptx::mbar_init(&bars->q_empty[b], 1);
+            ptx::mbar_init(&bars->k_full[b], 1);
+            ptx::mbar_init(&bars->k_empty[b], 1);
+            ptx::mbar_init(&bars->v_full[b], 1);
+            ptx::mbar_init(&bars->v_empty[b], 1);
+            ptx::mbar_init(&bars->s_full[b], 1);
+            ptx::mbar_init(&bars->p_full[b], 4);     // the four softmax warps of a group
+        }
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 4);
+        ptx::mbar_init(&bars->o_done, 1);
+        ptx::mbar_init(&bars->o_free, 4);            // the four epilogue warps
+        ptx::mbar_init(&bars->done, 1);
+        bars->abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&tm);
+    if (warp == 1) {
+        ptx::tmem_alloc(&bars->tmem_slot, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars->tmem_slot;
+
+    if (warp == 0 || warp == 10 || warp == 11) {
+        if (lane == 0) {
+            // ------------------------------------------------------------ TMA producers
+            const int role = warp == 0 ? 0 : warp - 9;   // 0 Q, 1 K, 2 V
+            uint64_t* full = role == 0 ? bars->q_full : role == 1 ? bars->k_full : bars->v_full;
+            uint64_t* empty = role == 0 ? bars->q_empty : role == 1 ? bars->k_empty : bars->v_empty;
+            uint8_t* ring = role == 0 ? sQ : role == 1 ? sK : sV;
+            const int boxes = role == 0 ? nq : p.nkb;
+            const int col0 = role * p.D;   // Q at 0, K at D, V at 2D
+            int k = 0;
+            bool ok = true;
+            for (; k < n_items; ++k) {
+                const int item = (int)blockIdx.x + k * (int)gridDim.x;
+                const int n = item / p.H, h = item - n * p.H;
+                const int b = k & 1;
+                if (!ptx::mbar_wait_bounded(&empty[b], ((k >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                ptx::mbar_arrive_expect_tx(&full[b], boxes * AW_BOX);
+                for (int r = 0; r < boxes; ++r)
+                    ptx::tma_load_3d(ring + (b * 2 + r) * AW_BOX, &tm, &full[b], col0 + h * AW_DH, r * AW_ROWS, n);
+            }
+            if (!ok) {
+                aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
+                *abort_flag = 1;
+            }
+            // let the copies in flight land before the CTA can exit
+            for (int b = 0; b < 2; ++b)
+                if (k > b && !ptx::mbar_wait_bounded(&full[b], ((k - 1 - b) >> 1) & 1, nullptr))
+                    aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------------------- MMA issuer
+            const uint32_t idS = ptx::idesc_bf16_f32(AW_ROWS, p.ns, false, false);
+            constexpr uint32_t idO = ptx::idesc_bf16_f32(AW_ROWS, AW_DH, false, true);
+            const int ksteps = p.ns >> 4;
+            bool ok = true;
+            for (int s = 0; s <= units && ok; ++s) {
+                if (s < units) {
+                    // S(s) = Q K^T into the unit's S slot
+                    const int u = s, k = u / nq, qt = u - k * nq, b = k & 1, g = u & 1;
+                    if (qt == 0) {
+                        if (!ptx::mbar_wait_bounded(&bars->q_full[b], (k >> 1) & 1, abort_flag) ||
+                            !ptx::mbar_wait_bounded(&bars->k_full[b], (k >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t qa = ptx::smem_addr(sQ + (b * 2 + qt) * AW_BOX);
+                    const uint32_t ka = ptx::smem_addr(sK + b * 2 * AW_BOX);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {   // 64 columns: 128-byte rows, 32 bytes per step
+                        const uint64_t ad = ptx::smem_desc(qa + kk * 32, 16, 1024, ptx::kLayoutSw128);
+                        const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 1024, ptx::kLayoutSw128);
+                        ptx::mma_bf16_ss(tmem + g * AW_MAX_KEYS, ad, bd, idS, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&bars->s_full[g]);
+                    if (qt == nq - 1) {
+                        ptx::mma_commit(&bars->q_empty[b]);
+                        ptx::mma_commit(&bars->k_empty[b]);
+                    }
+                }
+                if (s >= 1) {
+                    // PV(s - 1): O = P V, P read from tensor memory
+                    const int u = s - 1, k = u / nq, qt = u - k * nq, b = k & 1, g = u & 1;
+                    if (!ptx::mbar_wait_bounded(&bars->p_full[g], (u >> 1) & 1, abort_flag) ||
+                        (qt == 0 && !ptx::mbar_wait_bounded(&bars->v_full[b], (k >> 1) & 1, abort_flag)) ||
+                        (u >= 1 && !ptx::mbar_wait_bounded(&bars->o_free, (u - 1) & 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t va = ptx::smem_addr(sV + b * 2 * AW_BOX);
+                    const uint32_t tP = tmem + g * AW_MAX_KEYS;
+                    for (int kk = 0; kk < ksteps; ++kk) {
+                        // V: keys are the K dimension (rows of 128 bytes), head columns the
+                        // N dimension (MN-major); P: 16 keys = 8 columns of bf16 pairs
+                        const uint64_t bd = ptx::smem_desc(va + kk * 2048, 16, 1024, ptx::kLayoutSw128);
+                        ptx::mma_bf16_ts(tmem + AW_TMEM_O, tP + kk * 8, bd, idO, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&bars->o_done);
+                    if (qt == nq - 1) ptx::mma_commit(&bars->v_empty[b]);
+                }
+            }
+            if (!ok) {
+                aw_error(p.err, ERRBIT_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            ptx::mma_commit(&bars->done);
+            if (!ptx::mbar_wait_bounded(&bars->done, 0, nullptr)) aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else if (warp >= 2 && warp <= 9) {
+        // ------------------------------------------------------------------- softmax
+        const int g = (warp - 2) >> 2;          // 0: warps 2-5 (even units), 1: warps 6-9
+        const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+        const uint32_t tS = tmem + g * AW_MAX_KEYS + ((uint32_t)(quarter * 32) << 16);
+        const float sl2 = p.scale_log2;
+        const int T = p.T, nfull = p.ns >> 5;
+        const bool tail = (p.ns & 16) != 0;
+        bool ok = true;
+        for (int u = g; u < units; u += 2) {
+            const int k = u / nq, qt = u - k * nq;
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->s_full[g], (u >> 1) & 1, abort_flag));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            // a warp whose 32 query rows all lie past T has no output; it only keeps the
+            // barrier protocol
+            if (qt * AW_ROWS + quarter * 32 < T) {
+                // pass 1: row maximum over keys < T, 64 columns per TMEM wait
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 7; c += 2) {
+                    if (c + 1 < nfull) {
+                        uint32_t v0[32], v1[32];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v1);
+                        ptx::tmem_ld_wait();
+                        mask_tail(v0, T - c * 32);
+                        mask_tail(v1, T - (c + 1) * 32);
+                        mx = chunk_max(v1, chunk_max(v0, mx));
+                    } else if (c < nfull) {
+                        uint32_t v0[32];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_wait();
+                        mask_tail(v0, T - c * 32);
+                        mx = chunk_max(v0, mx);
+                    }
+                }
+                if (tail) {
+                    uint32_t v0[16];
+                    ptx::tmem_ld_32x32b_x16(tS + nfull * 32, v0);
+                    ptx::tmem_ld_wait();
+                    mask_tail(v0, T - nfull * 32);
+                    mx = chunk_max(v0, mx);
+                }
+                const float m = mx * sl2;
+                // pass 2: P over the consumed S columns (keys 32c.. go to columns 16c..)
+                float l = 0.f;
+#pragma unroll
+                for (int c = 0; c < 7; c += 2) {
+                    if (c + 1 < nfull) {
+                        uint32_t v0[32], v1[32], pk0[16], pk1[16];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v1);
+                        ptx::tmem_ld_wait();
+                        mask_tail(v0, T - c * 32);
+                        mask_tail(v1, T - (c + 1) * 32);
+                        l += chunk_exp(v0, sl2, m, pk0);
+                        l += chunk_exp(v1, sl2, m, pk1);
+                        ptx::tmem_st_32x32b_x16(tS + c * 16, pk0);
+                        ptx::tmem_st_32x32b_x16(tS + (c + 1) * 16, pk1);
+                    } else if (c < nfull) {
+                        uint32_t v0[32], pk0[16];
+                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_wait();
+                        mask_tail(v0, T - c * 32);
+                        l += chunk_exp(v0, sl2, m, pk0);
+                        ptx::tmem_st_32x32b_x16(tS + c * 16, pk0);
+                    }
+                }
+                if (tail) {
+                    uint32_t v0[16], pk0[8];
+                    ptx::tmem_ld_32x32b_x16(tS + nfull * 32, v0);
+                    ptx::tmem_ld_wait();
+                    mask_tail(v0, T - nfull * 32);
+                    l += chunk_exp(v0, sl2, m, pk0);
+                    ptx::tmem_st_32x32b_x8(tS + nfull * 16, pk0);
+                }
+                ptx::tmem_st_wait();
+                sL[(u & 3) * AW_ROWS + quarter * 32 + lane] = l;
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&bars->p_full[g]);
+                ptx::mbar_arrive(&bars->l_full[u & 3]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
+            *abort_flag = 1;
+        }
+    } else if (warp >= 12) {
+        // ------------------------------------------------------------------ epilogue
+        const int quarter = warp & 3;
+        const uint32_t tO = tmem + AW_TMEM_O + ((uint32_t)(quarter * 32) << 16);
+        const int D = p.D;
+        bool ok = true;
+        for (int u = 0; u < units; ++u) {
+            const int k = u / nq, qt = u - k * nq;
+            const int item = (int)blockIdx.x + k * (int)gridDim.x;
+            const int n = item / p.H, h = item - n * p.H;
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done, u & 1, abort_flag));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const bool live = qt * AW_ROWS + quarter * 32 < p.T;
+            uint32_t ov[64];
+            if (live) {
+                ptx::tmem_ld_32x32b_x32(tO, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+                ptx::tmem_ld_32x32b_x32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+                ptx::tmem_ld_wait();
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->o_free);
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->l_full[u & 3], (u >> 2) & 1, abort_flag));
+            if (!ok) break;
+            const int t = qt * AW_ROWS + quarter * 32 + lane;
+            if (live && t < p.T) {
+                const float inv = 1.f / sL[(u & 3) * AW_ROWS + quarter * 32 + lane];
+                __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * AW_DH;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + c * 8) = w;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
+            *abort_flag = 1;
+        }
+    }
+
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn aw_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault,
+                                             &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    });
+    return fn;
+}
+
+}  // namespace
+
+// VIT_ATTN_WHOLE=0 sends these shapes to the key-streaming kernel instead.
+bool attention_whole_supported(int64_t T, int64_t D, int64_t H) {
+    if (H <= 0 || D % H != 0 || D / H != AW_DH || T < 1 || T > AW_MAX_KEYS) return false;
+    static const bool off = [] {
+        const char* e = std::getenv("VIT_ATTN_WHOLE");
+        return e && e[0] == '0';
+    }();
+    return !off && aw_encode_fn() != nullptr;
+}
+
+cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
+                                   const DeviceInfo& dev, cudaStream_t s) {
+    if (N <= 0 || T <= 0) return cudaSuccess;
+    if (!attention_whole_supported(T, D, H) || N * H > 0x7fffffff) return cudaErrorInvalidValue;
+    EncodeTiledFn fn = aw_encode_fn();
+    alignas(64) CUtensorMap tm;
+    cuuint64_t dims[3] = {(cuuint64_t)(3 * D), (cuuint64_t)T, (cuuint64_t)N};
+    cuuint64_t strides[2] = {(cuuint64_t)(3 * D * 2), (cuuint64_t)(T * 3 * D * 2)};
+    cuuint32_t box[3] = {AW_DH, AW_ROWS, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    AwParams p;
+    p.T = (int)T;
+    p.D = (int)D;
+    p.H = (int)H;
+    p.nq = (int)((T + AW_ROWS - 1) / AW_ROWS);
+    p.ns = (int)((T + 15) / 16 * 16);
+    p.nkb = (p.ns + AW_ROWS - 1) / AW_ROWS;
+    p.items = (int)(N * H);
+    p.scale_log2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.err = dev.err_word;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(attention_whole_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             AW_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
+    attention_whole_kernel<<<grid, AW_THREADS, AW_SMEM, s>>>(tm, p);
+    return cudaGetLastError();
+}
+
+}  // namespace vit
