@@ -11,20 +11,25 @@
 // running maximum, no rescaling of O -- and O = P V is one MMA chain over ns keys.
 //
 // A unit is (sequence, head, 128-row query tile); the units of one (sequence, head)
-// item share its K and V. Persistent kernel, one CTA per SM, 16 warps:
-//   warps 0, 10, 11  TMA loads of Q, K and V (one issuing thread per stream, as a
+// item share its K and V. Persistent kernel, one CTA per SM, 24 warps:
+//   warps 0-7 / 8-15  softmax of even / odd units. Two warps per TMEM lane quarter
+//                    split the keys of their 32 rows: warp "half" 0 takes the first
+//                    `split` keys, half 1 the rest. Pass 1: each takes the maximum over
+//                    its valid keys, and the pair exchange it through shared memory.
+//                    Pass 2: P = exp2(S log2(e)/sqrt(dh) - max) in bf16, written into the
+//                    half's own S columns already consumed (32 keys fill 16 columns),
+//                    and the half's row sum to shared memory.
+//   warps 16-19      epilogue, one per TMEM lane quarter: O into registers, O's slot
+//                    released at once, then O / (l0 + l1) in bf16 to global memory.
+//   warp 20          TMEM owner and MMA issuer. MMA stream: S(0), S(1), PV(0), S(2),
+//                    PV(1), S(3), PV(2), ...: S of the next unit runs while the softmax
+//                    of the current one works, and PV(u) follows as soon as P(u) is in.
+//                    PV reads P of keys below `split` from the slot's first columns and
+//                    P of the rest from the columns starting at `split`.
+//   warps 21-23      TMA loads of Q, K and V (one issuing thread per stream, as a
 //                    thread's TMA copies are issued one after another). Each is
 //                    double-buffered per item; a 3-D tensor map (column, token,
 //                    sequence) zero-fills tokens past T.
-//   warp 1           TMEM owner and MMA issuer. MMA stream: S(0), S(1), PV(0), S(2),
-//                    PV(1), S(3), PV(2), ...: S of the next unit runs while the softmax
-//                    of the current one works, and PV(u) follows as soon as P(u) is in.
-//   warps 2-5 / 6-9  softmax of even / odd units, one query row per thread. Pass 1: row
-//                    maximum over the valid keys. Pass 2: P = exp2(S log2(e)/sqrt(dh) - max)
-//                    in bf16, written into the S columns already consumed (32 keys fill
-//                    16 columns), and the row sum l to shared memory.
-//   warps 12-15      epilogue, one per TMEM lane quarter: O into registers, O's slot
-//                    released at once, then O / l in bf16 to global memory.
 // TMEM, 512 columns: S / P of even units at [0, 224), of odd units at [224, 448), O at
 // [448, 512). S(u + 2) overwrites P(u) only after PV(u) in the same in-order MMA stream.
 // Every wait is bounded; on expiry the kernel records an error bit and unwinds.
@@ -45,13 +50,15 @@ namespace {
 constexpr int AW_DH = 64;
 constexpr int AW_ROWS = 128;               // query rows per unit (TMEM lanes)
 constexpr int AW_MAX_KEYS = 224;           // S columns per unit
-constexpr int AW_THREADS = 512;            // 16 warps
+constexpr int AW_THREADS = 768;            // 24 warps
+constexpr int AW_EPI_WARP = 16, AW_MMA_WARP = 20, AW_LOAD_WARP = 21;
 constexpr int AW_BOX = AW_ROWS * 128;      // 128 rows x 64 bf16 columns, 128B swizzle: 16 KB
 constexpr int AW_OFF_Q = 0;                        // [buffer][query tile]
 constexpr int AW_OFF_K = AW_OFF_Q + 4 * AW_BOX;    // [buffer][128-key box]
 constexpr int AW_OFF_V = AW_OFF_K + 4 * AW_BOX;    // [buffer][128-key box]
-constexpr int AW_OFF_L = AW_OFF_V + 4 * AW_BOX;    // row sums [unit % 4][row]
-constexpr int AW_OFF_BAR = AW_OFF_L + 4 * AW_ROWS * 4;
+constexpr int AW_OFF_L = AW_OFF_V + 4 * AW_BOX;    // row sums [unit % 4][half][row]
+constexpr int AW_OFF_MX = AW_OFF_L + 4 * 2 * AW_ROWS * 4;   // row maxima [group][half][row]
+constexpr int AW_OFF_BAR = AW_OFF_MX + 2 * 2 * AW_ROWS * 4;
 constexpr int AW_SMEM = AW_OFF_BAR + 256 + 1024;   // + alignment slack
 constexpr uint32_t AW_TMEM_O = 448;
 
@@ -60,6 +67,7 @@ struct AwParams {
     int nq;        // query tiles per item: 1 or 2
     int nkb;       // 128-key boxes per item: 1 or 2
     int ns;        // S columns: T rounded up to 16
+    int split;     // keys of softmax half 0: a multiple of 32
     int items;     // N * H
     float scale_log2;
     __nv_bfloat16* o;
@@ -69,6 +77,7 @@ struct AwParams {
 struct AwBars {
     uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], l_full[4];
+    uint64_t mx_full[2][4];   // [group][lane quarter]: both halves' maxima written
     uint64_t o_done, o_free, done;
     uint32_t tmem_slot;
     int abort_flag;
@@ -126,6 +135,7 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     uint8_t* sK = smem + AW_OFF_K;
     uint8_t* sV = smem + AW_OFF_V;
     float* sL = reinterpret_cast<float*>(smem + AW_OFF_L);
+    float* sMx = reinterpret_cast<float*>(smem + AW_OFF_MX);
     AwBars* bars = reinterpret_cast<AwBars*>(smem + AW_OFF_BAR);
     volatile int* abort_flag = &bars->abort_flag;
 
@@ -143,17 +153,18 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::mbar_init(&bars->v_full[b], 1);
             ptx::mbar_init(&bars->v_empty[b], 1);
             ptx::mbar_init(&bars->s_full[b], 1);
-            ptx::mbar_init(&bars->p_full[b], 4);     // the four softmax warps of a group
+            ptx::mbar_init(&bars->p_full[b], 8);     // the eight softmax warps of a group
+            for (int q = 0; q < 4; ++q) ptx::mbar_init(&bars->mx_full[b][q], 2);
         }
-        for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 4);
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 8);
         ptx::mbar_init(&bars->o_done, 1);
         ptx::mbar_init(&bars->o_free, 4);            // the four epilogue warps
         ptx::mbar_init(&bars->done, 1);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) ptx::prefetch_tensormap(&tm);
-    if (warp == 1) {
+    if (warp == AW_LOAD_WARP && lane == 0) ptx::prefetch_tensormap(&tm);
+    if (warp == AW_MMA_WARP) {
         ptx::tmem_alloc(&bars->tmem_slot, 512);
         ptx::tmem_relinquish();
     }
@@ -162,10 +173,10 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
 
-    if (warp == 0 || warp == 10 || warp == 11) {
+    if (warp >= AW_LOAD_WARP) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producers
-            const int role = warp == 0 ? 0 : warp - 9;   // 0 Q, 1 K, 2 V
+            const int role = warp - AW_LOAD_WARP;   // 0 Q, 1 K, 2 V
             uint64_t* full = role == 0 ? bars->q_full : role == 1 ? bars->k_full : bars->v_full;
             uint64_t* empty = role == 0 ? bars->q_empty : role == 1 ? bars->k_empty : bars->v_empty;
             uint8_t* ring = role == 0 ? sQ : role == 1 ? sK : sV;
@@ -191,12 +202,12 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                 if (k > b && !ptx::mbar_wait_bounded(&full[b], ((k - 1 - b) >> 1) & 1, nullptr))
                     aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
-    } else if (warp == 1) {
+    } else if (warp == AW_MMA_WARP) {
         if (lane == 0) {
             // ------------------------------------------------------------- MMA issuer
             const uint32_t idS = ptx::idesc_bf16_f32(AW_ROWS, p.ns, false, false);
             constexpr uint32_t idO = ptx::idesc_bf16_f32(AW_ROWS, AW_DH, false, true);
-            const int ksteps = p.ns >> 4;
+            const int ksteps = p.ns >> 4, ksplit = p.split >> 4;
             bool ok = true;
             for (int s = 0; s <= units && ok; ++s) {
                 if (s < units) {
@@ -238,9 +249,12 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                     const uint32_t tP = tmem + g * AW_MAX_KEYS;
                     for (int kk = 0; kk < ksteps; ++kk) {
                         // V: keys are the K dimension (rows of 128 bytes), head columns the
-                        // N dimension (MN-major); P: 16 keys = 8 columns of bf16 pairs
+                        // N dimension (MN-major); P: 16 keys = 8 columns of bf16 pairs, at
+                        // the start of the slot for half 0's keys, from column `split` on
+                        // for half 1's
                         const uint64_t bd = ptx::smem_desc(va + kk * 2048, 16, 1024, ptx::kLayoutSw128);
-                        ptx::mma_bf16_ts(tmem + AW_TMEM_O, tP + kk * 8, bd, idO, kk > 0 ? 1u : 0u);
+                        const uint32_t pa = kk < ksplit ? tP + kk * 8 : tP + p.split + (kk - ksplit) * 8;
+                        ptx::mma_bf16_ts(tmem + AW_TMEM_O, pa, bd, idO, kk > 0 ? 1u : 0u);
                     }
                     ptx::mma_commit(&bars->o_done);
                     if (qt == nq - 1) ptx::mma_commit(&bars->v_empty[b]);
@@ -253,14 +267,21 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::mma_commit(&bars->done);
             if (!ptx::mbar_wait_bounded(&bars->done, 0, nullptr)) aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
-    } else if (warp >= 2 && warp <= 9) {
+    } else if (warp < AW_EPI_WARP) {
         // ------------------------------------------------------------------- softmax
-        const int g = (warp - 2) >> 2;          // 0: warps 2-5 (even units), 1: warps 6-9
+        const int g = warp >> 3;                // 0: even units, 1: odd units
+        const int half = (warp >> 2) & 1;       // which keys of the rows
         const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+        const int row = quarter * 32 + lane;
         const uint32_t tS = tmem + g * AW_MAX_KEYS + ((uint32_t)(quarter * 32) << 16);
         const float sl2 = p.scale_log2;
-        const int T = p.T, nfull = p.ns >> 5;
-        const bool tail = (p.ns & 16) != 0;
+        const int T = p.T;
+        // this half's keys: 32-key chunks [c0, c1), then a 16-key tail (half 1 only)
+        const int c0 = half ? p.split >> 5 : 0, c1 = half ? p.ns >> 5 : p.split >> 5;
+        const bool tail = half && (p.ns & 16) != 0;
+        const uint32_t pbase = half ? (uint32_t)p.split : 0u;   // P columns of this half
+        float* mx_mine = sMx + (g * 2 + half) * AW_ROWS;
+        const float* mx_other = sMx + (g * 2 + (half ^ 1)) * AW_ROWS;
         bool ok = true;
         for (int u = g; u < units; u += 2) {
             const int k = u / nq, qt = u - k * nq;
@@ -269,69 +290,82 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::tc_fence_after();
             // a warp whose 32 query rows all lie past T has no output; it only keeps the
             // barrier protocol
-            if (qt * AW_ROWS + quarter * 32 < T) {
-                // pass 1: row maximum over keys < T, 64 columns per TMEM wait
-                float mx = -INFINITY;
+            const bool live = qt * AW_ROWS + quarter * 32 < T;
+            float mx = -INFINITY;
+            if (live) {
+                // pass 1: maximum over this half's keys < T, 64 columns per TMEM wait
 #pragma unroll
                 for (int c = 0; c < 7; c += 2) {
-                    if (c + 1 < nfull) {
+                    const int cc = c0 + c;
+                    if (cc + 1 < c1) {
                         uint32_t v0[32], v1[32];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
-                        ptx::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v1);
+                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + (cc + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        mask_tail(v0, T - c * 32);
-                        mask_tail(v1, T - (c + 1) * 32);
+                        mask_tail(v0, T - cc * 32);
+                        mask_tail(v1, T - (cc + 1) * 32);
                         mx = chunk_max(v1, chunk_max(v0, mx));
-                    } else if (c < nfull) {
+                    } else if (cc < c1) {
                         uint32_t v0[32];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
                         ptx::tmem_ld_wait();
-                        mask_tail(v0, T - c * 32);
+                        mask_tail(v0, T - cc * 32);
                         mx = chunk_max(v0, mx);
                     }
                 }
                 if (tail) {
                     uint32_t v0[16];
-                    ptx::tmem_ld_32x32b_x16(tS + nfull * 32, v0);
+                    ptx::tmem_ld_32x32b_x16(tS + c1 * 32, v0);
                     ptx::tmem_ld_wait();
-                    mask_tail(v0, T - nfull * 32);
+                    mask_tail(v0, T - c1 * 32);
                     mx = chunk_max(v0, mx);
                 }
-                const float m = mx * sl2;
-                // pass 2: P over the consumed S columns (keys 32c.. go to columns 16c..)
+                mx_mine[row] = mx;
+            }
+            // exchange the two halves' maxima
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&bars->mx_full[g][quarter]);
+            ok = __all_sync(0xffffffffu,
+                            ptx::mbar_wait_bounded(&bars->mx_full[g][quarter], (u >> 1) & 1, abort_flag));
+            if (!ok) break;
+            if (live) {
+                const float m = fmaxf(mx, mx_other[row]) * sl2;
+                // pass 2: P over this half's consumed S columns (keys of chunk c go to
+                // columns pbase + 16 (c - c0))
                 float l = 0.f;
 #pragma unroll
                 for (int c = 0; c < 7; c += 2) {
-                    if (c + 1 < nfull) {
+                    const int cc = c0 + c;
+                    if (cc + 1 < c1) {
                         uint32_t v0[32], v1[32], pk0[16], pk1[16];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
-                        ptx::tmem_ld_32x32b_x32(tS + (c + 1) * 32, v1);
+                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + (cc + 1) * 32, v1);
                         ptx::tmem_ld_wait();
-                        mask_tail(v0, T - c * 32);
-                        mask_tail(v1, T - (c + 1) * 32);
+                        mask_tail(v0, T - cc * 32);
+                        mask_tail(v1, T - (cc + 1) * 32);
                         l += chunk_exp(v0, sl2, m, pk0);
                         l += chunk_exp(v1, sl2, m, pk1);
-                        ptx::tmem_st_32x32b_x16(tS + c * 16, pk0);
-                        ptx::tmem_st_32x32b_x16(tS + (c + 1) * 16, pk1);
-                    } else if (c < nfull) {
+                        ptx::tmem_st_32x32b_x16(tS + pbase + c * 16, pk0);
+                        ptx::tmem_st_32x32b_x16(tS + pbase + (c + 1) * 16, pk1);
+                    } else if (cc < c1) {
                         uint32_t v0[32], pk0[16];
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, v0);
+                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
                         ptx::tmem_ld_wait();
-                        mask_tail(v0, T - c * 32);
+                        mask_tail(v0, T - cc * 32);
                         l += chunk_exp(v0, sl2, m, pk0);
-                        ptx::tmem_st_32x32b_x16(tS + c * 16, pk0);
+                        ptx::tmem_st_32x32b_x16(tS + pbase + c * 16, pk0);
                     }
                 }
                 if (tail) {
                     uint32_t v0[16], pk0[8];
-                    ptx::tmem_ld_32x32b_x16(tS + nfull * 32, v0);
+                    ptx::tmem_ld_32x32b_x16(tS + c1 * 32, v0);
                     ptx::tmem_ld_wait();
-                    mask_tail(v0, T - nfull * 32);
+                    mask_tail(v0, T - c1 * 32);
                     l += chunk_exp(v0, sl2, m, pk0);
-                    ptx::tmem_st_32x32b_x8(tS + nfull * 16, pk0);
+                    ptx::tmem_st_32x32b_x8(tS + pbase + (c1 - c0) * 16, pk0);
                 }
                 ptx::tmem_st_wait();
-                sL[(u & 3) * AW_ROWS + quarter * 32 + lane] = l;
+                sL[((u & 3) * 2 + half) * AW_ROWS + row] = l;
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -344,7 +378,7 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             if (lane == 0) aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
             *abort_flag = 1;
         }
-    } else if (warp >= 12) {
+    } else if (warp < AW_MMA_WARP) {
         // ------------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         const uint32_t tO = tmem + AW_TMEM_O + ((uint32_t)(quarter * 32) << 16);
@@ -371,7 +405,8 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             if (!ok) break;
             const int t = qt * AW_ROWS + quarter * 32 + lane;
             if (live && t < p.T) {
-                const float inv = 1.f / sL[(u & 3) * AW_ROWS + quarter * 32 + lane];
+                const int row = quarter * 32 + lane;
+                const float inv = 1.f / (sL[((u & 3) * 2) * AW_ROWS + row] + sL[((u & 3) * 2 + 1) * AW_ROWS + row]);
                 __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * AW_DH;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
@@ -391,7 +426,7 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     }
 
     __syncthreads();
-    if (warp == 1) {
+    if (warp == AW_MMA_WARP) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
@@ -449,6 +484,7 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
     p.nq = (int)((T + AW_ROWS - 1) / AW_ROWS);
     p.ns = (int)((T + 15) / 16 * 16);
     p.nkb = (p.ns + AW_ROWS - 1) / AW_ROWS;
+    p.split = (p.ns >> 5) / 2 * 32;   // half 0: the first floor(full chunks / 2) chunks
     p.items = (int)(N * H);
     p.scale_log2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
     p.o = static_cast<__nv_bfloat16*>(o);
