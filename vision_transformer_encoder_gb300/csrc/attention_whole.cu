@@ -99,31 +99,28 @@ __device__ __forceinline__ void mask_tail(uint32_t (&v)[W], int lim) {
     }
 }
 
+// Eight independent chains: the reductions are latency-bound otherwise.
 template <int W>
 __device__ __forceinline__ float chunk_max(const uint32_t (&v)[W], float m) {
-    float a = __uint_as_float(v[0]), b = __uint_as_float(v[1]);
+    float a[8];
 #pragma unroll
-    for (int e = 2; e < W; e += 2) {
-        a = fmaxf(a, __uint_as_float(v[e]));
-        b = fmaxf(b, __uint_as_float(v[e + 1]));
-    }
-    return fmaxf(m, fmaxf(a, b));
+    for (int e = 0; e < 8; ++e) a[e] = __uint_as_float(v[e]);
+#pragma unroll
+    for (int e = 8; e < W; ++e) a[e & 7] = fmaxf(a[e & 7], __uint_as_float(v[e]));
+    return fmaxf(m, fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7]))));
 }
 
-// P for W keys: W / 2 packed bf16 pairs; returns the partial row sum.
+// P for W keys: W / 2 packed bf16 pairs, added to the eight partial row sums ls.
 template <int W>
-__device__ __forceinline__ float chunk_exp(const uint32_t (&v)[W], float sl2, float m,
-                                           uint32_t (&pk)[W / 2]) {
-    float s0 = 0.f, s1 = 0.f;
+__device__ __forceinline__ void chunk_exp(const uint32_t (&v)[W], float sl2, float m, uint32_t (&pk)[W / 2],
+                                          float (&ls)[8]) {
 #pragma unroll
     for (int e = 0; e < W; e += 2) {
         const float p0 = exp2_approx(fmaf(__uint_as_float(v[e]), sl2, -m));
         const float p1 = exp2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m));
-        s0 += p0;
-        s1 += p1;
+        ls[(e >> 1) & 7] += p0 + p1;
         pk[e >> 1] = pack_bf16x2(p0, p1);
     }
-    return s0 + s1;
 }
 
 __global__ void __launch_bounds__(AW_THREADS, 1)
@@ -188,7 +185,7 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                 const int item = (int)blockIdx.x + k * (int)gridDim.x;
                 const int n = item / p.H, h = item - n * p.H;
                 const int b = k & 1;
-                if (!ptx::mbar_wait_bounded(&empty[b], ((k >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                if (!ptx::mbar_wait_bounded<true>(&empty[b], ((k >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
                 ptx::mbar_arrive_expect_tx(&full[b], boxes * AW_BOX);
                 for (int r = 0; r < boxes; ++r)
                     ptx::tma_load_3d(ring + (b * 2 + r) * AW_BOX, &tm, &full[b], col0 + h * AW_DH, r * AW_ROWS, n);
@@ -293,19 +290,12 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             const bool live = qt * AW_ROWS + quarter * 32 < T;
             float mx = -INFINITY;
             if (live) {
-                // pass 1: maximum over this half's keys < T, 64 columns per TMEM wait
+                // pass 1: maximum over this half's keys < T (one 32-key chunk per TMEM
+                // wait: two would not fit the register budget of 24 warps)
 #pragma unroll
-                for (int c = 0; c < 7; c += 2) {
+                for (int c = 0; c < 7; ++c) {
                     const int cc = c0 + c;
-                    if (cc + 1 < c1) {
-                        uint32_t v0[32], v1[32];
-                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
-                        ptx::tmem_ld_32x32b_x32(tS + (cc + 1) * 32, v1);
-                        ptx::tmem_ld_wait();
-                        mask_tail(v0, T - cc * 32);
-                        mask_tail(v1, T - (cc + 1) * 32);
-                        mx = chunk_max(v1, chunk_max(v0, mx));
-                    } else if (cc < c1) {
+                    if (cc < c1) {
                         uint32_t v0[32];
                         ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
                         ptx::tmem_ld_wait();
@@ -332,27 +322,16 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                 const float m = fmaxf(mx, mx_other[row]) * sl2;
                 // pass 2: P over this half's consumed S columns (keys of chunk c go to
                 // columns pbase + 16 (c - c0))
-                float l = 0.f;
+                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 7; c += 2) {
+                for (int c = 0; c < 7; ++c) {
                     const int cc = c0 + c;
-                    if (cc + 1 < c1) {
-                        uint32_t v0[32], v1[32], pk0[16], pk1[16];
-                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
-                        ptx::tmem_ld_32x32b_x32(tS + (cc + 1) * 32, v1);
-                        ptx::tmem_ld_wait();
-                        mask_tail(v0, T - cc * 32);
-                        mask_tail(v1, T - (cc + 1) * 32);
-                        l += chunk_exp(v0, sl2, m, pk0);
-                        l += chunk_exp(v1, sl2, m, pk1);
-                        ptx::tmem_st_32x32b_x16(tS + pbase + c * 16, pk0);
-                        ptx::tmem_st_32x32b_x16(tS + pbase + (c + 1) * 16, pk1);
-                    } else if (cc < c1) {
+                    if (cc < c1) {
                         uint32_t v0[32], pk0[16];
                         ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
                         ptx::tmem_ld_wait();
                         mask_tail(v0, T - cc * 32);
-                        l += chunk_exp(v0, sl2, m, pk0);
+                        chunk_exp(v0, sl2, m, pk0, ls);
                         ptx::tmem_st_32x32b_x16(tS + pbase + c * 16, pk0);
                     }
                 }
@@ -361,11 +340,12 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                     ptx::tmem_ld_32x32b_x16(tS + c1 * 32, v0);
                     ptx::tmem_ld_wait();
                     mask_tail(v0, T - c1 * 32);
-                    l += chunk_exp(v0, sl2, m, pk0);
+                    chunk_exp(v0, sl2, m, pk0, ls);
                     ptx::tmem_st_32x32b_x8(tS + pbase + (c1 - c0) * 16, pk0);
                 }
                 ptx::tmem_st_wait();
-                sL[((u & 3) * 2 + half) * AW_ROWS + row] = l;
+                sL[((u & 3) * 2 + half) * AW_ROWS + row] =
+                    ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -388,7 +368,12 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             const int k = u / nq, qt = u - k * nq;
             const int item = (int)blockIdx.x + k * (int)gridDim.x;
             const int n = item / p.H, h = item - n * p.H;
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done, u & 1, abort_flag));
+            // the row sums are in before O (PV waited for them): take 1 / l first
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->l_full[u & 3], (u >> 2) & 1, abort_flag));
+            if (!ok) break;
+            const int row = quarter * 32 + lane;
+            const float inv = 1.f / (sL[((u & 3) * 2) * AW_ROWS + row] + sL[((u & 3) * 2 + 1) * AW_ROWS + row]);
+            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(&bars->o_done, u & 1, abort_flag));
             if (!ok) break;
             ptx::tc_fence_after();
             const bool live = qt * AW_ROWS + quarter * 32 < p.T;
@@ -401,12 +386,8 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bars->o_free);
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->l_full[u & 3], (u >> 2) & 1, abort_flag));
-            if (!ok) break;
-            const int t = qt * AW_ROWS + quarter * 32 + lane;
+            const int t = qt * AW_ROWS + row;
             if (live && t < p.T) {
-                const int row = quarter * 32 + lane;
-                const float inv = 1.f / (sL[((u & 3) * 2) * AW_ROWS + row] + sL[((u & 3) * 2 + 1) * AW_ROWS + row]);
                 __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * AW_DH;
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {

@@ -202,7 +202,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const int n0 = (tile % n_tiles) * BN;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % STAGES, u = it / STAGES;
-                    if (!ptx::mbar_wait_bounded(empty + s, (u & 1) ^ 1, abort_flag)) {
+                    if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -289,7 +289,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int acc = local & 1;
             const uint32_t v = (uint32_t)(local >> 1);
             // The TMEM loads below are warp-collective: the whole warp goes on or stops.
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(tfull + acc, v & 1, abort_flag));
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
             if (!ok) {
                 if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
                 *abort_flag = 1;
@@ -567,7 +567,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const int n0 = (tile % n_tiles) * BN + (int)rank * (BN / 2);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % P_STAGES, u = it / P_STAGES;
-                    if (!ptx::mbar_wait_bounded(empty + s, (u & 1) ^ 1, abort_flag)) {
+                    if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -655,7 +655,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
             const int acc = local & 1;
             const uint32_t v = (uint32_t)(local >> 1);
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(tfull + acc, v & 1, abort_flag));
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
             if (!ok) {
                 if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
                 *abort_flag = 1;

@@ -35,11 +35,24 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-// The waiting thread is suspended until the phase completes or about 100 us pass, so
-// waiting warps do not take issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// The same with a suspend-time hint: the thread sleeps until the phase completes or
+// about 100 us pass, so a warp that waits long does not take issue slots from the
+// warps that work -- at the price of a slower wake-up (a few hundred clocks).
 constexpr uint32_t kWaitSuspendNs = 100000;
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -53,13 +66,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete. Gives up (returns
 // false) after kWaitTimeoutCycles, or as soon as *abort is non-zero.
-// A null `abort` waits for the timeout only.
+// A null `abort` waits for the timeout only. kSleep: suspend between polls (for
+// waits off the critical path).
+template <bool kSleep = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&]() { return kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const long long t0 = clock64();  // SM-local counter: cheap to read in the loop
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll()) return true;
         if (abort && *abort) return false;
         if (clock64() - t0 > kWaitTimeoutCycles) return false;
     }
