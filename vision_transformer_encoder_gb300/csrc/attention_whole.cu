@@ -291,16 +291,24 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             float mx = -INFINITY;
             if (live) {
                 // pass 1: maximum over this half's keys < T (one 32-key chunk per TMEM
-                // wait: two would not fit the register budget of 24 warps)
+                // wait: two would not fit the register budget of 24 warps). A chunk of
+                // valid keys only is reduced by the load itself (tcgen05.ld.red).
 #pragma unroll
                 for (int c = 0; c < 7; ++c) {
                     const int cc = c0 + c;
                     if (cc < c1) {
                         uint32_t v0[32];
-                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
-                        ptx::tmem_ld_wait();
-                        mask_tail(v0, T - cc * 32);
-                        mx = chunk_max(v0, mx);
+                        if (T - cc * 32 >= 32) {
+                            const float cm = ptx::tmem_ld_red_max_32x32b_x32(tS + cc * 32, v0);
+                            ptx::tmem_ld_wait();
+                            ptx::regs_keep(v0);
+                            mx = fmaxf(mx, cm);
+                        } else {
+                            ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
+                            ptx::tmem_ld_wait();
+                            mask_tail(v0, T - cc * 32);
+                            mx = chunk_max(v0, mx);
+                        }
                     }
                 }
                 if (tail) {
