@@ -483,7 +483,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
         p.parts_out[(int64_t)row * p.parts_stride + part_index] = make_float2(cmean, cm2);
 }
 
-constexpr int P_STAGES = 6;
+constexpr int P_STAGES = 5;
 constexpr int P_EPI_WARPS = 8;
 constexpr int P_THREADS = 416;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
                                 // warp 1: MMA; warps 5-12: epilogue
@@ -655,6 +655,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
             const int acc = local & 1;
             const uint32_t v = (uint32_t)(local >> 1);
+            const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
+            const int n0 = (tile % n_tiles) * BN;
+            const int row0 = m0 + quarter * 32;
             const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
             if (!ok) {
                 if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
@@ -662,9 +665,6 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 break;
             }
             ptx::tc_fence_after();
-            const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
-            const int n0 = (tile % n_tiles) * BN;
-            const int row0 = m0 + quarter * 32;
             const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
             epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA>(
                 p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row, row0 + lane, row0,
