@@ -159,6 +159,18 @@ def test_attention_cuda_core_types(dtype):
     _close(out, ref, atol=tol, rtol=tol)
 
 
+@pytest.mark.parametrize("N,T,D,H", [(2, 197, 128, 2), (1, 65, 160, 2), (3, 33, 96, 1), (1, 129, 256, 2),
+                                     (2, 16, 96, 2), (1, 300, 64, 2), (1, 1, 64, 1), (2, 200, 192, 3)])
+def test_attention_fp32_tiled(N, T, D, H):
+    # head widths 32 .. 128: the tiled fp32 kernel (keys and values staged in shared memory)
+    d = _dev()
+    qkv = _rand((N, T, 3 * D), 23 + T, std=1.5, dtype=torch.float32)
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    ref = oracle.attention(qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H)
+    _close(out, ref, atol=1e-5, rtol=1e-5)
+
+
 def test_attention_bf16_generic_head_width():
     # head width 24 is not one the tensor-core kernel takes: CUDA-core kernel, bf16 I/O
     d = _dev()

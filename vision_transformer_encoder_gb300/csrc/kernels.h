@@ -118,6 +118,10 @@ cudaError_t launch_attention_fast(const void* qkv, void* o, int64_t N, int64_t T
                                   int64_t H, cudaStream_t s);
 // tcgen05 flash attention (attention_tc.cu): head widths 64 and 80, bf16, 16-byte
 // aligned buffers. VIT_ATTN_TC=0 disables it (then the kernel above is used).
+// fp32 qkv -> fp32 o on the CUDA cores (head widths 32, 48, 64, 80, 96, 128).
+bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o);
+cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
+                                 cudaStream_t s);
 // Head width 64 and T <= 224: all keys of a row in one S tile, exact one-pass softmax.
 bool attention_whole_supported(int64_t T, int64_t D, int64_t H);
 cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,

@@ -421,7 +421,11 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             if (r == cudaSuccess) r = launch_gemm_simt(k2, s);
             return r;
         }));
-        step(run(K_ATTN, s, [&] { return launch_attention_simt(qkv, acc_dt, buf, a.N, a.T, D, a.H, s); }));
+        step(run(K_ATTN, s, [&] {
+            if (acc_dt == DT_F32 && attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
+                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, s);
+            return launch_attention_simt(qkv, acc_dt, buf, a.N, a.T, D, a.H, s);
+        }));
         step(run(K_WO, s, [&] {
             SimtGemmDesc w{buf, acc_dt, D, a.w_o, dt, D, nullptr, 0, a.x, dt, D, y, acc_dt, D,
                            M, D, D, TC_EPI_RESID};
@@ -703,6 +707,8 @@ int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, i
             return launch_attention_tc(qkv, o, N, T, D, H, st->info, s);
         if (dtype == DT_BF16 && attention_fast_supported(D, H, qkv, o) && (D * 2) % 16 == 0)
             return launch_attention_fast(qkv, o, N, T, D, H, s);
+        if (dtype == DT_F32 && attention_f32_supported(N, T, D, H, qkv, o))
+            return launch_attention_f32(qkv, o, N, T, D, H, s);
         return launch_attention_simt(qkv, dtype, o, N, T, D, H, s);
     });
     if (e != cudaSuccess) {
