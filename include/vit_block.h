@@ -120,8 +120,9 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
  * loads it, until the process exits. A call whose scratch would exceed 64 MiB returns
  * VIT_ERR_UNSUPPORTED before launching anything. (Scratch per token: 12 D + 2 F bytes
  * on the bf16 tensor-core path, e.g. 15,360 bytes for D 768 / F 3072, so 4,369
- * tokens; (5 D + F) times the element size on the other paths; more when VIT_LN_FOLD=1
- * selects the LayerNorm-folded path.) The call makes no
+ * tokens; (5 D + F) times the element size on the other paths, plus on the fp32
+ * tensor-core path 4 max(D, F) bytes per token and 8 (4 D^2 + 2 D F) bytes for the split
+ * weights; more when VIT_LN_FOLD=1 selects the LayerNorm-folded path.) The call makes no
  * cudaMalloc, cudaFree or other allocating call, and nothing in the array needs to be
  * cleared: every scratch byte is written before it is read.
  *

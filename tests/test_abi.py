@@ -89,7 +89,7 @@ def test_step_entry_points_validate(lib):
 
 
 def test_timing_interface_without_gpu(lib):
-    assert lib.vit_timing_kernels() == 9
+    assert lib.vit_timing_kernels() == 10
     ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
     assert lib.vit_timing_read(0, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm)) == 0
     assert nm.value == b"ln1"

@@ -127,6 +127,15 @@ def test_b16_whole_output_properties():
     assert torch.equal(out, inp.x)
 
 
+@pytest.mark.parametrize("N,T,D,H,F", [(2, 197, 128, 2, 256), (1, 65, 160, 2, 320), (3, 33, 96, 3, 192)])
+def test_fp32_tensor_core_path(N, T, D, H, F):
+    # fp32: 3xTF32 tensor-core GEMMs (K a multiple of 4, N a multiple of 4) and the tiled
+    # fp32 attention; shapes with several 128-row and 128-column tiles and ragged tails
+    inp = make_inputs(N, T, D, F, seed=41 + T, dtype=torch.float32, affine=True)
+    out, _ = _run(inp, H, 1e-5, affine=True)
+    assert _maxerr(out, _oracle(inp, H, 1e-5, affine=True)) <= TOL[torch.float32]
+
+
 def test_deterministic_bitwise():
     c = CONFIGS["vit_b16"]
     inp = make_config_inputs("vit_b16", dtype=torch.bfloat16, N=32)

@@ -24,3 +24,16 @@ def test_linear_stages_on_single_cta_kernel():
                         os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "linear"],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_fp32_block_on_cuda_core_gemm():
+    """The fp32 block takes the 3xTF32 tensor-core GEMM by default; VIT_FP32_TC=0 keeps
+    its products on the CUDA-core kernel."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, VIT_FP32_TC="0")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_gpu_block.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]

@@ -1,0 +1,375 @@
+// gemm_tf32.cu -- fp32 GEMMs with fused epilogues on the sm_103a tensor cores, as three
+// TF32 products per step ("3xTF32"):
+//   A B = A_hi B_hi + A_hi B_lo + A_lo B_hi  (+ A_lo B_lo, of relative size 2^-20, dropped)
+// where x_hi is x with its 13 low mantissa bits cleared -- the TF32 value the tensor core
+// takes from an fp32 operand, which it truncates -- and x_lo = x - x_hi, exact in fp32.
+// A single TF32 product per step would leave errors near 1e-3 in the block output.
+//
+// Serves the fp32 path of the block ("ViT Encoder Block" (crackedaicode): the Q, K, V,
+// output and MLP products). Split kernels first write A_lo (same layout as A) and, for a
+// weight stored (in, out), its transpose W^T and W^T_lo (out rows, K contiguous), so both
+// operands are K-major. The GEMM is a single-CTA persistent kernel: 128 x 128 output
+// tiles, K blocks of 32 (one 128-byte swizzled row of fp32), three stages of four 16 KB
+// TMA boxes (A, A_lo, W^T, W^T_lo), one box per producer warp; the MMA warp issues per
+// 8-element K step the three kind::tf32 MMAs into a double-buffered TMEM accumulator;
+// four epilogue warps (one per TMEM lane quarter) add bias and residual or apply GELU
+// (fp32 tanh) and store fp32 rows. Every wait is bounded.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace vit {
+namespace {
+
+constexpr int XM = 128, XN = 128, XK = 32, XSTAGES = 3;
+constexpr int X_BOX = 128 * XK * 4;                  // 16 KB: 128 rows x 32 fp32
+constexpr int X_STAGE = 4 * X_BOX;                   // A, A_lo, W^T, W^T_lo
+constexpr int X_ACC_COLS = XN;
+constexpr int X_TMEM_COLS = 2 * X_ACC_COLS;
+constexpr int X_THREADS = 288;   // warps 0-3 epilogue, 4-7 TMA (one operand each), 8 MMA
+constexpr int X_BAR_BYTES = 256;
+constexpr int X_SMEM = XSTAGES * X_STAGE + X_BAR_BYTES + 1024;
+
+struct XParams {
+    int M, N, K;
+    int epi;                 // TC_EPI_STORE, TC_EPI_GELU or TC_EPI_RESID
+    const float* bias;       // N, or null
+    const float* residual;   // M x N (ldr), for TC_EPI_RESID
+    int64_t ldr;
+    float* out;
+    int64_t ldo;
+    uint32_t* err;
+};
+
+__device__ __forceinline__ void x_error(uint32_t* err, uint32_t bit) {
+    if (err) atomicOr(err, bit);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32 (format 2 at
+// bits 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+
+__global__ void __launch_bounds__(X_THREADS, 1)
+gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
+                   const XParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + XSTAGES * X_STAGE);
+    uint64_t* empty = full + XSTAGES;
+    uint64_t* tfull = empty + XSTAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tiles = (p.M + XM - 1) / XM;
+    const int n_tiles = (p.N + XN - 1) / XN;
+    const int num_tiles = m_tiles * n_tiles;
+    const int kblocks = (p.K + XK - 1) / XK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < XSTAGES; ++s) {
+            ptx::mbar_init(full + s, 4);     // one expect-tx arrival per producer warp
+            ptx::mbar_init(empty + s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull + a, 1);
+            ptx::mbar_init(tempty + a, 128);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 8) {
+        ptx::tmem_alloc(tmem_slot, X_TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp >= 4 && warp <= 7) {
+        if (lane == 0) {
+            // ------------------------------------------ TMA producers, one operand each
+            const int which = warp - 4;   // 0 A, 1 A_lo, 2 W^T, 3 W^T_lo
+            const CUtensorMap* tm = which == 0 ? &tmA : which == 1 ? &tmAlo : which == 2 ? &tmB : &tmBlo;
+            ptx::prefetch_tensormap(tm);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int r0 = which < 2 ? (tile / n_tiles) * XM : (tile % n_tiles) * XN;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % XSTAGES, u = it / XSTAGES;
+                    if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full + s, X_BOX);
+                    ptx::tma_load_2d(smem + s * X_STAGE + which * X_BOX, tm, full + s, kb * XK, r0);
+                }
+            }
+            if (!ok) {
+                x_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
+                *abort_flag = 1;
+            }
+            // let the copies this thread issued land before the CTA can exit
+            for (uint32_t s = 0; s < XSTAGES; ++s) {
+                if (it > s) {
+                    const uint32_t u_last = (it - 1 - s) / XSTAGES;
+                    if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
+                        x_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+                }
+            }
+        }
+    } else if (warp == 8) {
+        if (lane == 0) {
+            // ---------------------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_tf32(XM, XN);
+            uint32_t it = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t v = (uint32_t)(local >> 1);
+                if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * X_ACC_COLS;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const uint32_t s = it % XSTAGES, u = it / XSTAGES;
+                    if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t st = ptx::smem_addr(smem + s * X_STAGE);
+#pragma unroll
+                    for (int k = 0; k < XK / 8; ++k) {
+                        // K-major, 128-byte swizzle: 8 fp32 = 32 bytes per K step
+                        const uint64_t a = ptx::smem_desc(st + k * 32, 16, 1024, ptx::kLayoutSw128);
+                        const uint64_t alo = ptx::smem_desc(st + X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
+                        const uint64_t b = ptx::smem_desc(st + 2 * X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
+                        const uint64_t blo = ptx::smem_desc(st + 3 * X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
+                        mma_tf32(d_tmem, alo, b, idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_tf32(d_tmem, a, blo, idesc, 1u);
+                        mma_tf32(d_tmem, a, b, idesc, 1u);
+                    }
+                    ptx::mma_commit(empty + s);
+                }
+                if (!ok) break;
+                ptx::mma_commit(tfull + acc);
+            }
+            if (!ok) {
+                x_error(p.err, ERRBIT_TIMEOUT_MMA);
+                *abort_flag = 1;
+            }
+            ptx::mma_commit(done);
+            if (!ptx::mbar_wait_bounded(done, 0, nullptr)) x_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------- epilogue warps 0-3
+        const int quarter = warp;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t v = (uint32_t)(local >> 1);
+            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
+            if (!ok) {
+                if (lane == 0) x_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            ptx::tc_fence_after();
+            const int row = (tile / n_tiles) * XM + quarter * 32 + lane;
+            const int n0 = (tile % n_tiles) * XN;
+            const uint32_t t_row = tmem_base + acc * X_ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+#pragma unroll 1
+            for (int c = 0; c < XN / 32; ++c) {
+                uint32_t r[32];
+                ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
+                ptx::tmem_ld_wait();
+                const int col0 = n0 + c * 32;
+                if (row < p.M && col0 < p.N) {
+                    float* orow = p.out + (int64_t)row * p.ldo;
+                    const float* rrow = p.epi == TC_EPI_RESID ? p.residual + (int64_t)row * p.ldr : nullptr;
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const int col = col0 + 4 * j4;
+                        if (col >= p.N) break;   // N is a multiple of 4
+                        float vv[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            float x = __uint_as_float(r[4 * j4 + e]);
+                            if (p.bias) x += p.bias[col + e];
+                            if (p.epi == TC_EPI_GELU) x = gelu_tanh_acc(x);
+                            vv[e] = x;
+                        }
+                        if (rrow) {
+                            const float4 rv = *reinterpret_cast<const float4*>(rrow + col);
+                            vv[0] += rv.x; vv[1] += rv.y; vv[2] += rv.z; vv[3] += rv.w;
+                        }
+                        *reinterpret_cast<float4*>(orow + col) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(tempty + acc);
+        }
+    }
+
+    __syncthreads();
+    if (warp == 8) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, X_TMEM_COLS);
+    }
+}
+
+// A_lo = A - A_hi, written contiguously (rows x cols); cols and lda multiples of 4.
+__global__ void split_lo_kernel(const float* __restrict__ a, int64_t rows, int64_t cols, int64_t lda,
+                                float* __restrict__ lo) {
+    const int64_t q = cols / 4, total = rows * q;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / q, c = (i - r * q) * 4;
+        const float4 v = *reinterpret_cast<const float4*>(a + r * lda + c);
+        *reinterpret_cast<float4*>(lo + r * cols + c) =
+            make_float4(v.x - tf32_hi(v.x), v.y - tf32_hi(v.y), v.z - tf32_hi(v.z), v.w - tf32_hi(v.w));
+    }
+}
+
+// W (K x N, ldw) -> W^T and W^T_lo (N x K) at rows [row0, row0 + N) of the outputs,
+// through 32 x 32 shared-memory tiles.
+__global__ void split_wt_kernel(const float* __restrict__ w, int64_t K, int64_t N, int64_t ldw, int64_t row0,
+                                float* __restrict__ wt, float* __restrict__ wt_lo) {
+    __shared__ float tile[32][33];
+    const int64_t k0 = (int64_t)blockIdx.y * 32, n0 = (int64_t)blockIdx.x * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t k = k0 + i, n = n0 + threadIdx.x;
+        tile[i][threadIdx.x] = (k < K && n < N) ? w[k * ldw + n] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t n = n0 + i, k = k0 + threadIdx.x;
+        if (n < N && k < K) {
+            const float v = tile[threadIdx.x][i];
+            wt[(row0 + n) * K + k] = v;
+            wt_lo[(row0 + n) * K + k] = v - tf32_hi(v);
+        }
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn x_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* q = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &q, 12000, cudaEnableDefault,
+                                             &r) == cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(q);
+    });
+    return fn;
+}
+
+// fp32 rows x cols (ld elements), box 32 x 128, 128-byte swizzle, zero fill past the edges.
+bool make_map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = x_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
+    cuuint32_t box[2] = {(cuuint32_t)XK, 128u};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool tf32x3_supported(int64_t M, int64_t N, int64_t K, int64_t lda, const void* a) {
+    return M > 0 && N > 0 && K > 0 && N % 4 == 0 && K % 4 == 0 && lda % 4 == 0 && aligned16(a) &&
+           M <= 0x7fffffff && N <= 0x7fffffff && K <= 0x7fffffff && x_encode_fn() != nullptr;
+}
+
+cudaError_t launch_split_lo(const float* a, int64_t rows, int64_t cols, int64_t lda, float* lo, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t total = rows * (cols / 4);
+    const int64_t blocks = (total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536;
+    split_lo_kernel<<<(unsigned)blocks, 256, 0, s>>>(a, rows, cols, lda, lo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_wt(const float* w, int64_t K, int64_t N, int64_t ldw, int64_t row0, float* wt, float* wt_lo,
+                            cudaStream_t s) {
+    if (K <= 0 || N <= 0) return cudaSuccess;
+    const dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
+    split_wt_kernel<<<grid, dim3(32, 8), 0, s>>>(w, K, N, ldw, row0, wt, wt_lo);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cudaStream_t s) {
+    if (d.M <= 0 || d.N <= 0) return cudaSuccess;
+    if (!tf32x3_supported(d.M, d.N, d.K, d.lda, d.a) || !aligned16(d.a_lo) || !aligned16(d.wt) ||
+        !aligned16(d.wt_lo) || !aligned16(d.out) || d.ldo % 4 != 0 ||
+        (d.epi == TC_EPI_RESID && (!aligned16(d.residual) || d.ldr % 4 != 0)))
+        return cudaErrorInvalidValue;
+    alignas(64) CUtensorMap ma, malo, mb, mblo;
+    if (!make_map_f32(&ma, d.a, d.M, d.K, d.lda) || !make_map_f32(&malo, d.a_lo, d.M, d.K, d.K) ||
+        !make_map_f32(&mb, d.wt, d.N, d.K, d.K) || !make_map_f32(&mblo, d.wt_lo, d.N, d.K, d.K))
+        return cudaErrorInvalidValue;
+    XParams p;
+    p.M = (int)d.M;
+    p.N = (int)d.N;
+    p.K = (int)d.K;
+    p.epi = d.epi;
+    p.bias = d.bias;
+    p.residual = d.residual;
+    p.ldr = d.ldr;
+    p.out = d.out;
+    p.ldo = d.ldo;
+    p.err = dev.err_word;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, X_SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int64_t tiles = ((d.M + XM - 1) / XM) * ((d.N + XN - 1) / XN);
+    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    gemm_tf32x3_kernel<<<grid, X_THREADS, X_SMEM, s>>>(ma, malo, mb, mblo, p);
+    return cudaGetLastError();
+}
+
+}  // namespace vit

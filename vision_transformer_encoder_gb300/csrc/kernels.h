@@ -118,6 +118,29 @@ cudaError_t launch_attention_fast(const void* qkv, void* o, int64_t N, int64_t T
                                   int64_t H, cudaStream_t s);
 // tcgen05 flash attention (attention_tc.cu): head widths 64 and 80, bf16, 16-byte
 // aligned buffers. VIT_ATTN_TC=0 disables it (then the kernel above is used).
+// fp32 GEMM as three TF32 tensor-core products per step. a_lo (M x K, contiguous) and
+// wt / wt_lo (N x K, contiguous: the weight transposed) come from launch_split_lo /
+// launch_split_wt. out (ldo), bias (N) and residual (ldr) are fp32.
+struct Tf32GemmDesc {
+    const float* a;
+    int64_t lda;
+    const float* a_lo;
+    const float* wt;
+    const float* wt_lo;
+    int64_t M, N, K;
+    int epi;
+    const float* bias;
+    const float* residual;
+    int64_t ldr;
+    float* out;
+    int64_t ldo;
+};
+bool tf32x3_supported(int64_t M, int64_t N, int64_t K, int64_t lda, const void* a);
+cudaError_t launch_split_lo(const float* a, int64_t rows, int64_t cols, int64_t lda, float* lo, cudaStream_t s);
+cudaError_t launch_split_wt(const float* w, int64_t K, int64_t N, int64_t ldw, int64_t row0, float* wt, float* wt_lo,
+                            cudaStream_t s);
+cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cudaStream_t s);
+
 // fp32 qkv -> fp32 o on the CUDA cores (head widths 32, 48, 64, 80, 96, 128).
 bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o);
 cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,

@@ -49,10 +49,11 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<int64_t> g_launches{0};
 
 // ---- per-kernel timing -------------------------------------------------------
-enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_COUNT };
+enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_TF32_SPLIT, K_COUNT };
 const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
                                          "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
-                                         "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep"};
+                                         "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep",
+                                         "tf32_weight_split"};
 struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -193,9 +194,20 @@ struct Workspace {
     int acc_dt;
     size_t sz_buf, sz_qkv, sz_y, sz_h;
     size_t sz_yb, sz_p1, sz_p2, sz_cols, sz_wq, sz_w1, sz_prep;
+    bool tf32;                // fp32 path on the 3xTF32 tensor-core GEMM
+    size_t sz_lo, sz_wt;      // its A_lo scratch and split, transposed weights
     int p2;   // LN2 partials per row
     size_t total;
 };
+
+// The fp32 path uses the 3xTF32 tensor-core GEMM unless VIT_FP32_TC=0.
+bool tf32_requested() {
+    static const bool on = [] {
+        const char* e = std::getenv("VIT_FP32_TC");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 
 Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     Workspace w;
@@ -210,6 +222,13 @@ Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     w.sz_h = round_up((size_t)(M * F) * ea, 256);
     w.p2 = (int)(2 * ((D + 255) / 256));
     w.sz_yb = w.sz_p1 = w.sz_p2 = w.sz_cols = w.sz_wq = w.sz_w1 = w.sz_prep = 0;
+    w.sz_lo = w.sz_wt = 0;
+    w.tf32 = !w.fast && a.dt == DT_F32 && tf32x3_supported(M, 3 * D, D, D, a.x) && F % 4 == 0 &&
+             tf32_requested();
+    if (w.tf32) {
+        w.sz_lo = round_up((size_t)(M * (F > D ? F : D)) * 4, 256);
+        w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
+    }
     if (w.fused) {
         w.sz_yb = round_up((size_t)(M * D) * 2, 256);
         w.sz_p1 = round_up((size_t)M * 8, 256);
@@ -221,7 +240,7 @@ Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
         w.sz_prep = round_up(p1 > p2 ? p1 : p2, 256);
     }
     w.total = w.sz_buf + w.sz_qkv + w.sz_y + w.sz_h + w.sz_yb + w.sz_p1 + w.sz_p2 + w.sz_cols + w.sz_wq +
-              w.sz_w1 + w.sz_prep;
+              w.sz_w1 + w.sz_prep + w.sz_lo + w.sz_wt;
     return w;
 }
 
@@ -402,6 +421,54 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             SimtGemmDesc sd{h, DT_BF16, F, a.w2, DT_BF16, D, a.b2, DT_BF16, y, DT_F32, D,
                             a.out, DT_BF16, D, M, D, F, TC_EPI_RESID};
             return launch_gemm_simt(sd, s);
+        }));
+    } else if (w.tf32) {
+        // fp32: LayerNorm and attention on the CUDA cores, the products as 3xTF32
+        uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // A_lo, then the split weights
+        float* lo = reinterpret_cast<float*>(tail);
+        float* wt = reinterpret_cast<float*>(tail + w.sz_lo);
+        float* wqkv_t = wt, *wqkv_lo = wqkv_t + 3 * D * D;
+        float* wo_t = wqkv_lo + 3 * D * D, *wo_lo = wo_t + D * D;
+        float* w1_t = wo_lo + D * D, *w1_lo = w1_t + F * D;
+        float* w2_t = w1_lo + F * D, *w2_lo = w2_t + D * F;
+        const float* fx = static_cast<const float*>(a.x);
+        float* fbuf = static_cast<float*>(buf);
+        float* fqkv = static_cast<float*>(qkv);
+        float* fy = static_cast<float*>(y);
+        float* fh = static_cast<float*>(h);
+        step(run(K_TF32_SPLIT, s, [&] {
+            const void* wq[3] = {a.w_q, a.w_k, a.w_v};
+            cudaError_t r = cudaSuccess;
+            for (int i = 0; i < 3 && r == cudaSuccess; ++i)
+                r = launch_split_wt(static_cast<const float*>(wq[i]), D, D, D, i * D, wqkv_t, wqkv_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo, s);
+            return r;
+        }));
+        auto gemm = [&](const float* A, int64_t K, const float* bt, const float* btlo, int64_t N, int epi,
+                        const void* bias, const float* res, float* out) {
+            cudaError_t r = launch_split_lo(A, M, K, K, lo, s);
+            if (r != cudaSuccess) return r;
+            Tf32GemmDesc g{A, K, lo, bt, btlo, M, N, K, epi, static_cast<const float*>(bias), res, N, out, N};
+            return launch_gemm_tf32x3(g, dev, s);
+        };
+        step(run(K_LN1, s, [&] {
+            return launch_layernorm(a.x, DT_F32, buf, DT_F32, a.ln1_g, a.ln1_b, DT_F32, M, D, a.eps, s);
+        }));
+        step(run(K_QKV, s, [&] { return gemm(fbuf, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, nullptr, nullptr, fqkv); }));
+        step(run(K_ATTN, s, [&] {
+            if (attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
+                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, s);
+            return launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
+        }));
+        step(run(K_WO, s, [&] { return gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, nullptr, fx, fy); }));
+        step(run(K_LN2, s, [&] {
+            return launch_layernorm(y, DT_F32, buf, DT_F32, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
+        }));
+        step(run(K_W1, s, [&] { return gemm(fbuf, D, w1_t, w1_lo, F, TC_EPI_GELU, a.b1, nullptr, fh); }));
+        step(run(K_W2, s, [&] {
+            return gemm(fh, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, fy, static_cast<float*>(a.out));
         }));
     } else {
         const int dt = a.dt;
