@@ -67,6 +67,12 @@ def open_library(path: str):
     lib.oracle_vit_block.argtypes = ([_dptr] * 13 + [_i64] * 5 + [ctypes.c_double]
                                      + [_dptr] * 7 + [ctypes.c_int])
     lib.oracle_vit_block.restype = ctypes.c_int
+    lib.oracle_vit_block_full.argtypes = ([_dptr] * 17 + [_i64] * 5 + [ctypes.c_double]
+                                          + [_dptr] * 7 + [ctypes.c_int])
+    lib.oracle_vit_block_full.restype = ctypes.c_int
+    lib.oracle_vit_encoder.argtypes = [_dptr, ctypes.POINTER(_dptr), _i64, _dptr, _dptr, ctypes.c_int,
+                                       _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _dptr, ctypes.c_int]
+    lib.oracle_vit_encoder.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -163,3 +169,59 @@ def vit_block(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln1_b=N
     if rc != 0:
         raise ValueError("oracle_vit_block failed with status %d" % rc)
     return (out, st) if stages else out
+
+
+def vit_block_full(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln1_b=None,
+                   ln2_g=None, ln2_b=None, b1=None, b2=None, b_q=None, b_k=None, b_v=None,
+                   b_o=None, stages=False, nthreads=0, lib=None):
+    """vit_block with the optional Q, K, V and output-projection biases."""
+    arrs = [_f64(a) for a in (x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2)]
+    opt = [_f64(a) for a in (ln1_g, ln1_b, ln2_g, ln2_b, b1, b2, b_q, b_k, b_v, b_o)]
+    x64 = arrs[0]
+    if x64.ndim == 2:
+        x64 = x64[None]
+        arrs[0] = x64
+    N, T, D = x64.shape
+    F = arrs[5].shape[1]
+    out = np.empty_like(x64)
+    st = {}
+    if stages:
+        st = {"xn": np.empty((N, T, D)), "qkv": np.empty((N, T, 3 * D)), "o": np.empty((N, T, D)),
+              "y": np.empty((N, T, D)), "yn": np.empty((N, T, D)), "g": np.empty((N, T, F))}
+    names = ("xn", "qkv", "o", "y", "yn", "g")
+    rc = (lib or _load()).oracle_vit_block_full(*[_p(a) for a in arrs], *[_p(a) for a in opt],
+                                       N, T, D, F, int(H), float(eps), _p(out),
+                                       *[_p(st.get(k)) for k in names], int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_vit_block_full failed with status %d" % rc)
+    return (out, st) if stages else out
+
+
+LAYER_KEYS = ("w_q", "w_k", "w_v", "w_o", "w_mlp1", "w_mlp2", "ln1_g", "ln1_b", "ln2_g",
+              "ln2_b", "b1", "b2", "b_q", "b_k", "b_v", "b_o")
+
+
+def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, nthreads=0, lib=None):
+    """A stack of blocks (layers: a list of dicts keyed by LAYER_KEYS; the six weights
+    required, the rest optional) and, with final_ln, the final LayerNorm. Float64."""
+    x64 = _f64(x)
+    if x64.ndim == 2:
+        x64 = x64[None]
+    N, T, D = x64.shape
+    L = len(layers)
+    keep = []
+    ptrs = (_dptr * (16 * L))()
+    F = None
+    for l, lay in enumerate(layers):
+        for j, key in enumerate(LAYER_KEYS):
+            a = _f64(lay.get(key))
+            keep.append(a)
+            ptrs[16 * l + j] = _p(a) if a is not None else _dptr()
+        F = _f64(lay["w_mlp1"]).shape[1]
+    g, b = _f64(lnf_g), _f64(lnf_b)
+    out = np.empty_like(x64)
+    rc = (lib or _load()).oracle_vit_encoder(_p(x64), ptrs, L, _p(g), _p(b), 1 if final_ln else 0,
+                                             N, T, D, int(F), int(H), float(eps), _p(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_vit_encoder failed with status %d" % rc)
+    return out

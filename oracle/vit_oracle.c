@@ -171,14 +171,19 @@ void oracle_attention(const double* Q, const double* K, const double* V,
  *
  * Returns 0 on success, -1 on invalid sizes (non-positive, or H not dividing D),
  * -2 if scratch allocation fails. nthreads <= 0 uses the OpenMP default. */
-int oracle_vit_block(const double* x, const double* w_q, const double* w_k,
-                     const double* w_v, const double* w_o, const double* w_mlp1,
-                     const double* w_mlp2, const double* ln1_g, const double* ln1_b,
-                     const double* ln2_g, const double* ln2_b, const double* b1,
-                     const double* b2, int64_t N, int64_t T, int64_t D, int64_t F,
-                     int64_t H, double eps, double* out, double* st_xn, double* st_qkv,
-                     double* st_o, double* st_y, double* st_yn, double* st_g,
-                     int nthreads)
+/* The block with the optional projection biases of the lecture transcript
+ * (nipunbatra.github.io), Pages 52-53 (Q = LN(x) W_Q + b_Q, likewise K and V) and
+ * Page 71 (the joined heads times W_O plus b_O, then the residual). NULL biases are
+ * absent (zero). */
+int oracle_vit_block_full(const double* x, const double* w_q, const double* w_k,
+                          const double* w_v, const double* w_o, const double* w_mlp1,
+                          const double* w_mlp2, const double* ln1_g, const double* ln1_b,
+                          const double* ln2_g, const double* ln2_b, const double* b1,
+                          const double* b2, const double* b_q, const double* b_k,
+                          const double* b_v, const double* b_o, int64_t N, int64_t T,
+                          int64_t D, int64_t F, int64_t H, double eps, double* out,
+                          double* st_xn, double* st_qkv, double* st_o, double* st_y,
+                          double* st_yn, double* st_g, int nthreads)
 {
     if (N <= 0 || T <= 0 || D <= 0 || F <= 0 || H <= 0 || D % H != 0) return -1;
     int failed = 0;
@@ -204,14 +209,14 @@ int oracle_vit_block(const double* x, const double* w_q, const double* w_k,
 
         /* 1. xn = LN1(x) */
         oracle_layernorm(xs, T, D, eps, ln1_g, ln1_b, xn);
-        /* 2. Q, K, V = xn @ w_q, xn @ w_k, xn @ w_v (no projection biases) */
-        oracle_matmul(xn, w_q, NULL, T, D, D, q);
-        oracle_matmul(xn, w_k, NULL, T, D, D, k);
-        oracle_matmul(xn, w_v, NULL, T, D, D, v);
+        /* 2. Q, K, V = xn @ w_q [+ b_q], xn @ w_k [+ b_k], xn @ w_v [+ b_v] */
+        oracle_matmul(xn, w_q, b_q, T, D, D, q);
+        oracle_matmul(xn, w_k, b_k, T, D, D, k);
+        oracle_matmul(xn, w_v, b_v, T, D, D, v);
         /* 3. per-head unmasked attention, heads concatenated in order */
         attention_one_sequence(q, k, v, T, D, H, o, scratch);
-        /* 4. y = x + o @ w_o  (the residual adds to the un-normalised x) */
-        oracle_matmul(o, w_o, NULL, T, D, D, a);
+        /* 4. y = x + o @ w_o [+ b_o]  (the residual adds to the un-normalised x) */
+        oracle_matmul(o, w_o, b_o, T, D, D, a);
         for (size_t i = 0; i < TD; ++i) y[i] = xs[i] + a[i];
         /* 5. yn = LN2(y)  (LN of y, not of x) */
         oracle_layernorm(y, T, D, eps, ln2_g, ln2_b, yn);
@@ -238,6 +243,64 @@ int oracle_vit_block(const double* x, const double* w_q, const double* w_k,
         free(buf);
     }
     return failed ? -2 : 0;
+}
+
+/* The block as the primary statement defines it: no projection biases. */
+int oracle_vit_block(const double* x, const double* w_q, const double* w_k,
+                     const double* w_v, const double* w_o, const double* w_mlp1,
+                     const double* w_mlp2, const double* ln1_g, const double* ln1_b,
+                     const double* ln2_g, const double* ln2_b, const double* b1,
+                     const double* b2, int64_t N, int64_t T, int64_t D, int64_t F,
+                     int64_t H, double eps, double* out, double* st_xn, double* st_qkv,
+                     double* st_o, double* st_y, double* st_yn, double* st_g,
+                     int nthreads)
+{
+    return oracle_vit_block_full(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, ln1_g, ln1_b, ln2_g,
+                                 ln2_b, b1, b2, NULL, NULL, NULL, NULL, N, T, D, F, H, eps,
+                                 out, st_xn, st_qkv, st_o, st_y, st_yn, st_g, nthreads);
+}
+
+/* A stack of L blocks and an optional final LayerNorm: "ViT Encoder Block"
+ * (ai-engineer-exhaustive), introduction (L identical blocks, each with its own
+ * weights); lecture transcript (nipunbatra.github.io), Pages 76-77 (block l's output is
+ * block l+1's input) and Pages 111-112 (twelve blocks, then the final normalisation of
+ * all rows); "E2E: Tiny Vision Transformer" (mlgrind), forward diagram (final LN).
+ * layers: L x 16 pointers per layer, in the order w_q, w_k, w_v, w_o, w_mlp1, w_mlp2,
+ * ln1_g, ln1_b, ln2_g, ln2_b, b1, b2, b_q, b_k, b_v, b_o (the last ten may be NULL).
+ * final_ln != 0 applies LN(., eps) with the nullable gain lnf_g and bias lnf_b. */
+int oracle_vit_encoder(const double* x, const double* const* layers, int64_t L,
+                       const double* lnf_g, const double* lnf_b, int final_ln, int64_t N,
+                       int64_t T, int64_t D, int64_t F, int64_t H, double eps, double* out,
+                       int nthreads)
+{
+    if (L <= 0 || N <= 0 || T <= 0 || D <= 0) return -1;
+    const size_t ND = (size_t)(N * T * D);
+    double* r0 = (double*)malloc(sizeof(double) * ND);
+    double* r1 = (double*)malloc(sizeof(double) * ND);
+    if (!r0 || !r1) {
+        free(r0);
+        free(r1);
+        return -2;
+    }
+    const double* cur = x;
+    int rc = 0;
+    for (int64_t l = 0; l < L && rc == 0; ++l) {
+        const double* const* w = layers + (size_t)l * 16;
+        double* nxt = (l & 1) ? r1 : r0;
+        rc = oracle_vit_block_full(cur, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7], w[8],
+                                   w[9], w[10], w[11], w[12], w[13], w[14], w[15], N, T, D, F,
+                                   H, eps, nxt, NULL, NULL, NULL, NULL, NULL, NULL, nthreads);
+        cur = nxt;
+    }
+    if (rc == 0) {
+        if (final_ln)
+            oracle_layernorm(cur, N * T, D, eps, lnf_g, lnf_b, out);
+        else
+            memcpy(out, cur, sizeof(double) * ND);
+    }
+    free(r0);
+    free(r1);
+    return rc;
 }
 
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */

@@ -45,6 +45,44 @@ def _rand_block(N, T, D, F, seed, affine=False):
     return a
 
 
+def _call_full(a, H, eps, **kw):
+    return oracle.vit_block_full(a["x"], a["w_q"], a["w_k"], a["w_v"], a["w_o"], a["w_mlp1"],
+                                 a["w_mlp2"], H, eps, **{k: a.get(k) for k in
+                                                         ("ln1_g", "ln1_b", "ln2_g", "ln2_b", "b1", "b2",
+                                                          "b_q", "b_k", "b_v", "b_o")}, **kw)
+
+
+def _with_proj_biases(a, seed):
+    rng = np.random.default_rng(seed)
+    D = a["w_q"].shape[0]
+    a = dict(a)
+    a.update(b_q=0.2 * rng.standard_normal(D), b_k=0.2 * rng.standard_normal(D),
+             b_v=0.2 * rng.standard_normal(D), b_o=0.2 * rng.standard_normal(D))
+    return a
+
+
+def _rand_layers(L, D, F, seed, affine=True, biases=True):
+    layers = []
+    for l in range(L):
+        a = _rand_block(1, 1, D, F, seed=seed + 17 * l, affine=affine)
+        a.pop("x")
+        if biases:
+            a = _with_proj_biases(a, seed + 31 * l)
+        layers.append(a)
+    return layers
+
+
+def _torch_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True):
+    """The stack written with the float64 PyTorch block above, then torch's layer_norm."""
+    cur = np.asarray(x, dtype=np.float64)
+    for lay in layers:
+        cur = _torch_block(dict(lay, x=cur), H, eps)
+    if not final_ln:
+        return cur
+    t = lambda v: None if v is None else torch.from_numpy(np.asarray(v, dtype=np.float64))
+    return Fn.layer_norm(torch.from_numpy(cur), (cur.shape[-1],), t(lnf_g), t(lnf_b), eps=eps).numpy()
+
+
 def _call(a, H, eps, **kw):
     return oracle.vit_block(a["x"], a["w_q"], a["w_k"], a["w_v"], a["w_o"], a["w_mlp1"],
                             a["w_mlp2"], H, eps, ln1_g=a.get("ln1_g"), ln1_b=a.get("ln1_b"),
@@ -201,9 +239,15 @@ def _torch_block(a, H, eps):
 
     def heads(m):
         return m.reshape(N, T, H, dh).transpose(1, 2)
-    q, k, v = heads(xn @ t["w_q"]), heads(xn @ t["w_k"]), heads(xn @ t["w_v"])
+    def proj(w, b):
+        m = xn @ t[w]
+        return m + t[b] if b in t else m
+    q, k, v = heads(proj("w_q", "b_q")), heads(proj("w_k", "b_k")), heads(proj("w_v", "b_v"))
     o = Fn.scaled_dot_product_attention(q, k, v).transpose(1, 2).reshape(N, T, D)
-    y = x + o @ t["w_o"]
+    a_o = o @ t["w_o"]
+    if "b_o" in t:
+        a_o = a_o + t["b_o"]
+    y = x + a_o
     yn = Fn.layer_norm(y, (D,), t.get("ln2_g"), t.get("ln2_b"), eps=eps)
     z = yn @ t["w_mlp1"]
     if "b1" in t:
@@ -330,6 +374,69 @@ def test_invalid_sizes_rejected():
 # The pins above catch plausible slips: each mutant is a copy of the oracle source
 # with one mistake planted (compiled on the CPU into a temporary library).
 # ---------------------------------------------------------------------------------
+@pytest.mark.parametrize("shape", [(2, 7, 12, 20, 3), (1, 33, 16, 64, 1), (2, 65, 40, 80, 4)])
+def test_projection_biases_match_torch(shape):
+    N, T, D, F, H = shape
+    a = _with_proj_biases(_rand_block(N, T, D, F, seed=7 + T, affine=True), seed=T)
+    np.testing.assert_allclose(_call_full(a, H, 1e-5), _torch_block(a, H, 1e-5), rtol=0, atol=1e-11)
+
+
+def test_key_bias_changes_nothing():
+    # a key bias shifts every score of a query row by q . b_k: the softmax ignores it
+    a = _rand_block(2, 9, 12, 24, seed=8, affine=True)
+    b = dict(a, b_k=np.random.default_rng(1).standard_normal(12))
+    np.testing.assert_allclose(_call_full(b, 3, 1e-6), _call_full(a, 3, 1e-6), rtol=0, atol=1e-12)
+
+
+def test_value_bias_alone_gives_constant_heads():
+    # w_v = 0: every value row is b_v, and attention weights sum to one, so o = b_v
+    a = _rand_block(2, 9, 12, 24, seed=9)
+    c = np.random.default_rng(2).standard_normal(12)
+    a = dict(a, w_v=np.zeros((12, 12)), b_v=c)
+    _, st = _call_full(a, 3, 1e-6, stages=True)
+    np.testing.assert_allclose(st["o"], np.broadcast_to(c, st["o"].shape), rtol=0, atol=1e-14)
+
+
+def test_output_bias_with_zero_wo():
+    a = _rand_block(2, 9, 12, 24, seed=10)
+    c = np.random.default_rng(3).standard_normal(12)
+    a = dict(a, w_o=np.zeros((12, 12)), b_o=c)
+    _, st = _call_full(a, 3, 1e-6, stages=True)
+    np.testing.assert_array_equal(st["y"], a["x"] + c)
+
+
+def test_encoder_single_layer_is_the_block():
+    a = _with_proj_biases(_rand_block(2, 9, 12, 24, seed=11, affine=True), seed=4)
+    lay = {k: v for k, v in a.items() if k != "x"}
+    np.testing.assert_array_equal(oracle.vit_encoder(a["x"], [lay], 3, 1e-6, final_ln=False),
+                                  _call_full(a, 3, 1e-6))
+
+
+@pytest.mark.parametrize("L,shape", [(3, (2, 9, 12, 24, 3)), (2, (1, 33, 16, 64, 2)), (4, (2, 5, 8, 16, 2))])
+def test_encoder_matches_torch_stack(L, shape):
+    N, T, D, F, H = shape
+    rng = np.random.default_rng(L)
+    x = rng.standard_normal((N, T, D))
+    layers = _rand_layers(L, D, F, seed=50 + L)
+    g, b = 1 + 0.1 * rng.standard_normal(D), 0.1 * rng.standard_normal(D)
+    np.testing.assert_allclose(oracle.vit_encoder(x, layers, H, 1e-6, lnf_g=g, lnf_b=b),
+                               _torch_encoder(x, layers, H, 1e-6, g, b), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(oracle.vit_encoder(x, layers, H, 1e-6, final_ln=False),
+                               _torch_encoder(x, layers, H, 1e-6, final_ln=False), rtol=0, atol=1e-11)
+
+
+def test_encoder_without_updates_is_layernorm_of_x():
+    # every block with w_o = 0 and w_mlp2 = 0 (no biases) returns its input exactly, so the
+    # stack is the final LayerNorm of x
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((2, 7, 12))
+    layers = _rand_layers(3, 12, 24, seed=70, affine=True, biases=False)
+    for lay in layers:
+        lay.update(w_o=np.zeros((12, 12)), w_mlp2=np.zeros((24, 12)), b2=np.zeros(12))
+    np.testing.assert_array_equal(oracle.vit_encoder(x, layers, 3, 1e-6, final_ln=False), x)
+    np.testing.assert_array_equal(oracle.vit_encoder(x, layers, 3, 1e-6), oracle.layernorm(x, 1e-6))
+
+
 MUTANTS = {
     "eps_fixed_1e-5": ("sqrt(var + eps)", "sqrt(var + 1e-5)"),
     "sample_variance": ("var /= (double)D;", "var /= (double)(D - 1 > 0 ? D - 1 : 1);"),
@@ -352,7 +459,15 @@ MUTANTS = {
     "gelu_constant": ("0.044715 * z * z * z", "0.04471 * z * z * z"),
     "gelu_square": ("0.044715 * z * z * z", "0.044715 * z * z"),
     "drop_b1": ("oracle_matmul(yn, w_mlp1, b1, T, D, F, z);", "oracle_matmul(yn, w_mlp1, NULL, T, D, F, z);"),
-    "wk_for_wv": ("oracle_matmul(xn, w_v, NULL, T, D, D, v);", "oracle_matmul(xn, w_k, NULL, T, D, D, v);"),
+    "wk_for_wv": ("oracle_matmul(xn, w_v, b_v, T, D, D, v);", "oracle_matmul(xn, w_k, b_v, T, D, D, v);"),
+    "drop_b_q": ("oracle_matmul(xn, w_q, b_q, T, D, D, q);", "oracle_matmul(xn, w_q, NULL, T, D, D, q);"),
+    "drop_b_v": ("oracle_matmul(xn, w_v, b_v, T, D, D, v);", "oracle_matmul(xn, w_v, NULL, T, D, D, v);"),
+    "drop_b_o": ("oracle_matmul(o, w_o, b_o, T, D, D, a);", "oracle_matmul(o, w_o, NULL, T, D, D, a);"),
+    "encoder_reuses_layer0": ("const double* const* w = layers + (size_t)l * 16;",
+                              "const double* const* w = layers + (size_t)l * 0;"),
+    "encoder_restarts_from_x": ("        cur = nxt;\n", "        cur = (l + 1 < L) ? x : nxt;\n"),
+    "final_ln_without_affine": ("oracle_layernorm(cur, N * T, D, eps, lnf_g, lnf_b, out);",
+                                "oracle_layernorm(cur, N * T, D, eps, NULL, NULL, out);"),
 }
 
 
@@ -368,7 +483,16 @@ def _pins_pass(lib):
         a = _rand_block(N, T, D, F, seed=21, affine=affine)
         if not np.allclose(_call(a, H, 1e-5, lib=lib), _torch_block(a, H, 1e-5), rtol=0, atol=1e-11):
             return False
-    return True
+    # projection biases and the stack with its final LayerNorm
+    a = _with_proj_biases(_rand_block(2, 7, 12, 20, seed=22, affine=True), seed=5)
+    if not np.allclose(_call_full(a, 3, 1e-5, lib=lib), _torch_block(a, 3, 1e-5), rtol=0, atol=1e-11):
+        return False
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((2, 7, 12))
+    layers = _rand_layers(3, 12, 20, seed=90)
+    g, b = 1 + 0.1 * rng.standard_normal(12), 0.1 * rng.standard_normal(12)
+    got = oracle.vit_encoder(x, layers, 3, 1e-5, lnf_g=g, lnf_b=b, lib=lib)
+    return bool(np.allclose(got, _torch_encoder(x, layers, 3, 1e-5, g, b), rtol=0, atol=1e-11))
 
 
 def test_pins_pass_on_unmodified_source(tmp_path):
