@@ -66,7 +66,10 @@ typedef enum {
  *   eps      LN epsilon (> 0 recommended; any finite value is accepted)
  *   dtype    VIT_BF16: bf16 storage, fp32 accumulation; LN statistics, softmax and
  *            GELU in fp32; y kept in fp32; out rounded to bf16 (round-to-nearest-even).
- *            VIT_F32: fp32 throughout. VIT_F64: fp64 throughout.
+ *            VIT_F32: fp32 storage, LN, softmax and GELU in fp32; the matrix products
+ *            as three TF32 tensor-core products per step (hi*hi + hi*lo + lo*hi, about
+ *            fp32 accuracy; VIT_FP32_TC=0 selects fp32 CUDA-core products).
+ *            VIT_F64: fp64 throughout.
  *   out      (N, T, D), must not overlap any input
  * Errors: VIT_ERR_ARG, VIT_ERR_DTYPE, VIT_ERR_NOMEM, VIT_ERR_CUDA (and VIT_ERR_TIMEOUT
  * under VIT_DEBUG_SYNC=1). On error nothing is guaranteed about `out`.
@@ -144,6 +147,38 @@ int vit_block_noalloc(const void* x, const void* w_q, const void* w_k, const voi
  * the same kernels as vit_block and exist for stage-by-stage checking and for
  * callers that compose the stages differently.
  * ------------------------------------------------------------------------------ */
+
+/*
+ * vit_encoder -- a stack of L encoder blocks and an optional final LayerNorm.
+ *
+ * Definition: "ViT Encoder Block" (ai-engineer-exhaustive), introduction (L identical
+ * blocks, each with its own weights); lecture transcript (nipunbatra.github.io), Pages
+ * 76-77 (block l's whole output is block l+1's input) and Pages 111-112 (the final
+ * normalisation of all rows after the stack); the Q, K, V and output-projection biases
+ * of Pages 52-53 and 71 (Q = LN(x) W_Q + b_Q, likewise K and V; the joined heads times
+ * W_O plus b_O, then the residual). Each block is vit_block_ex plus those biases.
+ *
+ *   x          (N, T, D) input tokens, `dtype`
+ *   layers     HOST array of L vit_layer records (their pointers are device pointers,
+ *              `dtype`): the six weights as in vit_block, the other ten nullable
+ *              (absent = gain 1, bias 0)
+ *   lnf_g, lnf_b  (D) nullable gain and bias of the final LayerNorm
+ *   final_ln   1: out = LN(stack output, eps); 0: out = stack output
+ *   other arguments as vit_block
+ * Between blocks the residual stream is kept in fp32 on the bf16 path (in `dtype`
+ * otherwise); only `out` is rounded to `dtype`. Errors as vit_block; VIT_ERR_ARG also for
+ * L < 1, a null `layers` or a null weight.
+ */
+typedef struct {
+    const void *w_q, *w_k, *w_v, *w_o, *w_mlp1, *w_mlp2;
+    const void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+    const void *b1, *b2;
+    const void *b_q, *b_k, *b_v, *b_o;
+} vit_layer;
+
+int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g,
+                const void* lnf_b, int final_ln, int64_t N, int64_t T, int64_t D, int64_t F,
+                int64_t H, double eps, int dtype, void* out, void* stream);
 
 /*
  * vit_layernorm -- out[r, :] = LN(x[r, :]) [* gamma + beta] for r < rows.

@@ -89,8 +89,23 @@ def test_step_entry_points_validate(lib):
 
 
 def test_timing_interface_without_gpu(lib):
-    assert lib.vit_timing_kernels() == 10
+    assert lib.vit_timing_kernels() == 11
     ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
     assert lib.vit_timing_read(0, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm)) == 0
     assert nm.value == b"ln1"
     assert lib.vit_timing_read(99, None, None, None) == -1
+
+
+def test_encoder_argument_checks(lib):
+    layer = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 10)
+    arr = (api.VitLayer * 1)(layer)
+    assert lib.vit_encoder(_fake(0), arr, 0, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    assert lib.vit_encoder(_fake(0), None, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    assert lib.vit_encoder(_fake(0), arr, 1, None, None, 1, 2, 5, 8, 16, 3, 1e-5, 1, _fake(10), None) == -1
+    assert lib.vit_encoder(_fake(0), arr, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 7, _fake(10), None) == -2
+    bad = (api.VitLayer * 1)(api.VitLayer(*[_fake(i + 1).value for i in range(5)] + [None] * 11))
+    assert lib.vit_encoder(_fake(0), bad, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    # out overlapping a projection bias
+    lay2 = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 6 + [_fake(10).value + 8] + [None] * 3)
+    arr2 = (api.VitLayer * 1)(lay2)
+    assert lib.vit_encoder(_fake(0), arr2, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1

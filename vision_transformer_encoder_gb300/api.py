@@ -21,6 +21,15 @@ EPI_STORE, EPI_GELU, EPI_RESIDUAL = 0, 1, 2
 
 _DT = {torch.float32: VIT_F32, torch.bfloat16: VIT_BF16, torch.float64: VIT_F64}
 
+LAYER_FIELDS = ("w_q", "w_k", "w_v", "w_o", "w_mlp1", "w_mlp2", "ln1_g", "ln1_b", "ln2_g", "ln2_b",
+                "b1", "b2", "b_q", "b_k", "b_v", "b_o")
+
+
+class VitLayer(ctypes.Structure):
+    """vit_layer of include/vit_block.h: sixteen device pointers of one block."""
+    _fields_ = [(name, ctypes.c_void_p) for name in LAYER_FIELDS]
+
+
 # Every exported symbol of the C ABI, with (restype, argtypes).
 _vp, _i64, _int, _dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
 SIGNATURES = {
@@ -28,6 +37,8 @@ SIGNATURES = {
     "vit_block_ex": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_block_host": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_block_noalloc": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
+    "vit_encoder": (_int, [_vp, ctypes.POINTER(VitLayer), _i64, _vp, _vp, _int] + [_i64] * 5
+                    + [_dbl, _int, _vp, _vp]),
     "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
     "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
     "vit_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _vp, _vp]),
@@ -148,6 +159,33 @@ def vit_block(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, out=None, stream=No
         rc = lib.vit_block(_ptr(x), *[_ptr(w) for w in ws], N, T, D, F, int(H), float(eps),
                            _dtype_code(dt), _ptr(out), _stream(stream))
     _check(rc, "vit_block")
+    return out
+
+
+def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, out=None, stream=None):
+    """out (N, T, D) = the stack of blocks in `layers` (a list of dicts keyed by
+    LAYER_FIELDS: the six weights required, the rest optional), then, with final_ln,
+    the final LayerNorm with the optional gain lnf_g and bias lnf_b."""
+    lib = load_library()
+    dt = x.dtype
+    _dev(x, "x", dt)
+    arr = (VitLayer * max(len(layers), 1))()
+    for i, lay in enumerate(layers):
+        for name in LAYER_FIELDS:
+            t = lay.get(name)
+            _dev(t, "layer %d %s" % (i, name), dt)
+            setattr(arr[i], name, None if t is None else t.data_ptr())
+    _dev(lnf_g, "lnf_g", dt)
+    _dev(lnf_b, "lnf_b", dt)
+    N, T, D = x.shape
+    F = layers[0]["w_mlp1"].shape[1] if layers else 0
+    if out is None:
+        out = torch.empty_like(x)
+    _dev(out, "out", dt)
+    with torch.cuda.device(x.device):
+        rc = lib.vit_encoder(_ptr(x), arr, len(layers), _ptr(lnf_g), _ptr(lnf_b), 1 if final_ln else 0,
+                             N, T, D, F, int(H), float(eps), _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_encoder")
     return out
 
 

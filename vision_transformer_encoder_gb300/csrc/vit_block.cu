@@ -49,11 +49,12 @@ DeviceState g_dev[kMaxDevices];
 std::atomic<int64_t> g_launches{0};
 
 // ---- per-kernel timing -------------------------------------------------------
-enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_TF32_SPLIT, K_COUNT };
+enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_TF32_SPLIT, K_FINAL_LN,
+            K_COUNT };
 const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
                                          "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
                                          "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep",
-                                         "tf32_weight_split"};
+                                         "tf32_weight_split", "final_ln"};
 struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -150,7 +151,30 @@ struct BlockArgs {
     double eps;
     int dt;
     void* out;
+    // For blocks inside a stack: x and out may be the fp32 residual stream (-1: dt), and
+    // the projection biases (dt) may be given; bias_scratch holds 3D elements of dt for
+    // the concatenated [b_q | b_k | b_v] of the fused QKV product.
+    int x_dt = -1, out_dt = -1;
+    const void *b_q = nullptr, *b_k = nullptr, *b_v = nullptr, *b_o = nullptr;
+    void* bias_scratch = nullptr;
 };
+
+inline int x_dtype(const BlockArgs& a) { return a.x_dt < 0 ? a.dt : a.x_dt; }
+inline int out_dtype(const BlockArgs& a) { return a.out_dt < 0 ? a.dt : a.out_dt; }
+inline bool has_qkv_bias(const BlockArgs& a) { return a.b_q || a.b_k || a.b_v; }
+
+// [b_q | b_k | b_v] into a.bias_scratch (absent ones zero), in stream order.
+cudaError_t concat_qkv_bias(const BlockArgs& a, cudaStream_t s) {
+    const size_t nb = (size_t)a.D * dt_size(a.dt);
+    const void* b[3] = {a.b_q, a.b_k, a.b_v};
+    for (int i = 0; i < 3; ++i) {
+        uint8_t* dst = static_cast<uint8_t*>(a.bias_scratch) + i * nb;
+        cudaError_t e = b[i] ? cudaMemcpyAsync(dst, b[i], nb, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemsetAsync(dst, 0, nb, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 int validate(const BlockArgs& a) {
     if (a.dt != DT_F32 && a.dt != DT_BF16 && a.dt != DT_F64) return VIT_ERR_DTYPE;
@@ -362,8 +386,10 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         if (e == cudaSuccess) e = err;
     };
     if (fast) {
+        const int xdt = x_dtype(a), odt = out_dtype(a);
+        if (has_qkv_bias(a)) step(concat_qkv_bias(a, s));
         step(run(K_LN1, s, [&] {
-            return launch_layernorm(a.x, DT_BF16, buf, DT_BF16, a.ln1_g, a.ln1_b, DT_BF16, M, D,
+            return launch_layernorm(a.x, xdt, buf, DT_BF16, a.ln1_g, a.ln1_b, DT_BF16, M, D,
                                     a.eps, s);
         }));
         TcGemmDesc g;
@@ -372,16 +398,17 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         g.w[0] = a.w_q; g.w[1] = a.w_k; g.w[2] = a.w_v; g.n_w = 3; g.n_per_w = D;
         g.M = M; g.N = 3 * D; g.K = D;
         g.epi = TC_EPI_STORE;
+        g.bias = has_qkv_bias(a) ? a.bias_scratch : nullptr;
         g.out = qkv; g.ldo = 3 * D; g.out_f32 = false;
         const bool tc = tc_gemm_supported(g);
         step(run(K_QKV, s, [&] {
             if (tc) return launch_gemm_tc(g, dev, s);
-            SimtGemmDesc sd{buf, DT_BF16, D, a.w_q, DT_BF16, D, nullptr, 0, nullptr, 0, 0,
+            SimtGemmDesc sd{buf, DT_BF16, D, a.w_q, DT_BF16, D, a.b_q, DT_BF16, nullptr, 0, 0,
                             qkv, DT_BF16, 3 * D, M, D, D, TC_EPI_STORE};
             cudaError_t r = launch_gemm_simt(sd, s);
-            sd.w = a.w_k; sd.out = static_cast<__nv_bfloat16*>(qkv) + D;
+            sd.w = a.w_k; sd.bias = a.b_k; sd.out = static_cast<__nv_bfloat16*>(qkv) + D;
             if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
-            sd.w = a.w_v; sd.out = static_cast<__nv_bfloat16*>(qkv) + 2 * D;
+            sd.w = a.w_v; sd.bias = a.b_v; sd.out = static_cast<__nv_bfloat16*>(qkv) + 2 * D;
             if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
             return r;
         }));
@@ -393,11 +420,11 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             return launch_attention_simt(qkv, DT_BF16, buf, a.N, a.T, D, a.H, s);
         }));
         g.a = buf; g.w[0] = a.w_o; g.n_w = 1; g.n_per_w = D; g.N = D; g.K = D;
-        g.epi = TC_EPI_RESID; g.residual = a.x; g.ldr = D; g.residual_f32 = false;
+        g.epi = TC_EPI_RESID; g.bias = a.b_o; g.residual = a.x; g.ldr = D; g.residual_f32 = xdt == DT_F32;
         g.out = y; g.ldo = D; g.out_f32 = true;
         step(run(K_WO, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
-            SimtGemmDesc sd{buf, DT_BF16, D, a.w_o, DT_BF16, D, nullptr, 0, a.x, DT_BF16, D,
+            SimtGemmDesc sd{buf, DT_BF16, D, a.w_o, DT_BF16, D, a.b_o, DT_BF16, a.x, xdt, D,
                             y, DT_F32, D, M, D, D, TC_EPI_RESID};
             return launch_gemm_simt(sd, s);
         }));
@@ -415,11 +442,11 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
         g.a = h; g.lda = F; g.w[0] = a.w2; g.n_w = 1; g.n_per_w = D; g.N = D; g.K = F;
         g.epi = TC_EPI_RESID; g.bias = a.b2; g.residual = y; g.ldr = D; g.residual_f32 = true;
-        g.out = a.out; g.ldo = D; g.out_f32 = false;
+        g.out = a.out; g.ldo = D; g.out_f32 = odt == DT_F32;
         step(run(K_W2, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{h, DT_BF16, F, a.w2, DT_BF16, D, a.b2, DT_BF16, y, DT_F32, D,
-                            a.out, DT_BF16, D, M, D, F, TC_EPI_RESID};
+                            a.out, odt, D, M, D, F, TC_EPI_RESID};
             return launch_gemm_simt(sd, s);
         }));
     } else if (w.tf32) {
@@ -456,13 +483,15 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         step(run(K_LN1, s, [&] {
             return launch_layernorm(a.x, DT_F32, buf, DT_F32, a.ln1_g, a.ln1_b, DT_F32, M, D, a.eps, s);
         }));
-        step(run(K_QKV, s, [&] { return gemm(fbuf, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, nullptr, nullptr, fqkv); }));
+        if (has_qkv_bias(a)) step(concat_qkv_bias(a, s));
+        const void* bqkv = has_qkv_bias(a) ? a.bias_scratch : nullptr;
+        step(run(K_QKV, s, [&] { return gemm(fbuf, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, bqkv, nullptr, fqkv); }));
         step(run(K_ATTN, s, [&] {
             if (attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
                 return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, s);
             return launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
         }));
-        step(run(K_WO, s, [&] { return gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, nullptr, fx, fy); }));
+        step(run(K_WO, s, [&] { return gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy); }));
         step(run(K_LN2, s, [&] {
             return launch_layernorm(y, DT_F32, buf, DT_F32, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
         }));
@@ -473,17 +502,19 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     } else {
         const int dt = a.dt;
         step(run(K_LN1, s, [&] {
-            return launch_layernorm(a.x, dt, buf, acc_dt, a.ln1_g, a.ln1_b, dt, M, D, a.eps, s);
+            return launch_layernorm(a.x, x_dtype(a), buf, acc_dt, a.ln1_g, a.ln1_b, dt, M, D, a.eps, s);
         }));
-        SimtGemmDesc sd{buf, acc_dt, D, a.w_q, dt, D, nullptr, 0, nullptr, 0, 0, qkv, acc_dt, 3 * D,
+        SimtGemmDesc sd{buf, acc_dt, D, a.w_q, dt, D, a.b_q, dt, nullptr, 0, 0, qkv, acc_dt, 3 * D,
                         M, D, D, TC_EPI_STORE};
         step(run(K_QKV, s, [&] {
             cudaError_t r = launch_gemm_simt(sd, s);
             SimtGemmDesc k2 = sd;
             k2.w = a.w_k;
+            k2.bias = a.b_k;
             k2.out = static_cast<uint8_t*>(qkv) + D * ea;
             if (r == cudaSuccess) r = launch_gemm_simt(k2, s);
             k2.w = a.w_v;
+            k2.bias = a.b_v;
             k2.out = static_cast<uint8_t*>(qkv) + 2 * D * ea;
             if (r == cudaSuccess) r = launch_gemm_simt(k2, s);
             return r;
@@ -494,7 +525,7 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             return launch_attention_simt(qkv, acc_dt, buf, a.N, a.T, D, a.H, s);
         }));
         step(run(K_WO, s, [&] {
-            SimtGemmDesc w{buf, acc_dt, D, a.w_o, dt, D, nullptr, 0, a.x, dt, D, y, acc_dt, D,
+            SimtGemmDesc w{buf, acc_dt, D, a.w_o, dt, D, a.b_o, dt, a.x, x_dtype(a), D, y, acc_dt, D,
                            M, D, D, TC_EPI_RESID};
             return launch_gemm_simt(w, s);
         }));
@@ -507,7 +538,7 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             return launch_gemm_simt(w, s);
         }));
         step(run(K_W2, s, [&] {
-            SimtGemmDesc w{h, acc_dt, F, a.w2, dt, D, a.b2, dt, y, acc_dt, D, a.out, dt, D,
+            SimtGemmDesc w{h, acc_dt, F, a.w2, dt, D, a.b2, dt, y, acc_dt, D, a.out, out_dtype(a), D,
                            M, D, F, TC_EPI_RESID};
             return launch_gemm_simt(w, s);
         }));
@@ -628,6 +659,87 @@ int vit_block(const void* x, const void* w_q, const void* w_k, const void* w_v, 
               int64_t H, double eps, int dtype, void* out, void* stream) {
     return vit_block_ex(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, nullptr, nullptr, nullptr, nullptr,
                         nullptr, nullptr, N, T, D, F, H, eps, dtype, out, stream);
+}
+
+int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g, const void* lnf_b,
+                int final_ln, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H, double eps, int dtype,
+                void* out, void* stream) {
+    if (!layers || L < 1 || L > (1 << 20)) return VIT_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto layer_args = [&](int64_t l, const void* in, void* o) {
+        const vit_layer& ly = layers[l];
+        BlockArgs a{in, ly.w_q, ly.w_k, ly.w_v, ly.w_o, ly.w_mlp1, ly.w_mlp2, ly.ln1_g, ly.ln1_b, ly.ln2_g,
+                    ly.ln2_b, ly.b1, ly.b2, N, T, D, F, H, eps, dtype, o};
+        a.b_q = ly.b_q; a.b_k = ly.b_k; a.b_v = ly.b_v; a.b_o = ly.b_o;
+        return a;
+    };
+    // argument checks of every layer against the caller's x and out (as vit_block_ex),
+    // plus the projection biases and the final LayerNorm's gain and bias
+    for (int64_t l = 0; l < L; ++l) {
+        int rc = validate(layer_args(l, x, out));
+        if (rc != VIT_OK) return rc;
+        const size_t xb = (size_t)(N * T * D) * dt_size(dtype), db = (size_t)D * dt_size(dtype);
+        const vit_layer& ly = layers[l];
+        const void* extra[] = {ly.b_q, ly.b_k, ly.b_v, ly.b_o};
+        for (const void* p : extra)
+            if (overlaps(out, xb, p, db)) return VIT_ERR_ARG;
+        if (overlaps(out, xb, lnf_g, db) || overlaps(out, xb, lnf_b, db)) return VIT_ERR_ARG;
+    }
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    const DeviceInfo& dev = st->info;
+    const int64_t M = N * T;
+    const int sdt = dtype == DT_BF16 ? DT_F32 : dtype;   // residual stream between blocks
+    const size_t stream_bytes = round_up((size_t)(M * D) * dt_size(sdt), 256);
+    const size_t bias_bytes = round_up((size_t)(3 * D) * dt_size(dtype), 256);
+    // scratch: the largest block workspace | two residual-stream buffers | qkv bias
+    std::vector<Workspace> wl((size_t)L);
+    size_t block_bytes = 0;
+    void* const probe = reinterpret_cast<void*>(256);   // pool memory is 256-byte aligned
+    for (int64_t l = 0; l < L; ++l) {
+        BlockArgs a = layer_args(l, l == 0 ? x : probe, probe);
+        wl[(size_t)l] = workspace_layout(a, false);
+        block_bytes = wl[(size_t)l].total > block_bytes ? wl[(size_t)l].total : block_bytes;
+    }
+    const size_t total = block_bytes + 2 * stream_bytes + bias_bytes;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    void* r[2] = {base + block_bytes, base + block_bytes + stream_bytes};
+    void* bias_scratch = base + block_bytes + 2 * stream_bytes;
+    const void* cur = x;
+    for (int64_t l = 0; l < L && e == cudaSuccess; ++l) {
+        const bool last = l == L - 1;
+        void* dst = (last && !final_ln) ? out : r[l & 1];
+        BlockArgs a = layer_args(l, cur, dst);
+        a.x_dt = l == 0 ? dtype : sdt;
+        a.out_dt = (last && !final_ln) ? dtype : sdt;
+        a.bias_scratch = bias_scratch;
+        e = launch_block_steps(a, dev, s, wl[(size_t)l], ws);
+        cur = dst;
+    }
+    if (e == cudaSuccess && final_ln)
+        e = run(K_FINAL_LN, s, [&] {
+            return launch_layernorm(cur, sdt, out, dtype, lnf_g, lnf_b, dtype, M, D, eps, s);
+        });
+    cudaError_t fe = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = fe;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+        uint32_t w = 0;
+        if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
+        if (w) return VIT_ERR_TIMEOUT;
+    }
+    return VIT_OK;
 }
 
 int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_host,

@@ -103,3 +103,30 @@ def make_config_inputs(name, seed=0, affine=False, dtype=torch.float32, device="
     c = CONFIGS[name]
     return make_inputs(N if N is not None else c["N"], c["T"], c["D"], c["F"], seed=seed,
                        affine=affine, dtype=dtype, device=device)
+
+
+def make_encoder_inputs(N, T, D, F, L, seed=0, affine=True, biases=True, dtype=torch.float32,
+                        device="cpu"):
+    """Inputs of an L-block stack: x, a list of per-layer dicts (the block's weights and
+    affine terms, drawn as make_inputs does with seed + 1000 l, plus, with biases, the Q, K,
+    V and output-projection biases ~ N(0, 0.02^2)) and the final LayerNorm's gain and bias
+    (1 + N(0, 0.02^2), N(0, 0.02^2)). Everything is drawn in fp32 and cast to dtype."""
+    x = make_inputs(N, T, D, F, seed=seed, dtype=dtype, device=device).x
+    layers = []
+    for l in range(L):
+        b = make_inputs(1, 1, D, F, seed=seed + 1000 * (l + 1), affine=affine)
+        lay = {n: getattr(b, n) for n in WEIGHT_NAMES}
+        if affine:
+            lay.update(b.affine())
+        if biases:
+            g = torch.Generator(device="cpu")
+            g.manual_seed(int(seed + 1000 * (l + 1) + 7))
+            for n in ("b_q", "b_k", "b_v", "b_o"):
+                lay[n] = torch.randn(D, generator=g, dtype=torch.float32) * 0.02
+        layers.append({k: (v.to(device=device, dtype=dtype).contiguous() if v is not None else None)
+                       for k, v in lay.items()})
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed + 7))
+    lnf_g = (1.0 + torch.randn(D, generator=g) * 0.02).to(device=device, dtype=dtype)
+    lnf_b = (torch.randn(D, generator=g) * 0.02).to(device=device, dtype=dtype)
+    return x, layers, lnf_g, lnf_b
