@@ -31,10 +31,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from vision_transformer_encoder_gb300 import api  # noqa: E402
-from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs  # noqa: E402
+from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs, make_encoder_inputs  # noqa: E402
 
 METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf16, 1 GPU"
 UNIT = "tokens/s"
+ENCODER_METRIC = "ViT encoder (%d blocks + final LN) tokens/s at ViT-B/16 width bf16, 1 GPU"
 L2_FLUSH_BYTES = 512 << 20  # > 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -260,6 +261,9 @@ def main():
                     help="steps of the host-buffer end-to-end measurement (0: skip it)")
     ap.add_argument("--n-seq", type=int, default=None,
                     help="override the number of sequences N (profiling of a smaller case)")
+    ap.add_argument("--encoder-layers", type=int, default=0,
+                    help="time vit_encoder: this many blocks with Q/K/V/O biases, LN affine "
+                         "terms and the final LayerNorm, instead of one block")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -278,9 +282,17 @@ def main():
     out = torch.empty_like(d.x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    L = args.encoder_layers
 
-    def step():
-        api.vit_block(d.x, *d.weights(), H, eps, out=out, stream=stream)
+    if L > 0:
+        ex, elayers, elnf_g, elnf_b = make_encoder_inputs(c["N"], c["T"], c["D"], c["F"], L, seed=rank,
+                                                          dtype=torch.bfloat16, device=dev)
+
+        def step():
+            api.vit_encoder(ex, elayers, H, eps, lnf_g=elnf_g, lnf_b=elnf_b, out=out, stream=stream)
+    else:
+        def step():
+            api.vit_block(d.x, *d.weights(), H, eps, out=out, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -321,7 +333,7 @@ def main():
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and L == 0:
         pinned = [t.pin_memory() for t in [inp.x] + inp.weights()]
         hout = torch.empty_like(pinned[0]).pin_memory()
         api.vit_block_host(*pinned, H, eps, out=hout, device=dev.index)
@@ -363,15 +375,18 @@ def main():
                  "peak_source": "%s (%s)" % (peak_src, "bf16 burst" if bound == "tensor" else "copy"),
                  "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
                                        if bound == "tensor" else None)})
-    step_tflops = flops_per_step(c) / (ms_per_step / 1e3) / 1e12
+    step_tflops = max(L, 1) * flops_per_step(c) / (ms_per_step / 1e3) / 1e12
     kernels = {k: {"avg_us": 1e3 * v[0] / v[1] if v[1] else None, "launches": v[1],
                    "share": v[0] / sum(x[0] for x in per_kernel.values())}
                for k, v in per_kernel.items()}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "metric": METRIC if L == 0 else ENCODER_METRIC % L, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(name, c),
+        "config": {"workload": workload_name(name, c) if L == 0 else
+                   "%d-block encoder (Q/K/V/O and MLP biases, LN gains, final LayerNorm) of %s"
+                   % (L, workload_name(name, c)),
                    "tokens_per_step_per_gpu": tokens,
                    "inputs": "seeded synthetic: x ~ N(0,1), weights ~ N(0, 1/fan_in), bf16",
                    "l2": "512 MiB written between timed steps (flush); per-step working set "
@@ -385,7 +400,7 @@ def main():
         "e2e": e2e,
         "clocks": sampler.summary(t0, t1),
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and L == 0:
         line["cpu_baseline"] = cpu_baseline(name, c)
     if args.n_seq:
         line["config"]["note"] = "N overridden on the command line (not the headline workload)"
