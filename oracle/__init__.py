@@ -73,6 +73,9 @@ def open_library(path: str):
     lib.oracle_vit_encoder.argtypes = [_dptr, ctypes.POINTER(_dptr), _i64, _dptr, _dptr, ctypes.c_int,
                                        _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _dptr, ctypes.c_int]
     lib.oracle_vit_encoder.restype = ctypes.c_int
+    lib.oracle_patch_embed.argtypes = [_dptr, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dptr, _dptr,
+                                       _dptr, _dptr, _i64, _dptr]
+    lib.oracle_patch_embed.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = ctypes.c_int
     return lib
@@ -224,4 +227,21 @@ def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, nthrea
                                              N, T, D, int(F), int(H), float(eps), _p(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_vit_encoder failed with status %d" % rc)
+    return out
+
+
+def patch_embed(images, P, w, b=None, cls=None, pos=None, order=0, lib=None):
+    """Tokens (N, T, D) in float64 from images (N, C, Hi, Wi): patches of P x P flattened in
+    `order` (0: channel, row, column; 1: row, column, channel), @ w (+ b), the cls row
+    prepended when given, pos (T, D) added when given."""
+    im = _f64(images)
+    N, C, Hi, Wi = im.shape
+    w64, b64, c64, p64 = _f64(w), _f64(b), _f64(cls), _f64(pos)
+    D = w64.shape[1]
+    T = (Hi // P) * (Wi // P) + (1 if cls is not None else 0)
+    out = np.empty((N, T, D), dtype=np.float64)
+    rc = (lib or _load()).oracle_patch_embed(_p(im), N, C, Hi, Wi, int(P), int(order), _p(w64), _p(b64),
+                                             _p(c64), _p(p64), D, _p(out))
+    if rc != 0:
+        raise ValueError("oracle_patch_embed failed with status %d" % rc)
     return out

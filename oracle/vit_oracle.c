@@ -303,6 +303,60 @@ int oracle_vit_encoder(const double* x, const double* const* layers, int64_t L,
     return rc;
 }
 
+/* Patch embedding front end. Images (N, C, Hi, Wi), non-overlapping P x P patches taken
+ * in row-major order over the (Hi/P, Wi/P) grid, each flattened to C P P values and
+ * projected: tokens = patches @ w (+ b), w of shape (C P P, D); then, with cls non-NULL,
+ * the cls row is prepended; with pos non-NULL, pos (T, D) is added to every row
+ * (T = patches + (cls ? 1 : 0)). Flatten order inside a patch:
+ *   order 0: (c, p1, p2) -- channel by channel, each row by row: lecture transcript
+ *            (nipunbatra.github.io), Pages 98 and 101 (unfold; the same as the stride-P
+ *            convolution of Pages 99-100);
+ *   order 1: (p1, p2, c) -- "E2E: Tiny Vision Transformer" (mlgrind), "Patch order".
+ * CLS prepend and position add: lecture transcript, Page 105; "E2E: Tiny Vision
+ * Transformer", forward diagram. */
+int oracle_patch_embed(const double* images, int64_t N, int64_t C, int64_t Hi, int64_t Wi,
+                       int64_t P, int order, const double* w, const double* b,
+                       const double* cls, const double* pos, int64_t D, double* out)
+{
+    if (N <= 0 || C <= 0 || P <= 0 || D <= 0 || Hi % P != 0 || Wi % P != 0 || (order != 0 && order != 1))
+        return -1;
+    const int64_t gh = Hi / P, gw = Wi / P, NP = gh * gw, K = C * P * P;
+    const int64_t T = NP + (cls ? 1 : 0), off = cls ? 1 : 0;
+    double* patch = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!patch) return -2;
+    for (int64_t n = 0; n < N; ++n) {
+        double* o = out + (size_t)n * T * D;
+        if (cls)
+            for (int64_t d = 0; d < D; ++d) o[d] = cls[d];
+        for (int64_t py = 0; py < gh; ++py)
+            for (int64_t px = 0; px < gw; ++px) {
+                /* flatten this patch */
+                for (int64_t c = 0; c < C; ++c)
+                    for (int64_t i = 0; i < P; ++i)
+                        for (int64_t j = 0; j < P; ++j) {
+                            const double v = images[(((size_t)n * C + c) * Hi + py * P + i) * Wi + px * P + j];
+                            const int64_t k = order == 0 ? (c * P + i) * P + j : (i * P + j) * C + c;
+                            patch[k] = v;
+                        }
+                /* project: row = patch @ w (+ b) */
+                double* row = o + (size_t)(off + py * gw + px) * D;
+                for (int64_t d = 0; d < D; ++d) row[d] = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    const double a = patch[k];
+                    const double* wk = w + (size_t)k * D;
+                    for (int64_t d = 0; d < D; ++d) row[d] += a * wk[d];
+                }
+                if (b)
+                    for (int64_t d = 0; d < D; ++d) row[d] += b[d];
+            }
+        if (pos)
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t d = 0; d < D; ++d) o[(size_t)t * D + d] += pos[(size_t)t * D + d];
+    }
+    free(patch);
+    return 0;
+}
+
 /* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
 int oracle_max_threads(void)
 {

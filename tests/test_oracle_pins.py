@@ -437,6 +437,65 @@ def test_encoder_without_updates_is_layernorm_of_x():
     np.testing.assert_array_equal(oracle.vit_encoder(x, layers, 3, 1e-6), oracle.layernorm(x, 1e-6))
 
 
+# --------------------------------------------------------------- patch embedding front end
+
+def _rand_images(N, C, H, W, P, D, seed):
+    rng = np.random.default_rng(seed)
+    T = (H // P) * (W // P) + 1
+    return (rng.standard_normal((N, C, H, W)), rng.standard_normal((C * P * P, D)) / np.sqrt(C * P * P),
+            rng.standard_normal(D), rng.standard_normal(D), rng.standard_normal((T, D)))
+
+
+def _torch_patch_rows(im, P, order):
+    t = torch.from_numpy(im)
+    if order == 0:   # unfold: each patch channel by channel, each channel row by row
+        return Fn.unfold(t, P, stride=P).transpose(1, 2)
+    N, C, H, W = t.shape   # (p1, p2, c): reshape and permute
+    t = t.reshape(N, C, H // P, P, W // P, P).permute(0, 2, 4, 3, 5, 1)
+    return t.reshape(N, (H // P) * (W // P), P * P * C)
+
+
+@pytest.mark.parametrize("order", [0, 1])
+@pytest.mark.parametrize("shape", [(2, 3, 32, 48, 16, 20), (1, 1, 8, 8, 4, 16), (2, 3, 28, 14, 14, 12)])
+def test_patch_embed_matches_torch(order, shape):
+    N, C, H, W, P, D = shape
+    im, w, b, cls, pos = _rand_images(N, C, H, W, P, D, seed=sum(shape) + order)
+    rows = _torch_patch_rows(im, P, order) @ torch.from_numpy(w) + torch.from_numpy(b)
+    ref = torch.cat([torch.from_numpy(cls).expand(N, 1, D), rows], 1) + torch.from_numpy(pos)
+    got = oracle.patch_embed(im, P, w, b, cls=cls, pos=pos, order=order)
+    np.testing.assert_allclose(got, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_patch_embed_channel_order_is_the_stride_p_convolution():
+    # the lecture's second implementation: the projection weights reshaped into D filters
+    # of C x P x P applied by a stride-P convolution give the same rows
+    N, C, H, W, P, D = 2, 3, 32, 32, 16, 8
+    im, w, b, _, _ = _rand_images(N, C, H, W, P, D, seed=3)
+    conv = Fn.conv2d(torch.from_numpy(im), torch.from_numpy(w.T.reshape(D, C, P, P).copy()),
+                     torch.from_numpy(b), stride=P)
+    ref = conv.flatten(2).transpose(1, 2).numpy()
+    np.testing.assert_allclose(oracle.patch_embed(im, P, w, b, order=0), ref, rtol=0, atol=1e-12)
+
+
+def test_patch_embed_printed_flat_index():
+    g = _load("p5_patch_flat_index.json")
+    C, P, px = g["channels"], g["patch"], g["pixel"]
+    im = np.zeros((1, C, P, P))
+    im[0, px["channel"], px["row"], px["col"]] = 1.0
+    K = C * P * P
+    out = oracle.patch_embed(im, P, np.eye(K), order=0)   # identity projection: the flat patch
+    assert out.shape == (1, 1, K)
+    assert np.flatnonzero(out[0, 0]).tolist() == [g["flat_index"]]
+
+
+def test_patch_embed_cls_and_positions():
+    N, C, H, W, P, D = 2, 3, 16, 16, 8, 6
+    im, _, _, cls, pos = _rand_images(N, C, H, W, P, D, seed=4)
+    out = oracle.patch_embed(im, P, np.zeros((C * P * P, D)), np.zeros(D), cls=cls, pos=pos)
+    np.testing.assert_array_equal(out[:, 0], np.broadcast_to(cls + pos[0], (N, D)))
+    np.testing.assert_array_equal(out[:, 1:], np.broadcast_to(pos[1:], (N, pos.shape[0] - 1, D)))
+
+
 MUTANTS = {
     "eps_fixed_1e-5": ("sqrt(var + eps)", "sqrt(var + 1e-5)"),
     "sample_variance": ("var /= (double)D;", "var /= (double)(D - 1 > 0 ? D - 1 : 1);"),
@@ -468,6 +527,14 @@ MUTANTS = {
     "encoder_restarts_from_x": ("        cur = nxt;\n", "        cur = (l + 1 < L) ? x : nxt;\n"),
     "final_ln_without_affine": ("oracle_layernorm(cur, N * T, D, eps, lnf_g, lnf_b, out);",
                                 "oracle_layernorm(cur, N * T, D, eps, NULL, NULL, out);"),
+    "patch_orders_swapped": ("order == 0 ? (c * P + i) * P + j : (i * P + j) * C + c",
+                             "order == 1 ? (c * P + i) * P + j : (i * P + j) * C + c"),
+    "patch_rows_transposed": ("for (int64_t i = 0; i < P; ++i)\n                        for (int64_t j = 0; j < P; ++j) {\n                            const double v = images[(((size_t)n * C + c) * Hi + py * P + i) * Wi + px * P + j];",
+                              "for (int64_t i = 0; i < P; ++i)\n                        for (int64_t j = 0; j < P; ++j) {\n                            const double v = images[(((size_t)n * C + c) * Hi + py * P + j) * Wi + px * P + i];"),
+    "pos_skips_cls_row": ("for (int64_t t = 0; t < T; ++t)\n                for (int64_t d = 0; d < D; ++d) o[(size_t)t * D + d] += pos[(size_t)t * D + d];",
+                          "for (int64_t t = 1; t < T; ++t)\n                for (int64_t d = 0; d < D; ++d) o[(size_t)t * D + d] += pos[(size_t)t * D + d];"),
+    "drop_patch_bias": ("                if (b)\n                    for (int64_t d = 0; d < D; ++d) row[d] += b[d];",
+                        "                if (b && 0)\n                    for (int64_t d = 0; d < D; ++d) row[d] += b[d];"),
 }
 
 
@@ -492,7 +559,17 @@ def _pins_pass(lib):
     layers = _rand_layers(3, 12, 20, seed=90)
     g, b = 1 + 0.1 * rng.standard_normal(12), 0.1 * rng.standard_normal(12)
     got = oracle.vit_encoder(x, layers, 3, 1e-5, lnf_g=g, lnf_b=b, lib=lib)
-    return bool(np.allclose(got, _torch_encoder(x, layers, 3, 1e-5, g, b), rtol=0, atol=1e-11))
+    if not np.allclose(got, _torch_encoder(x, layers, 3, 1e-5, g, b), rtol=0, atol=1e-11):
+        return False
+    # patch embedding, both orders, with the CLS row and positions
+    im, w, bb, cls, pos = _rand_images(2, 3, 16, 24, 8, 10, seed=24)
+    for order in (0, 1):
+        rows = _torch_patch_rows(im, 8, order) @ torch.from_numpy(w) + torch.from_numpy(bb)
+        ref = torch.cat([torch.from_numpy(cls).expand(2, 1, 10), rows], 1) + torch.from_numpy(pos)
+        got = oracle.patch_embed(im, 8, w, bb, cls=cls, pos=pos, order=order, lib=lib)
+        if not np.allclose(got, ref.numpy(), rtol=0, atol=1e-12):
+            return False
+    return True
 
 
 def test_pins_pass_on_unmodified_source(tmp_path):
