@@ -35,6 +35,7 @@ from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs,
 
 METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf16, 1 GPU"
 UNIT = "tokens/s"
+PATCH_METRIC = "ViT patch-embedding front end tokens/s at ViT-B/16 width bf16, 1 GPU"
 ENCODER_METRIC = "ViT encoder (%d blocks + final LN) tokens/s at ViT-B/16 width bf16, 1 GPU"
 L2_FLUSH_BYTES = 512 << 20  # > 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -69,6 +70,12 @@ def kernel_work(c):
         # statistics of x; the fold's column terms are computed once per call
         "ln1_row_stats": ("hbm", M * D * 2 + M * 8, "bytes"),
         "ln_fold_prep": ("hbm", (3 * D * D + D * F) * 2 + (3 * D + F) * 8, "bytes"),
+        # stacks: the final LayerNorm reads the fp32 stream and writes bf16
+        "final_ln": ("hbm", M * D * (4 + 2), "bytes"),
+        # patch-embedding front end (images 3 x 224 x 224, P 16: T - 1 patches of 768)
+        "patchify": ("hbm", N * (T - 1) * 768 * 2 * 2, "bytes"),
+        "patch_gemm": ("tensor", 2 * N * (T - 1) * 768 * D, "flops"),
+        "patch_assemble": ("hbm", N * (T - 1) * D * 4 + M * D * 2, "bytes"),
     }
 
 
@@ -261,6 +268,9 @@ def main():
                     help="steps of the host-buffer end-to-end measurement (0: skip it)")
     ap.add_argument("--n-seq", type=int, default=None,
                     help="override the number of sequences N (profiling of a smaller case)")
+    ap.add_argument("--patch-embed", action="store_true",
+                    help="time vit_patch_embed: N images of 3 x 224 x 224, 16 x 16 patches, CLS "
+                         "row and positions, into (N, 197, D) tokens")
     ap.add_argument("--encoder-layers", type=int, default=0,
                     help="time vit_encoder: this many blocks with Q/K/V/O biases, LN affine "
                          "terms and the final LayerNorm, instead of one block")
@@ -284,7 +294,18 @@ def main():
     stream = torch.cuda.current_stream()
     L = args.encoder_layers
 
-    if L > 0:
+    if args.patch_embed:
+        g = torch.Generator().manual_seed(rank)
+        K = 3 * 16 * 16
+        pim = torch.randn(c["N"], 3, 224, 224, generator=g).to(torch.bfloat16).to(dev)
+        pw = (torch.randn(K, c["D"], generator=g) / K ** 0.5).to(torch.bfloat16).to(dev)
+        pb = (torch.randn(c["D"], generator=g) * 0.02).to(torch.bfloat16).to(dev)
+        pcls = (torch.randn(c["D"], generator=g) * 0.02).to(torch.bfloat16).to(dev)
+        ppos = (torch.randn(197, c["D"], generator=g) * 0.02).to(torch.bfloat16).to(dev)
+
+        def step():
+            api.vit_patch_embed(pim, 16, pw, b=pb, cls=pcls, pos=ppos, out=out, stream=stream)
+    elif L > 0:
         ex, elayers, elnf_g, elnf_b = make_encoder_inputs(c["N"], c["T"], c["D"], c["F"], L, seed=rank,
                                                           dtype=torch.bfloat16, device=dev)
 
@@ -333,7 +354,7 @@ def main():
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
-    if args.e2e_steps > 0 and L == 0:
+    if args.e2e_steps > 0 and L == 0 and not args.patch_embed:
         pinned = [t.pin_memory() for t in [inp.x] + inp.weights()]
         hout = torch.empty_like(pinned[0]).pin_memory()
         api.vit_block_host(*pinned, H, eps, out=hout, device=dev.index)
@@ -375,16 +396,20 @@ def main():
                  "peak_source": "%s (%s)" % (peak_src, "bf16 burst" if bound == "tensor" else "copy"),
                  "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
                                        if bound == "tensor" else None)})
-    step_tflops = max(L, 1) * flops_per_step(c) / (ms_per_step / 1e3) / 1e12
+    step_flops = (2 * c["N"] * 196 * 768 * c["D"]) if args.patch_embed else max(L, 1) * flops_per_step(c)
+    step_tflops = step_flops / (ms_per_step / 1e3) / 1e12
     kernels = {k: {"avg_us": 1e3 * v[0] / v[1] if v[1] else None, "launches": v[1],
                    "share": v[0] / sum(x[0] for x in per_kernel.values())}
                for k, v in per_kernel.items()}
     line = {
-        "metric": METRIC if L == 0 else ENCODER_METRIC % L, "value": value, "unit": UNIT,
+        "metric": (PATCH_METRIC if args.patch_embed else METRIC if L == 0 else ENCODER_METRIC % L),
+        "value": value, "unit": UNIT,
         "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_name(name, c) if L == 0 else
+        "config": {"workload": ("patch embedding of %d images 3 x 224 x 224 (16 x 16 patches, CLS row, "
+                                "positions) into (%d, 197, %d) tokens" % (c["N"], c["N"], c["D"]))
+                   if args.patch_embed else workload_name(name, c) if L == 0 else
                    "%d-block encoder (Q/K/V/O and MLP biases, LN gains, final LayerNorm) of %s"
                    % (L, workload_name(name, c)),
                    "tokens_per_step_per_gpu": tokens,
@@ -400,7 +425,7 @@ def main():
         "e2e": e2e,
         "clocks": sampler.summary(t0, t1),
     }
-    if world == 1 and not args.no_cpu_baseline and L == 0:
+    if world == 1 and not args.no_cpu_baseline and L == 0 and not args.patch_embed:
         line["cpu_baseline"] = cpu_baseline(name, c)
     if args.n_seq:
         line["config"]["note"] = "N overridden on the command line (not the headline workload)"

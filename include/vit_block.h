@@ -181,6 +181,31 @@ int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* l
                 int64_t H, double eps, int dtype, void* out, void* stream);
 
 /*
+ * vit_patch_embed -- the patch-embedding front end: images to tokens.
+ *
+ * Definition: lecture transcript (nipunbatra.github.io), Pages 96-105 -- non-overlapping
+ * P x P patches over the image grid in row-major order, each flattened and projected by
+ * one shared linear layer with bias (Pages 96-98, 101), then the CLS row prepended and the
+ * positions added (Page 105); "E2E: Tiny Vision Transformer" (mlgrind), forward diagram
+ * and patch order.
+ *
+ *   images   (N, C, Hi, Wi), Hi and Wi multiples of P
+ *   order    flatten order inside a patch: 0 = (channel, row, column), the order of
+ *            Pages 98 and 101 and of the stride-P convolution; 1 = (row, column, channel),
+ *            the E2E page's order
+ *   w        (C P P, D) projection, used as  patch_row @ w;  b (D) nullable bias
+ *   cls      (D) nullable: prepended as token 0 when given
+ *   pos      ((Hi/P)(Wi/P) + [cls], D) nullable: added to every token when given
+ *   tokens   (N, T, D) output, T = (Hi/P)(Wi/P) + (cls ? 1 : 0); must not overlap an input
+ * dtype as vit_block (bf16: the projection accumulates in fp32 and the position add
+ * happens in fp32 before the single rounding). Errors as vit_block; VIT_ERR_ARG also for
+ * Hi or Wi not a multiple of P or an unknown order.
+ */
+int vit_patch_embed(const void* images, int64_t N, int64_t C, int64_t Hi, int64_t Wi, int64_t P,
+                    int order, const void* w, const void* b, const void* cls, const void* pos,
+                    int64_t D, int dtype, void* tokens, void* stream);
+
+/*
  * vit_layernorm -- out[r, :] = LN(x[r, :]) [* gamma + beta] for r < rows.
  * "ViT Encoder Block" (crackedaicode), "Normalize before each stage".
  *   x     (rows, D) of in_dtype; gamma, beta (D) of out_dtype or NULL

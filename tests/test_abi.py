@@ -89,7 +89,7 @@ def test_step_entry_points_validate(lib):
 
 
 def test_timing_interface_without_gpu(lib):
-    assert lib.vit_timing_kernels() == 11
+    assert lib.vit_timing_kernels() == 14
     ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
     assert lib.vit_timing_read(0, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm)) == 0
     assert nm.value == b"ln1"
@@ -109,3 +109,19 @@ def test_encoder_argument_checks(lib):
     lay2 = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 6 + [_fake(10).value + 8] + [None] * 3)
     arr2 = (api.VitLayer * 1)(lay2)
     assert lib.vit_encoder(_fake(0), arr2, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+
+
+def test_patch_embed_argument_checks(lib):
+    args = dict(N=2, C=3, Hi=32, Wi=32, P=16, order=0, D=8)
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.vit_patch_embed(_fake(0), a["N"], a["C"], a["Hi"], a["Wi"], a["P"], a["order"], _fake(1),
+                                   None, None, None, a["D"], kw.get("dtype", 1), _fake(10), None)
+    assert call(Hi=30) == -1            # not a multiple of P
+    assert call(order=2) == -1
+    assert call(P=0) == -1
+    assert call(dtype=5) == -2
+    assert lib.vit_patch_embed(None, 2, 3, 32, 32, 16, 0, _fake(1), None, None, None, 8, 1, _fake(10), None) == -1
+    # tokens overlapping the images
+    assert lib.vit_patch_embed(_fake(0), 2, 3, 32, 32, 16, 0, _fake(1), None, None, None, 8, 1,
+                               ctypes.c_void_p(_fake(0).value + 64), None) == -1

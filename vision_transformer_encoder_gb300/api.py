@@ -39,6 +39,7 @@ SIGNATURES = {
     "vit_block_noalloc": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_encoder": (_int, [_vp, ctypes.POINTER(VitLayer), _i64, _vp, _vp, _int] + [_i64] * 5
                     + [_dbl, _int, _vp, _vp]),
+    "vit_patch_embed": (_int, [_vp] + [_i64] * 5 + [_int] + [_vp] * 4 + [_i64, _int, _vp, _vp]),
     "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
     "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
     "vit_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _vp, _vp]),
@@ -186,6 +187,27 @@ def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, out=No
         rc = lib.vit_encoder(_ptr(x), arr, len(layers), _ptr(lnf_g), _ptr(lnf_b), 1 if final_ln else 0,
                              N, T, D, F, int(H), float(eps), _dtype_code(dt), _ptr(out), _stream(stream))
     _check(rc, "vit_encoder")
+    return out
+
+
+def vit_patch_embed(images, P, w, b=None, cls=None, pos=None, order=0, out=None, stream=None):
+    """tokens (N, T, D) from images (N, C, Hi, Wi): P x P patches flattened in `order`
+    (0: channel, row, column; 1: row, column, channel) @ w (+ b), the cls row prepended and
+    pos (T, D) added when given."""
+    lib = load_library()
+    dt = images.dtype
+    for name, t in (("images", images), ("w", w), ("b", b), ("cls", cls), ("pos", pos)):
+        _dev(t, name, dt)
+    N, C, Hi, Wi = images.shape
+    D = w.shape[1]
+    T = (Hi // P) * (Wi // P) + (1 if cls is not None else 0)
+    if out is None:
+        out = torch.empty((N, T, D), dtype=dt, device=images.device)
+    _dev(out, "out", dt)
+    with torch.cuda.device(images.device):
+        rc = lib.vit_patch_embed(_ptr(images), N, C, Hi, Wi, int(P), int(order), _ptr(w), _ptr(b), _ptr(cls),
+                                 _ptr(pos), D, _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_patch_embed")
     return out
 
 

@@ -141,6 +141,15 @@ cudaError_t launch_split_wt(const float* w, int64_t K, int64_t N, int64_t ldw, i
                             cudaStream_t s);
 cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cudaStream_t s);
 
+// ---- Patch embedding (patch_embed.cu) ----------------------------------------
+// images (N, C, Hi, Wi) -> A (N * NP, C P P) in the same dtype, flatten order 0 (c, p1, p2)
+// or 1 (p1, p2, c); then tokens (N, NP + [cls], D) = [cls;] E (+ pos), E = A @ w (+ b) in
+// e_dt (fp32 for bf16 tokens).
+cudaError_t launch_patchify(const void* images, int dt, int64_t N, int64_t C, int64_t Hi, int64_t Wi, int64_t P,
+                            int order, void* A, cudaStream_t s);
+cudaError_t launch_patch_assemble(const void* E, int e_dt, const void* cls, const void* pos, int dt, int64_t N,
+                                  int64_t NP, int64_t D, void* out, cudaStream_t s);
+
 // fp32 qkv -> fp32 o on the CUDA cores (head widths 32, 48, 64, 80, 96, 128).
 bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o);
 cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,

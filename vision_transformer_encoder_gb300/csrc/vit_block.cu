@@ -50,11 +50,12 @@ std::atomic<int64_t> g_launches{0};
 
 // ---- per-kernel timing -------------------------------------------------------
 enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_TF32_SPLIT, K_FINAL_LN,
-            K_COUNT };
+            K_PATCHIFY, K_PATCH_GEMM, K_PATCH_ASSEMBLE, K_COUNT };
 const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
                                          "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
                                          "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep",
-                                         "tf32_weight_split", "final_ln"};
+                                         "tf32_weight_split", "final_ln", "patchify", "patch_gemm",
+                                         "patch_assemble"};
 struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -738,6 +739,89 @@ int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* l
         uint32_t w = 0;
         if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
         if (w) return VIT_ERR_TIMEOUT;
+    }
+    return VIT_OK;
+}
+
+int vit_patch_embed(const void* images, int64_t N, int64_t C, int64_t Hi, int64_t Wi, int64_t P, int order,
+                    const void* w, const void* b, const void* cls, const void* pos, int64_t D, int dtype,
+                    void* tokens, void* stream) {
+    if (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F64) return VIT_ERR_DTYPE;
+    if (!images || !w || !tokens) return VIT_ERR_ARG;
+    if (N <= 0 || C <= 0 || Hi <= 0 || Wi <= 0 || P <= 0 || D <= 0 || Hi % P != 0 || Wi % P != 0 ||
+        (order != 0 && order != 1))
+        return VIT_ERR_ARG;
+    if (C * P * P > (1 << 22) || D > (1 << 20) || Hi > (1 << 20) || Wi > (1 << 20) || N > ((int64_t)1 << 31))
+        return VIT_ERR_ARG;
+    const int64_t NP = (Hi / P) * (Wi / P), K = C * P * P, T = NP + (cls ? 1 : 0), M = N * NP;
+    const size_t es = dt_size(dtype);
+    const size_t tb = (size_t)(N * T * D) * es;
+    const void* in[] = {images, w, b, cls, pos};
+    const size_t nb[] = {(size_t)(N * C * Hi * Wi) * es, (size_t)(K * D) * es, (size_t)D * es, (size_t)D * es,
+                         (size_t)(T * D) * es};
+    for (int i = 0; i < 5; ++i)
+        if (overlaps(tokens, tb, in[i], nb[i])) return VIT_ERR_ARG;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    const DeviceInfo& dev = st->info;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int e_dt = dtype == DT_BF16 ? DT_F32 : dtype;
+    const bool tf32 = dtype == DT_F32 && tf32_requested() && tf32x3_supported(M, D, K, K, reinterpret_cast<void*>(256)) &&
+                      al16(w) && (!b || al16(b));
+    // scratch: A (M x K) | E (M x D) | for the fp32 tensor-core product: A_lo | W^T | W^T_lo
+    const size_t sa = round_up((size_t)(M * K) * es, 256), se = round_up((size_t)(M * D) * dt_size(e_dt), 256);
+    const size_t slo = tf32 ? round_up((size_t)(M * K) * 4, 256) : 0, swt = tf32 ? round_up((size_t)(D * K) * 4, 256) : 0;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, sa + se + slo + 2 * swt, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    void* A = base;
+    void* E = base + sa;
+    e = run(K_PATCHIFY, s, [&] { return launch_patchify(images, dtype, N, C, Hi, Wi, P, order, A, s); });
+    if (e == cudaSuccess)
+        e = run(K_PATCH_GEMM, s, [&] {
+            if (dtype == DT_BF16) {
+                TcGemmDesc g;
+                std::memset(&g, 0, sizeof(g));
+                g.a = A; g.lda = K; g.w[0] = w; g.n_w = 1; g.n_per_w = D;
+                g.M = M; g.N = D; g.K = K;
+                g.epi = TC_EPI_STORE; g.bias = b;
+                g.out = E; g.ldo = D; g.out_f32 = true;
+                if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            }
+            if (tf32) {
+                float* lo = reinterpret_cast<float*>(base + sa + se);
+                float* wt = reinterpret_cast<float*>(base + sa + se + slo);
+                float* wt_lo = reinterpret_cast<float*>(base + sa + se + slo + swt);
+                cudaError_t r = launch_split_wt(static_cast<const float*>(w), K, D, D, 0, wt, wt_lo, s);
+                if (r == cudaSuccess) r = launch_split_lo(static_cast<const float*>(A), M, K, K, lo, s);
+                if (r != cudaSuccess) return r;
+                Tf32GemmDesc g{static_cast<const float*>(A), K, lo, wt, wt_lo, M, D, K, TC_EPI_STORE,
+                               static_cast<const float*>(b), nullptr, 0, static_cast<float*>(E), D};
+                return launch_gemm_tf32x3(g, dev, s);
+            }
+            SimtGemmDesc sd{A, dtype, K, w, dtype, D, b, dtype, nullptr, 0, 0, E, e_dt, D, M, D, K, TC_EPI_STORE};
+            return launch_gemm_simt(sd, s);
+        });
+    if (e == cudaSuccess)
+        e = run(K_PATCH_ASSEMBLE, s, [&] {
+            return launch_patch_assemble(E, e_dt, cls, pos, dtype, N, NP, D, tokens, s);
+        });
+    cudaError_t fe = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = fe;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+        uint32_t word = 0;
+        if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return VIT_ERR_CUDA;
+        if (word) return VIT_ERR_TIMEOUT;
     }
     return VIT_OK;
 }
