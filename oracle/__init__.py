@@ -73,6 +73,10 @@ def open_library(path: str):
     lib.oracle_vit_encoder.argtypes = [_dptr, ctypes.POINTER(_dptr), _i64, _dptr, _dptr, ctypes.c_int,
                                        _i64, _i64, _i64, _i64, _i64, ctypes.c_double, _dptr, ctypes.c_int]
     lib.oracle_vit_encoder.restype = ctypes.c_int
+    lib.oracle_vit_block_cls.argtypes = [_dptr] * 17 + [_i64] * 5 + [ctypes.c_double, _dptr, ctypes.c_int]
+    lib.oracle_vit_block_cls.restype = ctypes.c_int
+    lib.oracle_vit_encoder_cls.argtypes = lib.oracle_vit_encoder.argtypes
+    lib.oracle_vit_encoder_cls.restype = ctypes.c_int
     lib.oracle_patch_embed.argtypes = [_dptr, _i64, _i64, _i64, _i64, _i64, ctypes.c_int, _dptr, _dptr,
                                        _dptr, _dptr, _i64, _dptr]
     lib.oracle_patch_embed.restype = ctypes.c_int
@@ -204,9 +208,32 @@ LAYER_KEYS = ("w_q", "w_k", "w_v", "w_o", "w_mlp1", "w_mlp2", "ln1_g", "ln1_b", 
               "ln2_b", "b1", "b2", "b_q", "b_k", "b_v", "b_o")
 
 
-def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, nthreads=0, lib=None):
+def vit_block_cls(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln1_b=None,
+                  ln2_g=None, ln2_b=None, b1=None, b2=None, b_q=None, b_k=None, b_v=None,
+                  b_o=None, nthreads=0, lib=None):
+    """The CLS-only readout of one block: row 0 of each sequence's block output, computed
+    from the one CLS query against all T keys and values. Returns (N, D) float64."""
+    arrs = [_f64(a) for a in (x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2)]
+    opt = [_f64(a) for a in (ln1_g, ln1_b, ln2_g, ln2_b, b1, b2, b_q, b_k, b_v, b_o)]
+    x64 = arrs[0]
+    if x64.ndim == 2:
+        x64 = x64[None]
+        arrs[0] = x64
+    N, T, D = x64.shape
+    F = arrs[5].shape[1]
+    out = np.empty((N, D))
+    rc = (lib or _load()).oracle_vit_block_cls(*[_p(a) for a in arrs], *[_p(a) for a in opt],
+                                               N, T, D, F, int(H), float(eps), _p(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_vit_block_cls failed with status %d" % rc)
+    return out
+
+
+def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, nthreads=0, lib=None,
+                cls_only=False):
     """A stack of blocks (layers: a list of dicts keyed by LAYER_KEYS; the six weights
-    required, the rest optional) and, with final_ln, the final LayerNorm. Float64."""
+    required, the rest optional) and, with final_ln, the final LayerNorm. Float64.
+    cls_only: the last block is the CLS-only readout and the result is (N, D)."""
     x64 = _f64(x)
     if x64.ndim == 2:
         x64 = x64[None]
@@ -222,9 +249,11 @@ def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, nthrea
             ptrs[16 * l + j] = _p(a) if a is not None else _dptr()
         F = _f64(lay["w_mlp1"]).shape[1]
     g, b = _f64(lnf_g), _f64(lnf_b)
-    out = np.empty_like(x64)
-    rc = (lib or _load()).oracle_vit_encoder(_p(x64), ptrs, L, _p(g), _p(b), 1 if final_ln else 0,
-                                             N, T, D, int(F), int(H), float(eps), _p(out), int(nthreads))
+    lib = lib or _load()
+    out = np.empty((N, D)) if cls_only else np.empty_like(x64)
+    fn = lib.oracle_vit_encoder_cls if cls_only else lib.oracle_vit_encoder
+    rc = fn(_p(x64), ptrs, L, _p(g), _p(b), 1 if final_ln else 0,
+            N, T, D, int(F), int(H), float(eps), _p(out), int(nthreads))
     if rc != 0:
         raise ValueError("oracle_vit_encoder failed with status %d" % rc)
     return out

@@ -303,6 +303,120 @@ int oracle_vit_encoder(const double* x, const double* const* layers, int64_t L,
     return rc;
 }
 
+/* CLS-only readout of one block: lecture transcript (nipunbatra.github.io), Page 55 --
+ * when only the CLS token (row 0 of each sequence) is read after the last block, that
+ * block need only produce row 0: its single query is scored against the keys of all T
+ * rows and mixes the value rows of all T rows; the rest of the block then acts on that
+ * one row. Per sequence:
+ *   xn = LN1(x) for all T rows;  K = xn W_K (+ b_K), V = xn W_V (+ b_V) for all T rows;
+ *   q = xn[0] W_Q (+ b_Q);  per head h: s_u = q_h . K_h[u] / sqrt(D/H) for u < T,
+ *   p = softmax(s), o_h = sum_u p_u V_h[u];
+ *   y0 = x[0] + o W_O (+ b_O);  out[n] = y0 + GELU_tanh(LN2(y0) W1 (+ b1)) W2 (+ b2).
+ * out is (N, D). Returns as oracle_vit_block_full. */
+int oracle_vit_block_cls(const double* x, const double* w_q, const double* w_k,
+                         const double* w_v, const double* w_o, const double* w_mlp1,
+                         const double* w_mlp2, const double* ln1_g, const double* ln1_b,
+                         const double* ln2_g, const double* ln2_b, const double* b1,
+                         const double* b2, const double* b_q, const double* b_k,
+                         const double* b_v, const double* b_o, int64_t N, int64_t T,
+                         int64_t D, int64_t F, int64_t H, double eps, double* out,
+                         int nthreads)
+{
+    if (N <= 0 || T <= 0 || D <= 0 || F <= 0 || H <= 0 || D % H != 0) return -1;
+    int failed = 0;
+    const int64_t dh = D / H;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        const size_t TD = (size_t)(T * D);
+        double* buf = (double*)malloc(sizeof(double) * (3 * TD + 6 * (size_t)D + 2 * (size_t)F +
+                                                         2 * (size_t)T));
+        if (!buf) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+            continue;
+        }
+        double *xn = buf, *keys = xn + TD, *vals = keys + TD, *q0 = vals + TD, *o0 = q0 + D;
+        double *a0 = o0 + D, *y0 = a0 + D, *yn0 = y0 + D, *m0 = yn0 + D, *z0 = m0 + D, *g0 = z0 + F;
+        double *sc = g0 + F, *pw = sc + T;
+        const double* xs = x + (size_t)n * TD;
+
+        /* LN1 and the keys and values of every row */
+        oracle_layernorm(xs, T, D, eps, ln1_g, ln1_b, xn);
+        oracle_matmul(xn, w_k, b_k, T, D, D, keys);
+        oracle_matmul(xn, w_v, b_v, T, D, D, vals);
+        /* the query of the CLS row (row 0) alone */
+        oracle_matmul(xn, w_q, b_q, 1, D, D, q0);
+        /* per head: the T scores of that query, softmax, weighted sum of all T values */
+        for (int64_t h = 0; h < H; ++h) {
+            const int64_t first = h * dh;
+            for (int64_t u = 0; u < T; ++u) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < dh; ++c) dot += q0[first + c] * keys[u * D + first + c];
+                sc[u] = dot / sqrt((double)dh);
+            }
+            oracle_softmax_rows(sc, 1, T, pw);
+            for (int64_t c = 0; c < dh; ++c) {
+                double acc = 0.0;
+                for (int64_t u = 0; u < T; ++u) acc += pw[u] * vals[u * D + first + c];
+                o0[first + c] = acc;
+            }
+        }
+        /* y0 = x[0] + o W_O (+ b_O), then the MLP of the one row with its residual */
+        oracle_matmul(o0, w_o, b_o, 1, D, D, a0);
+        for (int64_t j = 0; j < D; ++j) y0[j] = xs[j] + a0[j];
+        oracle_layernorm(y0, 1, D, eps, ln2_g, ln2_b, yn0);
+        oracle_matmul(yn0, w_mlp1, b1, 1, D, F, z0);
+        oracle_gelu_tanh_array(z0, F, g0);
+        oracle_matmul(g0, w_mlp2, b2, 1, F, D, m0);
+        for (int64_t j = 0; j < D; ++j) out[(size_t)n * D + j] = y0[j] + m0[j];
+        free(buf);
+    }
+    return failed ? -2 : 0;
+}
+
+/* The stack of oracle_vit_encoder with its last block replaced by the CLS-only readout
+ * (oracle_vit_block_cls) and the final LayerNorm applied to the N CLS rows: out is
+ * (N, D). The first L - 1 blocks are oracle_vit_encoder without its final LayerNorm. */
+int oracle_vit_encoder_cls(const double* x, const double* const* layers, int64_t L,
+                           const double* lnf_g, const double* lnf_b, int final_ln, int64_t N,
+                           int64_t T, int64_t D, int64_t F, int64_t H, double eps, double* out,
+                           int nthreads)
+{
+    if (L <= 0 || N <= 0 || T <= 0 || D <= 0) return -1;
+    double* body = NULL;
+    double* c = (double*)malloc(sizeof(double) * (size_t)(N * D));
+    if (L > 1) body = (double*)malloc(sizeof(double) * (size_t)(N * T * D));
+    if (!c || (L > 1 && !body)) {
+        free(body);
+        free(c);
+        return -2;
+    }
+    int rc = 0;
+    if (L > 1)
+        rc = oracle_vit_encoder(x, layers, L - 1, NULL, NULL, 0, N, T, D, F, H, eps, body, nthreads);
+    if (rc == 0) {
+        const double* const* last = layers + (size_t)(L - 1) * 16;
+        rc = oracle_vit_block_cls(L > 1 ? body : x, last[0], last[1], last[2], last[3], last[4],
+                                  last[5], last[6], last[7], last[8], last[9], last[10], last[11],
+                                  last[12], last[13], last[14], last[15], N, T, D, F, H, eps, c,
+                                  nthreads);
+    }
+    if (rc == 0) {
+        if (final_ln)
+            oracle_layernorm(c, N, D, eps, lnf_g, lnf_b, out);
+        else
+            memcpy(out, c, sizeof(double) * (size_t)(N * D));
+    }
+    free(body);
+    free(c);
+    return rc;
+}
+
 /* Patch embedding front end. Images (N, C, Hi, Wi), non-overlapping P x P patches taken
  * in row-major order over the (Hi/P, Wi/P) grid, each flattened to C P P values and
  * projected: tokens = patches @ w (+ b), w of shape (C P P, D); then, with cls non-NULL,

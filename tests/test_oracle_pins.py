@@ -437,6 +437,50 @@ def test_encoder_without_updates_is_layernorm_of_x():
     np.testing.assert_array_equal(oracle.vit_encoder(x, layers, 3, 1e-6), oracle.layernorm(x, 1e-6))
 
 
+# --------------------------------------------------------------- CLS-only last block
+
+def _call_cls(a, H, eps, **kw):
+    return oracle.vit_block_cls(a["x"], a["w_q"], a["w_k"], a["w_v"], a["w_o"], a["w_mlp1"],
+                                a["w_mlp2"], H, eps, **{k: a.get(k) for k in
+                                                        ("ln1_g", "ln1_b", "ln2_g", "ln2_b", "b1", "b2",
+                                                         "b_q", "b_k", "b_v", "b_o")}, **kw)
+
+
+@pytest.mark.parametrize("shape", [(2, 7, 12, 20, 3), (3, 5, 6, 6, 6), (2, 33, 16, 64, 1),
+                                   (1, 197, 192, 768, 3), (2, 2, 8, 16, 2)])
+def test_cls_block_is_row0_of_torch_block(shape):
+    # the readout is row 0 of the whole block, whose float64 PyTorch composition is an
+    # independent statement of it
+    N, T, D, F, H = shape
+    a = _with_proj_biases(_rand_block(N, T, D, F, seed=sum(shape), affine=True), seed=6)
+    np.testing.assert_allclose(_call_cls(a, H, 1e-6), _torch_block(a, H, 1e-6)[:, 0], rtol=0, atol=1e-11)
+
+
+def test_cls_block_is_row0_of_the_oracle_block():
+    a = _with_proj_biases(_rand_block(3, 11, 12, 24, seed=13, affine=True), seed=8)
+    np.testing.assert_array_equal(_call_cls(a, 3, 1e-6), _call_full(a, 3, 1e-6)[:, 0])
+
+
+def test_cls_block_single_token():
+    # T = 1: the one query sees only its own key, so the attention output is its value row
+    a = _rand_block(4, 1, 8, 16, seed=14)
+    a = dict(a, w_o=np.eye(8), w_mlp2=np.zeros((16, 8)))
+    xn = oracle.layernorm(a["x"][:, 0], 1e-6)
+    np.testing.assert_allclose(_call_cls(a, 2, 1e-6), a["x"][:, 0] + xn @ a["w_v"], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3])
+def test_encoder_cls_matches_torch_stack(L):
+    rng = np.random.default_rng(40 + L)
+    x = rng.standard_normal((2, 9, 12))
+    layers = _rand_layers(L, 12, 24, seed=60 + L)
+    g, b = 1 + 0.1 * rng.standard_normal(12), 0.1 * rng.standard_normal(12)
+    np.testing.assert_allclose(oracle.vit_encoder(x, layers, 3, 1e-6, lnf_g=g, lnf_b=b, cls_only=True),
+                               _torch_encoder(x, layers, 3, 1e-6, g, b)[:, 0], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(oracle.vit_encoder(x, layers, 3, 1e-6, final_ln=False, cls_only=True),
+                               _torch_encoder(x, layers, 3, 1e-6, final_ln=False)[:, 0], rtol=0, atol=1e-11)
+
+
 # --------------------------------------------------------------- patch embedding front end
 
 def _rand_images(N, C, H, W, P, D, seed):
@@ -533,6 +577,17 @@ MUTANTS = {
                               "for (int64_t i = 0; i < P; ++i)\n                        for (int64_t j = 0; j < P; ++j) {\n                            const double v = images[(((size_t)n * C + c) * Hi + py * P + j) * Wi + px * P + i];"),
     "pos_skips_cls_row": ("for (int64_t t = 0; t < T; ++t)\n                for (int64_t d = 0; d < D; ++d) o[(size_t)t * D + d] += pos[(size_t)t * D + d];",
                           "for (int64_t t = 1; t < T; ++t)\n                for (int64_t d = 0; d < D; ++d) o[(size_t)t * D + d] += pos[(size_t)t * D + d];"),
+    "cls_query_from_row1": ("oracle_matmul(xn, w_q, b_q, 1, D, D, q0);",
+                            "oracle_matmul(xn + D, w_q, b_q, 1, D, D, q0);"),
+    "cls_drop_b_q": ("oracle_matmul(xn, w_q, b_q, 1, D, D, q0);", "oracle_matmul(xn, w_q, NULL, 1, D, D, q0);"),
+    "cls_keys_without_ln": ("oracle_matmul(xn, w_k, b_k, T, D, D, keys);",
+                            "oracle_matmul(xs, w_k, b_k, T, D, D, keys);"),
+    "cls_first_key_only": ("oracle_softmax_rows(sc, 1, T, pw);",
+                           "oracle_softmax_rows(sc, 1, 1, pw);\n            for (int64_t u = 1; u < T; ++u) pw[u] = 0.0;"),
+    "cls_residual_on_normalised": ("y0[j] = xs[j] + a0[j];", "y0[j] = xn[j] + a0[j];"),
+    "cls_skips_earlier_blocks": ("rc = oracle_vit_block_cls(L > 1 ? body : x,", "rc = oracle_vit_block_cls(x,"),
+    "cls_final_ln_skipped": ("oracle_layernorm(c, N, D, eps, lnf_g, lnf_b, out);",
+                             "memcpy(out, c, sizeof(double) * (size_t)(N * D));"),
     "drop_patch_bias": ("                if (b)\n                    for (int64_t d = 0; d < D; ++d) row[d] += b[d];",
                         "                if (b && 0)\n                    for (int64_t d = 0; d < D; ++d) row[d] += b[d];"),
 }
@@ -560,6 +615,13 @@ def _pins_pass(lib):
     g, b = 1 + 0.1 * rng.standard_normal(12), 0.1 * rng.standard_normal(12)
     got = oracle.vit_encoder(x, layers, 3, 1e-5, lnf_g=g, lnf_b=b, lib=lib)
     if not np.allclose(got, _torch_encoder(x, layers, 3, 1e-5, g, b), rtol=0, atol=1e-11):
+        return False
+    # the CLS-only readout of one block and of a stack
+    a = _with_proj_biases(_rand_block(2, 7, 12, 20, seed=25, affine=True), seed=6)
+    if not np.allclose(_call_cls(a, 3, 1e-5, lib=lib), _torch_block(a, 3, 1e-5)[:, 0], rtol=0, atol=1e-11):
+        return False
+    got = oracle.vit_encoder(x, layers, 3, 1e-5, lnf_g=g, lnf_b=b, lib=lib, cls_only=True)
+    if not np.allclose(got, _torch_encoder(x, layers, 3, 1e-5, g, b)[:, 0], rtol=0, atol=1e-11):
         return False
     # patch embedding, both orders, with the CLS row and positions
     im, w, bb, cls, pos = _rand_images(2, 3, 16, 24, 8, 10, seed=24)
