@@ -37,6 +37,9 @@ METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf1
 UNIT = "tokens/s"
 PATCH_METRIC = "ViT patch-embedding front end tokens/s at ViT-B/16 width bf16, 1 GPU"
 ENCODER_METRIC = "ViT encoder (%d blocks + final LN) tokens/s at ViT-B/16 width bf16, 1 GPU"
+CLS_METRIC = "ViT CLS-only last block tokens/s at ViT-B/16 bf16, 1 GPU"
+ENCODER_CLS_METRIC = ("ViT encoder (%d blocks, the last CLS-only, + final LN of the CLS rows) tokens/s at "
+                      "ViT-B/16 width bf16, 1 GPU")
 L2_FLUSH_BYTES = 512 << 20  # > 126 MB L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -52,6 +55,13 @@ def workload_name(name, c):
 def flops_per_step(c):
     N, T, D, F = c["N"], c["T"], c["D"], c["F"]
     return 2 * N * T * (4 * D * D + 2 * D * F) + 4 * N * T * T * D
+
+
+def cls_flops_per_step(c):
+    """The CLS-only block: K/V projections of every row; query, attention, output
+    projection and MLP of the N CLS rows."""
+    N, T, D, F = c["N"], c["T"], c["D"], c["F"]
+    return 2 * N * T * D * 2 * D + 2 * N * (2 * D * D + 2 * D * F) + 4 * N * T * D
 
 
 def kernel_work(c):
@@ -76,6 +86,14 @@ def kernel_work(c):
         "patchify": ("hbm", N * (T - 1) * 768 * 2 * 2, "bytes"),
         "patch_gemm": ("tensor", 2 * N * (T - 1) * 768 * D, "flops"),
         "patch_assemble": ("hbm", N * (T - 1) * D * 4 + M * D * 2, "bytes"),
+        # CLS-only last block: K/V of all rows; one query row per sequence
+        "kv_gemm": ("tensor", 2 * M * D * 2 * D, "flops"),
+        "cls_q_gemm": ("tensor", 2 * N * D * D, "flops"),
+        "cls_attention": ("hbm", M * 2 * D * 2 + N * D * 2 * 2, "bytes"),   # K, V read; q read, o written
+        "cls_wo_gemm_residual": ("tensor", 2 * N * D * D, "flops"),
+        "cls_ln2": ("hbm", N * D * (4 + 2), "bytes"),
+        "cls_w1_gemm_gelu": ("tensor", 2 * N * D * F, "flops"),
+        "cls_w2_gemm_residual": ("tensor", 2 * N * F * D, "flops"),
     }
 
 
@@ -274,6 +292,9 @@ def main():
     ap.add_argument("--encoder-layers", type=int, default=0,
                     help="time vit_encoder: this many blocks with Q/K/V/O biases, LN affine "
                          "terms and the final LayerNorm, instead of one block")
+    ap.add_argument("--cls-only", action="store_true",
+                    help="the last block computes the CLS rows alone: vit_block_cls (with "
+                         "--encoder-layers 0) or vit_encoder_cls")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -305,6 +326,17 @@ def main():
 
         def step():
             api.vit_patch_embed(pim, 16, pw, b=pb, cls=pcls, pos=ppos, out=out, stream=stream)
+    elif args.cls_only:
+        ex, elayers, elnf_g, elnf_b = make_encoder_inputs(c["N"], c["T"], c["D"], c["F"], max(L, 1), seed=rank,
+                                                          dtype=torch.bfloat16, device=dev)
+        out = torch.empty((c["N"], c["D"]), dtype=torch.bfloat16, device=dev)
+        if L == 0:
+            def step():
+                api.vit_block_cls(ex, elayers[0], H, eps, out=out, stream=stream)
+        else:
+            def step():
+                api.vit_encoder(ex, elayers, H, eps, lnf_g=elnf_g, lnf_b=elnf_b, out=out, stream=stream,
+                                cls_only=True)
     elif L > 0:
         ex, elayers, elnf_g, elnf_b = make_encoder_inputs(c["N"], c["T"], c["D"], c["F"], L, seed=rank,
                                                           dtype=torch.bfloat16, device=dev)
@@ -354,7 +386,8 @@ def main():
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
-    if args.e2e_steps > 0 and L == 0 and not args.patch_embed:
+    single_block = L == 0 and not args.patch_embed and not args.cls_only
+    if args.e2e_steps > 0 and single_block:
         pinned = [t.pin_memory() for t in [inp.x] + inp.weights()]
         hout = torch.empty_like(pinned[0]).pin_memory()
         api.vit_block_host(*pinned, H, eps, out=hout, device=dev.index)
@@ -396,22 +429,41 @@ def main():
                  "peak_source": "%s (%s)" % (peak_src, "bf16 burst" if bound == "tensor" else "copy"),
                  "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
                                        if bound == "tensor" else None)})
-    step_flops = (2 * c["N"] * 196 * 768 * c["D"]) if args.patch_embed else max(L, 1) * flops_per_step(c)
+    if args.patch_embed:
+        step_flops = 2 * c["N"] * 196 * 768 * c["D"]
+    elif args.cls_only:
+        step_flops = max(L - 1, 0) * flops_per_step(c) + cls_flops_per_step(c)
+    else:
+        step_flops = max(L, 1) * flops_per_step(c)
+    if args.patch_embed:
+        metric = PATCH_METRIC
+        workload = ("patch embedding of %d images 3 x 224 x 224 (16 x 16 patches, CLS row, positions) into "
+                    "(%d, 197, %d) tokens" % (c["N"], c["N"], c["D"]))
+    elif args.cls_only and L == 0:
+        metric = CLS_METRIC
+        workload = ("CLS-only block (row 0 of each sequence; Q/K/V/O and MLP biases, LN gains) of %s"
+                    % workload_name(name, c))
+    elif args.cls_only:
+        metric = ENCODER_CLS_METRIC % L
+        workload = ("%d-block encoder with a CLS-only last block (Q/K/V/O and MLP biases, LN gains, final "
+                    "LayerNorm of the CLS rows) of %s" % (L, workload_name(name, c)))
+    elif L > 0:
+        metric = ENCODER_METRIC % L
+        workload = ("%d-block encoder (Q/K/V/O and MLP biases, LN gains, final LayerNorm) of %s"
+                    % (L, workload_name(name, c)))
+    else:
+        metric, workload = METRIC, workload_name(name, c)
     step_tflops = step_flops / (ms_per_step / 1e3) / 1e12
     kernels = {k: {"avg_us": 1e3 * v[0] / v[1] if v[1] else None, "launches": v[1],
                    "share": v[0] / sum(x[0] for x in per_kernel.values())}
                for k, v in per_kernel.items()}
     line = {
-        "metric": (PATCH_METRIC if args.patch_embed else METRIC if L == 0 else ENCODER_METRIC % L),
+        "metric": metric,
         "value": value, "unit": UNIT,
         "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": ("patch embedding of %d images 3 x 224 x 224 (16 x 16 patches, CLS row, "
-                                "positions) into (%d, 197, %d) tokens" % (c["N"], c["N"], c["D"]))
-                   if args.patch_embed else workload_name(name, c) if L == 0 else
-                   "%d-block encoder (Q/K/V/O and MLP biases, LN gains, final LayerNorm) of %s"
-                   % (L, workload_name(name, c)),
+        "config": {"workload": workload,
                    "tokens_per_step_per_gpu": tokens,
                    "inputs": "seeded synthetic: x ~ N(0,1), weights ~ N(0, 1/fan_in), bf16",
                    "l2": "512 MiB written between timed steps (flush); per-step working set "
@@ -425,7 +477,7 @@ def main():
         "e2e": e2e,
         "clocks": sampler.summary(t0, t1),
     }
-    if world == 1 and not args.no_cpu_baseline and L == 0 and not args.patch_embed:
+    if world == 1 and not args.no_cpu_baseline and single_block:
         line["cpu_baseline"] = cpu_baseline(name, c)
     if args.n_seq:
         line["config"]["note"] = "N overridden on the command line (not the headline workload)"

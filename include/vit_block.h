@@ -181,6 +181,37 @@ int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* l
                 int64_t H, double eps, int dtype, void* out, void* stream);
 
 /*
+ * vit_block_cls -- one block computed for the CLS row (row 0 of each sequence) alone.
+ *
+ * Definition: lecture transcript (nipunbatra.github.io), Page 55 -- when only the CLS
+ * token is read after the last block, that block need only produce row 0: its single
+ * query is scored against the keys of all T rows and mixes the value rows of all T rows,
+ * and the output projection, residual and MLP act on that one row. The result equals row
+ * 0 of vit_encoder's single-block output with the same layer.
+ *
+ *   x      (N, T, D) input tokens, `dtype`, row 0 of each sequence the CLS token
+ *   layer  HOST pointer to one vit_layer record (as in vit_encoder)
+ *   out    (N, D) `dtype`: the block's output row 0 of each sequence
+ * Work and traffic: LN1 and the key and value projections cover all N T rows; the query,
+ * attention, output projection, LN2 and MLP cover N rows. Errors as vit_encoder;
+ * VIT_ERR_UNSUPPORTED when the T scores of one query do not fit in shared memory
+ * (T above about 50,000 in fp32, 25,000 in fp64).
+ */
+int vit_block_cls(const void* x, const vit_layer* layer, int64_t N, int64_t T, int64_t D,
+                  int64_t F, int64_t H, double eps, int dtype, void* out, void* stream);
+
+/*
+ * vit_encoder_cls -- vit_encoder whose last block is vit_block_cls: the stack's CLS
+ * features. Lecture transcript, Page 55 (CLS-only readout in the final block) and Pages
+ * 111-112 (the final normalisation; applied here to the N CLS rows, the only rows read).
+ *   out  (N, D) `dtype`: LN(last block's row 0) when final_ln, else that row
+ * Other arguments and errors as vit_encoder and vit_block_cls.
+ */
+int vit_encoder_cls(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g,
+                    const void* lnf_b, int final_ln, int64_t N, int64_t T, int64_t D, int64_t F,
+                    int64_t H, double eps, int dtype, void* out, void* stream);
+
+/*
  * vit_patch_embed -- the patch-embedding front end: images to tokens.
  *
  * Definition: lecture transcript (nipunbatra.github.io), Pages 96-105 -- non-overlapping

@@ -89,7 +89,7 @@ def test_step_entry_points_validate(lib):
 
 
 def test_timing_interface_without_gpu(lib):
-    assert lib.vit_timing_kernels() == 14
+    assert lib.vit_timing_kernels() == 21
     ms, n, nm = ctypes.c_double(), ctypes.c_int64(), ctypes.c_char_p()
     assert lib.vit_timing_read(0, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(nm)) == 0
     assert nm.value == b"ln1"
@@ -109,6 +109,24 @@ def test_encoder_argument_checks(lib):
     lay2 = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 6 + [_fake(10).value + 8] + [None] * 3)
     arr2 = (api.VitLayer * 1)(lay2)
     assert lib.vit_encoder(_fake(0), arr2, 1, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+
+
+def test_cls_argument_checks(lib):
+    layer = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 10)
+    arr = (api.VitLayer * 1)(layer)
+    assert lib.vit_block_cls(_fake(0), None, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    assert lib.vit_block_cls(_fake(0), arr, 2, 5, 8, 16, 3, 1e-5, 1, _fake(10), None) == -1   # H does not divide D
+    assert lib.vit_block_cls(_fake(0), arr, 2, 5, 8, 16, 2, 1e-5, 9, _fake(10), None) == -2
+    assert lib.vit_block_cls(None, arr, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    # the (N, D) output overlapping x; (N, D) bf16 is 32 bytes, so an output 64 bytes before
+    # x does not overlap it, but one 16 bytes before does
+    assert lib.vit_block_cls(_fake(0), arr, 2, 5, 8, 16, 2, 1e-5, 1, ctypes.c_void_p(_fake(0).value - 16),
+                             None) == -1
+    assert lib.vit_encoder_cls(_fake(0), arr, 0, None, None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    assert lib.vit_encoder_cls(_fake(0), arr, 1, None, None, 1, 0, 5, 8, 16, 2, 1e-5, 1, _fake(10), None) == -1
+    # out overlapping the final LayerNorm's gain
+    assert lib.vit_encoder_cls(_fake(0), arr, 1, _fake(10), None, 1, 2, 5, 8, 16, 2, 1e-5, 1, _fake(10),
+                               None) == -1
 
 
 def test_patch_embed_argument_checks(lib):

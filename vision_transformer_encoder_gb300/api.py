@@ -39,6 +39,9 @@ SIGNATURES = {
     "vit_block_noalloc": (_int, [_vp] * 13 + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_encoder": (_int, [_vp, ctypes.POINTER(VitLayer), _i64, _vp, _vp, _int] + [_i64] * 5
                     + [_dbl, _int, _vp, _vp]),
+    "vit_encoder_cls": (_int, [_vp, ctypes.POINTER(VitLayer), _i64, _vp, _vp, _int] + [_i64] * 5
+                        + [_dbl, _int, _vp, _vp]),
+    "vit_block_cls": (_int, [_vp, ctypes.POINTER(VitLayer)] + [_i64] * 5 + [_dbl, _int, _vp, _vp]),
     "vit_patch_embed": (_int, [_vp] + [_i64] * 5 + [_int] + [_vp] * 4 + [_i64, _int, _vp, _vp]),
     "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
     "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
@@ -163,30 +166,57 @@ def vit_block(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, out=None, stream=No
     return out
 
 
-def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, out=None, stream=None):
-    """out (N, T, D) = the stack of blocks in `layers` (a list of dicts keyed by
-    LAYER_FIELDS: the six weights required, the rest optional), then, with final_ln,
-    the final LayerNorm with the optional gain lnf_g and bias lnf_b."""
-    lib = load_library()
-    dt = x.dtype
-    _dev(x, "x", dt)
+def _layer_array(layers, dt):
     arr = (VitLayer * max(len(layers), 1))()
     for i, lay in enumerate(layers):
         for name in LAYER_FIELDS:
             t = lay.get(name)
             _dev(t, "layer %d %s" % (i, name), dt)
             setattr(arr[i], name, None if t is None else t.data_ptr())
+    return arr
+
+
+def vit_encoder(x, layers, H, eps, lnf_g=None, lnf_b=None, final_ln=True, out=None, stream=None,
+                cls_only=False):
+    """out (N, T, D) = the stack of blocks in `layers` (a list of dicts keyed by
+    LAYER_FIELDS: the six weights required, the rest optional), then, with final_ln,
+    the final LayerNorm with the optional gain lnf_g and bias lnf_b. cls_only: the last
+    block computes the CLS row alone (vit_encoder_cls) and out is (N, D)."""
+    lib = load_library()
+    dt = x.dtype
+    _dev(x, "x", dt)
+    arr = _layer_array(layers, dt)
     _dev(lnf_g, "lnf_g", dt)
     _dev(lnf_b, "lnf_b", dt)
     N, T, D = x.shape
     F = layers[0]["w_mlp1"].shape[1] if layers else 0
     if out is None:
-        out = torch.empty_like(x)
+        out = torch.empty((N, D) if cls_only else (N, T, D), dtype=dt, device=x.device)
+    _dev(out, "out", dt)
+    fn = lib.vit_encoder_cls if cls_only else lib.vit_encoder
+    with torch.cuda.device(x.device):
+        rc = fn(_ptr(x), arr, len(layers), _ptr(lnf_g), _ptr(lnf_b), 1 if final_ln else 0,
+                N, T, D, F, int(H), float(eps), _dtype_code(dt), _ptr(out), _stream(stream))
+    _check(rc, "vit_encoder_cls" if cls_only else "vit_encoder")
+    return out
+
+
+def vit_block_cls(x, layer, H, eps, out=None, stream=None):
+    """out (N, D) = row 0 of each sequence's block output, computed for that row alone
+    (its query against all T keys and values); layer: a dict keyed by LAYER_FIELDS."""
+    lib = load_library()
+    dt = x.dtype
+    _dev(x, "x", dt)
+    arr = _layer_array([layer], dt)
+    N, T, D = x.shape
+    F = layer["w_mlp1"].shape[1]
+    if out is None:
+        out = torch.empty((N, D), dtype=dt, device=x.device)
     _dev(out, "out", dt)
     with torch.cuda.device(x.device):
-        rc = lib.vit_encoder(_ptr(x), arr, len(layers), _ptr(lnf_g), _ptr(lnf_b), 1 if final_ln else 0,
-                             N, T, D, F, int(H), float(eps), _dtype_code(dt), _ptr(out), _stream(stream))
-    _check(rc, "vit_encoder")
+        rc = lib.vit_block_cls(_ptr(x), arr, N, T, D, F, int(H), float(eps), _dtype_code(dt), _ptr(out),
+                               _stream(stream))
+    _check(rc, "vit_block_cls")
     return out
 
 

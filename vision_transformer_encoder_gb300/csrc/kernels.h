@@ -162,6 +162,12 @@ bool attention_tc_supported(int64_t N, int64_t T, int64_t D, int64_t H, const vo
                             const void* o);
 cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, int64_t D,
                                 int64_t H, const DeviceInfo& dev, cudaStream_t s);
+// One query row per sequence (attention_cls.cu): q row n at q + n ldq, keys / values of
+// sequence n row u at k / v + (n T + u) ldkv, o row n at o + n ldo, all of type dt; heads
+// are column blocks of D / H. Supported while the T scores fit in shared memory.
+bool attention_cls_supported(int64_t N, int64_t T, int64_t D, int64_t H, int dt);
+cudaError_t launch_attention_cls(const void* q, int64_t ldq, const void* k, const void* v, int64_t ldkv, int dt,
+                                 int64_t N, int64_t T, int64_t D, int64_t H, void* o, int64_t ldo, cudaStream_t s);
 // Any dtype (f32/bf16/f64 in and out, same type), any head width.
 cudaError_t launch_attention_simt(const void* qkv, int dt, void* o, int64_t N, int64_t T,
                                   int64_t D, int64_t H, cudaStream_t s);

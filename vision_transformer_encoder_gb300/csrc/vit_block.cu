@@ -50,12 +50,15 @@ std::atomic<int64_t> g_launches{0};
 
 // ---- per-kernel timing -------------------------------------------------------
 enum Kern { K_LN1 = 0, K_QKV, K_ATTN, K_WO, K_LN2, K_W1, K_W2, K_LN1_STATS, K_FOLD_PREP, K_TF32_SPLIT, K_FINAL_LN,
-            K_PATCHIFY, K_PATCH_GEMM, K_PATCH_ASSEMBLE, K_COUNT };
+            K_PATCHIFY, K_PATCH_GEMM, K_PATCH_ASSEMBLE, K_KV, K_CLS_Q, K_CLS_ATTN, K_CLS_WO, K_CLS_LN2,
+            K_CLS_W1, K_CLS_W2, K_COUNT };
 const char* const kKernNames[K_COUNT] = {"ln1",          "qkv_gemm",         "attention",
                                          "wo_gemm_residual", "ln2",          "w1_gemm_gelu",
                                          "w2_gemm_residual", "ln1_row_stats", "ln_fold_prep",
                                          "tf32_weight_split", "final_ln", "patchify", "patch_gemm",
-                                         "patch_assemble"};
+                                         "patch_assemble", "kv_gemm", "cls_q_gemm", "cls_attention",
+                                         "cls_wo_gemm_residual", "cls_ln2", "cls_w1_gemm_gelu",
+                                         "cls_w2_gemm_residual"};
 struct Pending {
     int kind;
     cudaEvent_t a, b;
@@ -177,7 +180,8 @@ cudaError_t concat_qkv_bias(const BlockArgs& a, cudaStream_t s) {
     return cudaSuccess;
 }
 
-int validate(const BlockArgs& a) {
+// out_bytes: the size of the caller's output (0: the block's (N, T, D) in dt).
+int validate(const BlockArgs& a, size_t out_bytes = 0) {
     if (a.dt != DT_F32 && a.dt != DT_BF16 && a.dt != DT_F64) return VIT_ERR_DTYPE;
     if (!a.x || !a.w_q || !a.w_k || !a.w_v || !a.w_o || !a.w1 || !a.w2 || !a.out) return VIT_ERR_ARG;
     if (a.N <= 0 || a.T <= 0 || a.D <= 0 || a.F <= 0 || a.H <= 0 || a.D % a.H != 0) return VIT_ERR_ARG;
@@ -191,8 +195,9 @@ int validate(const BlockArgs& a) {
     const size_t nb[] = {xb, dd, dd, dd, dd, df, df,
                          (size_t)a.D * es, (size_t)a.D * es, (size_t)a.D * es, (size_t)a.D * es,
                          (size_t)a.F * es, (size_t)a.D * es};
+    const size_t ob = out_bytes ? out_bytes : xb;
     for (int i = 0; i < 13; ++i)
-        if (overlaps(a.out, xb, in[i], nb[i])) return VIT_ERR_ARG;
+        if (overlaps(a.out, ob, in[i], nb[i])) return VIT_ERR_ARG;
     return VIT_OK;
 }
 
@@ -547,6 +552,222 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     return e;
 }
 
+// ---- CLS-only block -------------------------------------------------------------
+// Lecture transcript (nipunbatra.github.io), Page 55: when only the CLS token (row 0 of
+// each sequence) is read after the last block, that block need only produce row 0. Its
+// one query is scored against the keys of all T rows and mixes the value rows of all T
+// rows, so LN1 and the key and value projections still cover every row; the query, the
+// attention output, the output projection, LN2 and the MLP cover the N CLS rows:
+//   1 LN1        x (all rows)          -> xn
+//   2 K/V GEMM   xn                    -> kv = xn @ [w_k | w_v] (+ [b_k | b_v])
+//   3 Q GEMM     xn rows 0 (stride T D) -> q = xn0 @ w_q (+ b_q)
+//   4 attention  q, kv                 -> o (N, D)
+//   5 Wo GEMM    o                     -> y = x0 + o @ w_o (+ b_o)
+//   6 LN2        y                     -> yn
+//   7 W1 GEMM    yn                    -> h = GELU_tanh(yn @ w_mlp1 (+ b1))
+//   8 W2 GEMM    h                     -> out (N, D) = y + h @ w_mlp2 (+ b2)
+// Scratch: xn (M, D) | kv (M, 2D) | q, o (N, D) | y (N, D) | yn (N, D) | h (N, F), in the
+// accumulation type (y fp32 on the bf16 path), plus the 3xTF32 pieces on the fp32 path.
+struct ClsWorkspace {
+    bool fast, tf32;
+    int acc_dt;
+    size_t sz_xn, sz_kv, sz_row, sz_y, sz_h, sz_lo, sz_wt;
+    size_t total;
+};
+
+ClsWorkspace cls_workspace_layout(const BlockArgs& a) {
+    ClsWorkspace w;
+    const int64_t M = a.N * a.T, N = a.N, D = a.D, F = a.F;
+    w.fast = fast_path_ok(a);
+    w.acc_dt = w.fast ? DT_BF16 : (a.dt == DT_F64 ? DT_F64 : DT_F32);
+    const size_t ea = dt_size(w.acc_dt);
+    w.sz_xn = round_up((size_t)(M * D) * ea, 256);
+    w.sz_kv = round_up((size_t)(M * 2 * D) * ea, 256);
+    w.sz_row = round_up((size_t)(N * D) * ea, 256);
+    w.sz_y = round_up((size_t)(N * D) * (w.fast ? 4 : ea), 256);
+    w.sz_h = round_up((size_t)(N * F) * ea, 256);
+    w.tf32 = !w.fast && a.dt == DT_F32 && tf32x3_supported(M, 2 * D, D, D, a.x) && F % 4 == 0 && tf32_requested();
+    w.sz_lo = w.sz_wt = 0;
+    if (w.tf32) {
+        const int64_t lo = M * D > N * F ? M * D : N * F;
+        w.sz_lo = round_up((size_t)lo * 4, 256);
+        w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
+    }
+    w.total = w.sz_xn + w.sz_kv + 3 * w.sz_row + w.sz_y + w.sz_h + w.sz_lo + w.sz_wt;
+    return w;
+}
+
+// Enqueues the CLS-only block on `s`; a.out is (N, D) of out_dtype(a).
+cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s,
+                                   const ClsWorkspace& w, void* ws) {
+    const int64_t M = a.N * a.T, N = a.N, T = a.T, D = a.D, F = a.F;
+    const int acc = w.acc_dt, xdt = x_dtype(a), odt = out_dtype(a);
+    const size_t ea = dt_size(acc);
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    void* xn = p;  p += w.sz_xn;
+    void* kv = p;  p += w.sz_kv;
+    void* q = p;   p += w.sz_row;
+    void* o = p;   p += w.sz_row;
+    void* yn = p;  p += w.sz_row;
+    void* y = p;   p += w.sz_y;
+    void* h = p;   p += w.sz_h;
+    uint8_t* tail = p;
+    void* v_of_kv = static_cast<uint8_t*>(kv) + D * ea;
+    cudaError_t e = cudaSuccess;
+    auto step = [&](cudaError_t err) {
+        if (e == cudaSuccess) e = err;
+    };
+    const bool qkv_bias = has_qkv_bias(a);
+    if (qkv_bias) step(concat_qkv_bias(a, s));
+    // [b_k | b_v] of the concatenated [b_q | b_k | b_v]
+    const void* bkv = qkv_bias ? static_cast<const uint8_t*>(a.bias_scratch) + D * dt_size(a.dt) : nullptr;
+    step(run(K_LN1, s, [&] {
+        return launch_layernorm(a.x, xdt, xn, acc, a.ln1_g, a.ln1_b, w.fast ? DT_BF16 : a.dt, M, D, a.eps, s);
+    }));
+    auto attention = [&] {
+        return run(K_CLS_ATTN, s, [&] {
+            return launch_attention_cls(q, D, kv, v_of_kv, 2 * D, acc, N, T, D, a.H, o, D, s);
+        });
+    };
+    if (w.fast) {
+        TcGemmDesc g;
+        std::memset(&g, 0, sizeof(g));
+        g.a = xn; g.lda = D;
+        g.w[0] = a.w_k; g.w[1] = a.w_v; g.n_w = 2; g.n_per_w = D;
+        g.M = M; g.N = 2 * D; g.K = D;
+        g.epi = TC_EPI_STORE; g.bias = bkv;
+        g.out = kv; g.ldo = 2 * D; g.out_f32 = false;
+        step(run(K_KV, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{xn, DT_BF16, D, a.w_k, DT_BF16, D, a.b_k, DT_BF16, nullptr, 0, 0,
+                            kv, DT_BF16, 2 * D, M, D, D, TC_EPI_STORE};
+            cudaError_t r = launch_gemm_simt(sd, s);
+            sd.w = a.w_v; sd.bias = a.b_v; sd.out = v_of_kv;
+            if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
+            return r;
+        }));
+        std::memset(&g, 0, sizeof(g));
+        g.a = xn; g.lda = T * D; g.w[0] = a.w_q; g.n_w = 1; g.n_per_w = D;
+        g.M = N; g.N = D; g.K = D;
+        g.epi = TC_EPI_STORE; g.bias = a.b_q;
+        g.out = q; g.ldo = D; g.out_f32 = false;
+        step(run(K_CLS_Q, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{xn, DT_BF16, T * D, a.w_q, DT_BF16, D, a.b_q, DT_BF16, nullptr, 0, 0,
+                            q, DT_BF16, D, N, D, D, TC_EPI_STORE};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(attention());
+        std::memset(&g, 0, sizeof(g));
+        g.a = o; g.lda = D; g.w[0] = a.w_o; g.n_w = 1; g.n_per_w = D;
+        g.M = N; g.N = D; g.K = D;
+        g.epi = TC_EPI_RESID; g.bias = a.b_o; g.residual = a.x; g.ldr = T * D; g.residual_f32 = xdt == DT_F32;
+        g.out = y; g.ldo = D; g.out_f32 = true;
+        step(run(K_CLS_WO, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{o, DT_BF16, D, a.w_o, DT_BF16, D, a.b_o, DT_BF16, a.x, xdt, T * D,
+                            y, DT_F32, D, N, D, D, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(run(K_CLS_LN2, s, [&] {
+            return launch_layernorm(y, DT_F32, yn, DT_BF16, a.ln2_g, a.ln2_b, DT_BF16, N, D, a.eps, s);
+        }));
+        std::memset(&g, 0, sizeof(g));
+        g.a = yn; g.lda = D; g.w[0] = a.w1; g.n_w = 1; g.n_per_w = F;
+        g.M = N; g.N = F; g.K = D;
+        g.epi = TC_EPI_GELU; g.bias = a.b1;
+        g.out = h; g.ldo = F; g.out_f32 = false;
+        step(run(K_CLS_W1, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{yn, DT_BF16, D, a.w1, DT_BF16, F, a.b1, DT_BF16, nullptr, 0, 0,
+                            h, DT_BF16, F, N, F, D, TC_EPI_GELU};
+            return launch_gemm_simt(sd, s);
+        }));
+        std::memset(&g, 0, sizeof(g));
+        g.a = h; g.lda = F; g.w[0] = a.w2; g.n_w = 1; g.n_per_w = D;
+        g.M = N; g.N = D; g.K = F;
+        g.epi = TC_EPI_RESID; g.bias = a.b2; g.residual = y; g.ldr = D; g.residual_f32 = true;
+        g.out = a.out; g.ldo = D; g.out_f32 = odt == DT_F32;
+        step(run(K_CLS_W2, s, [&] {
+            if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
+            SimtGemmDesc sd{h, DT_BF16, F, a.w2, DT_BF16, D, a.b2, DT_BF16, y, DT_F32, D,
+                            a.out, odt, D, N, D, F, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+    } else if (w.tf32) {
+        float* lo = reinterpret_cast<float*>(tail);
+        float* wqkv_t = reinterpret_cast<float*>(tail + w.sz_lo), *wqkv_lo = wqkv_t + 3 * D * D;
+        float* wo_t = wqkv_lo + 3 * D * D, *wo_lo = wo_t + D * D;
+        float* w1_t = wo_lo + D * D, *w1_lo = w1_t + F * D;
+        float* w2_t = w1_lo + F * D, *w2_lo = w2_t + D * F;
+        step(run(K_TF32_SPLIT, s, [&] {
+            const void* wq[3] = {a.w_q, a.w_k, a.w_v};
+            cudaError_t r = cudaSuccess;
+            for (int i = 0; i < 3 && r == cudaSuccess; ++i)
+                r = launch_split_wt(static_cast<const float*>(wq[i]), D, D, D, i * D, wqkv_t, wqkv_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo, s);
+            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo, s);
+            return r;
+        }));
+        // out (rows, N) = epi(A (rows, K; row stride lda) @ W + bias [+ res (row stride ldr)])
+        auto gemm = [&](const void* A, int64_t rows, int64_t K, int64_t lda, const float* bt, const float* btlo,
+                        int64_t Nc, int epi, const void* bias, const void* res, int64_t ldr, void* out) {
+            cudaError_t r = launch_split_lo(static_cast<const float*>(A), rows, K, lda, lo, s);
+            if (r != cudaSuccess) return r;
+            Tf32GemmDesc g{static_cast<const float*>(A), lda, lo, bt, btlo, rows, Nc, K, epi,
+                           static_cast<const float*>(bias), static_cast<const float*>(res), ldr,
+                           static_cast<float*>(out), Nc};
+            return launch_gemm_tf32x3(g, dev, s);
+        };
+        step(run(K_KV, s, [&] {
+            return gemm(xn, M, D, D, wqkv_t + D * D, wqkv_lo + D * D, 2 * D, TC_EPI_STORE, bkv, nullptr, 0, kv);
+        }));
+        step(run(K_CLS_Q, s, [&] {
+            return gemm(xn, N, D, T * D, wqkv_t, wqkv_lo, D, TC_EPI_STORE, a.b_q, nullptr, 0, q);
+        }));
+        step(attention());
+        step(run(K_CLS_WO, s, [&] {
+            return gemm(o, N, D, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, a.x, T * D, y);
+        }));
+        step(run(K_CLS_LN2, s, [&] {
+            return launch_layernorm(y, DT_F32, yn, DT_F32, a.ln2_g, a.ln2_b, DT_F32, N, D, a.eps, s);
+        }));
+        step(run(K_CLS_W1, s, [&] { return gemm(yn, N, D, D, w1_t, w1_lo, F, TC_EPI_GELU, a.b1, nullptr, 0, h); }));
+        step(run(K_CLS_W2, s, [&] { return gemm(h, N, F, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, y, D, a.out); }));
+    } else {
+        const int dt = a.dt;
+        step(run(K_KV, s, [&] {
+            SimtGemmDesc sd{xn, acc, D, a.w_k, dt, D, a.b_k, dt, nullptr, 0, 0, kv, acc, 2 * D, M, D, D, TC_EPI_STORE};
+            cudaError_t r = launch_gemm_simt(sd, s);
+            sd.w = a.w_v; sd.bias = a.b_v; sd.out = v_of_kv;
+            if (r == cudaSuccess) r = launch_gemm_simt(sd, s);
+            return r;
+        }));
+        step(run(K_CLS_Q, s, [&] {
+            SimtGemmDesc sd{xn, acc, T * D, a.w_q, dt, D, a.b_q, dt, nullptr, 0, 0, q, acc, D, N, D, D, TC_EPI_STORE};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(attention());
+        step(run(K_CLS_WO, s, [&] {
+            SimtGemmDesc sd{o, acc, D, a.w_o, dt, D, a.b_o, dt, a.x, xdt, T * D, y, acc, D, N, D, D, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(run(K_CLS_LN2, s, [&] {
+            return launch_layernorm(y, acc, yn, acc, a.ln2_g, a.ln2_b, dt, N, D, a.eps, s);
+        }));
+        step(run(K_CLS_W1, s, [&] {
+            SimtGemmDesc sd{yn, acc, D, a.w1, dt, F, a.b1, dt, nullptr, 0, 0, h, acc, F, N, F, D, TC_EPI_GELU};
+            return launch_gemm_simt(sd, s);
+        }));
+        step(run(K_CLS_W2, s, [&] {
+            SimtGemmDesc sd{h, acc, F, a.w2, dt, D, a.b2, dt, y, acc, D, a.out, odt, D, N, D, F, TC_EPI_RESID};
+            return launch_gemm_simt(sd, s);
+        }));
+    }
+    return e;
+}
+
 // LayerNorm folded into the GEMMs is opt-in (VIT_LN_FOLD=1): it removes the LN2 pass
 // and LN1's normalised copy, but the extra epilogue work in the Wo and W1 GEMMs
 // currently costs as much as it saves.
@@ -633,6 +854,103 @@ int noalloc_device(NoAllocState** out) {
     return VIT_OK;
 }
 
+// A stack of L blocks (the last one CLS-only when cls_only) and the optional final
+// LayerNorm; the entry points vit_encoder, vit_encoder_cls and vit_block_cls.
+int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g, const void* lnf_b,
+                 int final_ln, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H, double eps, int dtype,
+                 void* out, void* stream, bool cls_only) {
+    if (!layers || L < 1 || L > (1 << 20)) return VIT_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto layer_args = [&](int64_t l, const void* in, void* o) {
+        const vit_layer& ly = layers[l];
+        BlockArgs a{in, ly.w_q, ly.w_k, ly.w_v, ly.w_o, ly.w_mlp1, ly.w_mlp2, ly.ln1_g, ly.ln1_b, ly.ln2_g,
+                    ly.ln2_b, ly.b1, ly.b2, N, T, D, F, H, eps, dtype, o};
+        a.b_q = ly.b_q; a.b_k = ly.b_k; a.b_v = ly.b_v; a.b_o = ly.b_o;
+        return a;
+    };
+    // argument checks of every layer against the caller's x and out (as vit_block_ex),
+    // plus the projection biases and the final LayerNorm's gain and bias
+    // the caller's output: (N, T, D), or (N, D) with a CLS-only last block
+    const size_t ob = (size_t)((cls_only ? N : N * T) * D) * dt_size(dtype);
+    for (int64_t l = 0; l < L; ++l) {
+        int rc = validate(layer_args(l, x, out), ob);
+        if (rc != VIT_OK) return rc;
+        const size_t xb = ob, db = (size_t)D * dt_size(dtype);
+        const vit_layer& ly = layers[l];
+        const void* extra[] = {ly.b_q, ly.b_k, ly.b_v, ly.b_o};
+        for (const void* p : extra)
+            if (overlaps(out, xb, p, db)) return VIT_ERR_ARG;
+        if (overlaps(out, xb, lnf_g, db) || overlaps(out, xb, lnf_b, db)) return VIT_ERR_ARG;
+    }
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    const DeviceInfo& dev = st->info;
+    const int64_t M = N * T;
+    const int sdt = dtype == DT_BF16 ? DT_F32 : dtype;   // residual stream between blocks
+    const size_t stream_bytes = round_up((size_t)(M * D) * dt_size(sdt), 256);
+    const size_t bias_bytes = round_up((size_t)(3 * D) * dt_size(dtype), 256);
+    // scratch: the largest block workspace | two residual-stream buffers | qkv bias
+    std::vector<Workspace> wl((size_t)L);
+    ClsWorkspace wc{};
+    size_t block_bytes = 0;
+    void* const probe = reinterpret_cast<void*>(256);   // pool memory is 256-byte aligned
+    for (int64_t l = 0; l < L; ++l) {
+        BlockArgs a = layer_args(l, l == 0 ? x : probe, probe);
+        size_t need;
+        if (cls_only && l == L - 1) {
+            wc = cls_workspace_layout(a);
+            if (!attention_cls_supported(N, T, D, H, wc.acc_dt)) return VIT_ERR_UNSUPPORTED;
+            need = wc.total;
+        } else {
+            wl[(size_t)l] = workspace_layout(a, false);
+            need = wl[(size_t)l].total;
+        }
+        block_bytes = need > block_bytes ? need : block_bytes;
+    }
+    const size_t total = block_bytes + 2 * stream_bytes + bias_bytes;
+    void* ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
+    }
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    void* r[2] = {base + block_bytes, base + block_bytes + stream_bytes};
+    void* bias_scratch = base + block_bytes + 2 * stream_bytes;
+    const void* cur = x;
+    for (int64_t l = 0; l < L && e == cudaSuccess; ++l) {
+        const bool last = l == L - 1;
+        void* dst = (last && !final_ln) ? out : r[l & 1];
+        BlockArgs a = layer_args(l, cur, dst);
+        a.x_dt = l == 0 ? dtype : sdt;
+        a.out_dt = (last && !final_ln) ? dtype : sdt;
+        a.bias_scratch = bias_scratch;
+        if (cls_only && last)
+            e = launch_block_cls_steps(a, dev, s, wc, ws);
+        else
+            e = launch_block_steps(a, dev, s, wl[(size_t)l], ws);
+        cur = dst;
+    }
+    if (e == cudaSuccess && final_ln)
+        e = run(K_FINAL_LN, s, [&] {
+            return launch_layernorm(cur, sdt, out, dtype, lnf_g, lnf_b, dtype, cls_only ? N : M, D, eps, s);
+        });
+    cudaError_t fe = cudaFreeAsync(ws, s);
+    if (e == cudaSuccess) e = fe;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    if (debug_sync()) {
+        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
+        uint32_t w = 0;
+        if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
+        if (w) return VIT_ERR_TIMEOUT;
+    }
+    return VIT_OK;
+}
+
 }  // namespace
 }  // namespace vit
 
@@ -665,82 +983,18 @@ int vit_block(const void* x, const void* w_q, const void* w_k, const void* w_v, 
 int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g, const void* lnf_b,
                 int final_ln, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H, double eps, int dtype,
                 void* out, void* stream) {
-    if (!layers || L < 1 || L > (1 << 20)) return VIT_ERR_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    auto layer_args = [&](int64_t l, const void* in, void* o) {
-        const vit_layer& ly = layers[l];
-        BlockArgs a{in, ly.w_q, ly.w_k, ly.w_v, ly.w_o, ly.w_mlp1, ly.w_mlp2, ly.ln1_g, ly.ln1_b, ly.ln2_g,
-                    ly.ln2_b, ly.b1, ly.b2, N, T, D, F, H, eps, dtype, o};
-        a.b_q = ly.b_q; a.b_k = ly.b_k; a.b_v = ly.b_v; a.b_o = ly.b_o;
-        return a;
-    };
-    // argument checks of every layer against the caller's x and out (as vit_block_ex),
-    // plus the projection biases and the final LayerNorm's gain and bias
-    for (int64_t l = 0; l < L; ++l) {
-        int rc = validate(layer_args(l, x, out));
-        if (rc != VIT_OK) return rc;
-        const size_t xb = (size_t)(N * T * D) * dt_size(dtype), db = (size_t)D * dt_size(dtype);
-        const vit_layer& ly = layers[l];
-        const void* extra[] = {ly.b_q, ly.b_k, ly.b_v, ly.b_o};
-        for (const void* p : extra)
-            if (overlaps(out, xb, p, db)) return VIT_ERR_ARG;
-        if (overlaps(out, xb, lnf_g, db) || overlaps(out, xb, lnf_b, db)) return VIT_ERR_ARG;
-    }
-    DeviceState* st = nullptr;
-    int rc = current_device(&st);
-    if (rc != VIT_OK) return rc;
-    const DeviceInfo& dev = st->info;
-    const int64_t M = N * T;
-    const int sdt = dtype == DT_BF16 ? DT_F32 : dtype;   // residual stream between blocks
-    const size_t stream_bytes = round_up((size_t)(M * D) * dt_size(sdt), 256);
-    const size_t bias_bytes = round_up((size_t)(3 * D) * dt_size(dtype), 256);
-    // scratch: the largest block workspace | two residual-stream buffers | qkv bias
-    std::vector<Workspace> wl((size_t)L);
-    size_t block_bytes = 0;
-    void* const probe = reinterpret_cast<void*>(256);   // pool memory is 256-byte aligned
-    for (int64_t l = 0; l < L; ++l) {
-        BlockArgs a = layer_args(l, l == 0 ? x : probe, probe);
-        wl[(size_t)l] = workspace_layout(a, false);
-        block_bytes = wl[(size_t)l].total > block_bytes ? wl[(size_t)l].total : block_bytes;
-    }
-    const size_t total = block_bytes + 2 * stream_bytes + bias_bytes;
-    void* ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, total, st->pool, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : VIT_ERR_CUDA;
-    }
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    void* r[2] = {base + block_bytes, base + block_bytes + stream_bytes};
-    void* bias_scratch = base + block_bytes + 2 * stream_bytes;
-    const void* cur = x;
-    for (int64_t l = 0; l < L && e == cudaSuccess; ++l) {
-        const bool last = l == L - 1;
-        void* dst = (last && !final_ln) ? out : r[l & 1];
-        BlockArgs a = layer_args(l, cur, dst);
-        a.x_dt = l == 0 ? dtype : sdt;
-        a.out_dt = (last && !final_ln) ? dtype : sdt;
-        a.bias_scratch = bias_scratch;
-        e = launch_block_steps(a, dev, s, wl[(size_t)l], ws);
-        cur = dst;
-    }
-    if (e == cudaSuccess && final_ln)
-        e = run(K_FINAL_LN, s, [&] {
-            return launch_layernorm(cur, sdt, out, dtype, lnf_g, lnf_b, dtype, M, D, eps, s);
-        });
-    cudaError_t fe = cudaFreeAsync(ws, s);
-    if (e == cudaSuccess) e = fe;
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return status_from(e);
-    }
-    if (debug_sync()) {
-        if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
-        uint32_t w = 0;
-        if (cudaMemcpyFromSymbol(&w, g_err_word, sizeof(w)) != cudaSuccess) return VIT_ERR_CUDA;
-        if (w) return VIT_ERR_TIMEOUT;
-    }
-    return VIT_OK;
+    return encoder_impl(x, layers, L, lnf_g, lnf_b, final_ln, N, T, D, F, H, eps, dtype, out, stream, false);
+}
+
+int vit_encoder_cls(const void* x, const vit_layer* layers, int64_t L, const void* lnf_g, const void* lnf_b,
+                    int final_ln, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H, double eps, int dtype,
+                    void* out, void* stream) {
+    return encoder_impl(x, layers, L, lnf_g, lnf_b, final_ln, N, T, D, F, H, eps, dtype, out, stream, true);
+}
+
+int vit_block_cls(const void* x, const vit_layer* layer, int64_t N, int64_t T, int64_t D, int64_t F, int64_t H,
+                  double eps, int dtype, void* out, void* stream) {
+    return encoder_impl(x, layer, 1, nullptr, nullptr, 0, N, T, D, F, H, eps, dtype, out, stream, true);
 }
 
 int vit_patch_embed(const void* images, int64_t N, int64_t C, int64_t Hi, int64_t Wi, int64_t P, int order,
