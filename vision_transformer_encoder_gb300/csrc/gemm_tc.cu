@@ -59,6 +59,10 @@ struct Params {
     TcLnFold fold;
     float2* parts_out;   // extra outputs: row partials (mean, M2), 2 per 256-column tile
     int parts_stride;
+    // split K (pair kernel): work item w is tile w / ksplit over k blocks
+    // [ks kb_per, (ks + 1) kb_per) with ks = w % ksplit; ksplit > 1 stores the raw fp32
+    // sums of slice ks at depth ks of a 3-D output map
+    int ksplit, kb_per;
 };
 
 __device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
@@ -395,7 +399,7 @@ template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS, bool FOLD
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
                                                   const CUtensorMap* tmOut2, uint8_t* stage,
                                                   uint32_t t_row, int row, int row0, int n0,
-                                                  int lane, int part_index) {
+                                                  int lane, int part_index, int zk = -1) {
     float rv[32];
     epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
     float2 st = make_float2(0.f, 1.f);
@@ -446,7 +450,10 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-                ptx::tma_store_2d(tmOut, buf, col, row0);
+                if (zk >= 0)
+                    ptx::tma_store_3d(tmOut, buf, col, row0, zk);
+                else
+                    ptx::tma_store_2d(tmOut, buf, col, row0);
                 ptx::bulk_commit_group();
             }
             if (EXTRA) {
@@ -521,6 +528,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int n_tiles = (p.N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles;
     const int kblocks = p.K / BK;
+    const int num_items = num_tiles * p.ksplit;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P_STAGES; ++s) {
@@ -562,10 +570,12 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(full), 0);  // leader's
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+            for (int w = cluster; w < num_items && ok; w += nclusters) {
+                const int tile = w / p.ksplit, ks = w - tile * p.ksplit;
                 const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
                 const int n0 = (tile % n_tiles) * BN + (int)rank * (BN / 2);
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int kb0 = ks * p.kb_per, kb1 = min(kblocks, kb0 + p.kb_per);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const uint32_t s = it % P_STAGES, u = it / P_STAGES;
                     if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
                         ok = false;
@@ -609,7 +619,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t it = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+            for (int w = cluster; w < num_items; w += nclusters, ++local) {
+                const int ks = w % p.ksplit;
+                const int kb0 = ks * p.kb_per, kb1 = min(kblocks, kb0 + p.kb_per);
                 const int acc = local & 1;
                 const uint32_t v = (uint32_t)(local >> 1);
                 if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
@@ -618,7 +630,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
                     const uint32_t s = it % P_STAGES, u = it / P_STAGES;
                     if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
                         ok = false;
@@ -632,7 +644,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint64_t adesc = ptx::smem_desc_sw128(a_base + k * 32, 16, 1024);
                         const uint64_t bdesc =
                             ptx::smem_desc_sw128(b_base + k * 2048, B_BOX_BYTES, 1024);
-                        ptx::mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
+                        ptx::mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, kb != kb0 || k != 0);
                     }
                     ptx::mma_commit_pair_mc(empty + s, 0x3);
                 }
@@ -652,7 +664,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int half = (warp - 5) >> 2;           // which 128 of the 256 columns
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);  // leader's
         int local = 0;
-        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+        for (int w = cluster; w < num_items; w += nclusters, ++local) {
+            const int tile = w / p.ksplit, ks = w - tile * p.ksplit;
             const int acc = local & 1;
             const uint32_t v = (uint32_t)(local >> 1);
             const int m0 = (tile / n_tiles) * 2 * BM + (int)rank * BM;
@@ -668,7 +681,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
             epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA>(
                 p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row, row0 + lane, row0,
-                n0 + half * 128, lane, (n0 / BN) * 2 + half);
+                n0 + half * 128, lane, (n0 / BN) * 2 + half, p.ksplit > 1 ? ks : -1);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
@@ -787,7 +800,118 @@ bool use_pair_kernel() {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Split K (VIT_GEMM_SPLITK=0 turns it off): a pair-kernel GEMM whose output tiles fill at
+// most half of the CTA pairs is cut along K so that every pair gets work, with at least
+// two 64-deep k blocks per slice.
+bool split_k_enabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char* e = std::getenv("VIT_GEMM_SPLITK");
+        v = (e && e[0] == '0') ? 0 : 1;
+    }
+    return v == 1;
+}
+
+struct SplitK {
+    int ksplit = 1, kb_per = 0;
+};
+
+SplitK split_k_for(int64_t M, int64_t N, int64_t K, int num_sms) {
+    SplitK r;
+    const int kblocks = (int)(K / BK);
+    r.kb_per = kblocks;
+    if (!split_k_enabled() || !use_pair_kernel() || num_sms < 4) return r;
+    const int64_t tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
+    const int64_t pairs = num_sms / 2;
+    if (tiles * 2 > pairs || kblocks < 4) return r;
+    int64_t ks = pairs / tiles;
+    if (ks > kblocks / 2) ks = kblocks / 2;
+    if (ks < 2) return r;
+    r.kb_per = (int)((kblocks + ks - 1) / ks);
+    r.ksplit = (kblocks + r.kb_per - 1) / r.kb_per;
+    return r;
+}
+
+// out[m, n] = epi(sum over slices k of part[k][m][n] (+ bias[n])) (+ residual[m, n]), the
+// slices added in order; four columns per thread (N % 64 == 0).
+template <int EPI, typename OutT, typename ResT>
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(const float* __restrict__ part, int ksplit, int M, int N, const __nv_bfloat16* __restrict__ bias,
+                    const ResT* __restrict__ residual, int64_t ldr, OutT* __restrict__ out, int64_t ldo) {
+    const int nq = N / 4;
+    const int64_t total = (int64_t)M * nq, slice = (int64_t)M * N;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int m = (int)(i / nq), n = (int)(i - (int64_t)m * nq) * 4;
+        const float* src = part + (int64_t)m * N + n;
+        float4 a = *reinterpret_cast<const float4*>(src);
+        for (int k = 1; k < ksplit; ++k) {
+            const float4 b = *reinterpret_cast<const float4*>(src + k * slice);
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        float v[4] = {a.x, a.y, a.z, a.w};
+        if (bias) {
+            const uint2 u = *reinterpret_cast<const uint2*>(bias + n);
+            const float2 b0 = unpack_bf16x2(u.x), b1 = unpack_bf16x2(u.y);
+            v[0] += b0.x; v[1] += b0.y; v[2] += b1.x; v[3] += b1.y;
+        }
+        if (EPI == TC_EPI_GELU) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = gelu_tanh_fast(v[j]);
+        } else if (EPI == TC_EPI_RESID) {
+            const ResT* r = residual + (int64_t)m * ldr + n;
+            if constexpr (sizeof(ResT) == 4) {
+                const float4 q = *reinterpret_cast<const float4*>(r);
+                v[0] += q.x; v[1] += q.y; v[2] += q.z; v[3] += q.w;
+            } else {
+                const uint2 u = *reinterpret_cast<const uint2*>(r);
+                const float2 q0 = unpack_bf16x2(u.x), q1 = unpack_bf16x2(u.y);
+                v[0] += q0.x; v[1] += q0.y; v[2] += q1.x; v[3] += q1.y;
+            }
+        }
+        OutT* o = out + (int64_t)m * ldo + n;
+        if constexpr (sizeof(OutT) == 4) {
+            *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            uint2 u;
+            u.x = pack_bf16x2(v[0], v[1]);
+            u.y = pack_bf16x2(v[2], v[3]);
+            *reinterpret_cast<uint2*>(o) = u;
+        }
+    }
+}
+
+template <int EPI, typename OutT, typename ResT>
+cudaError_t launch_split_reduce(const TcGemmDesc& d, int ksplit, const DeviceInfo& dev, cudaStream_t s) {
+    const int64_t total = d.M * (d.N / 4);
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 8 * (int64_t)dev.num_sms) blocks = 8 * (int64_t)dev.num_sms;
+    split_reduce_kernel<EPI, OutT, ResT><<<(unsigned)blocks, 256, 0, s>>>(
+        d.split_ws, ksplit, (int)d.M, (int)d.N, static_cast<const __nv_bfloat16*>(d.bias),
+        static_cast<const ResT*>(d.residual), d.ldr, static_cast<OutT*>(d.out), d.ldo);
+    return cudaGetLastError();
+}
+
+// fp32 partial sums (ksplit, rows, cols), contiguous; 32 x 32 x 1 boxes, 128B swizzle.
+bool make_map_split(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int ksplit) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)ksplit};
+    cuuint64_t strides[2] = {(cuuint64_t)(cols * 4), (cuuint64_t)(rows * cols * 4)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+int64_t tc_split_ws_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+    if (M <= 0 || N <= 0 || K <= 0 || K % BK != 0) return 0;
+    const SplitK sk = split_k_for(M, N, K, dev.num_sms);
+    return sk.ksplit > 1 ? (int64_t)sk.ksplit * M * N * 4 : 0;
+}
 
 bool tc_pair_enabled(const DeviceInfo& dev) { return use_pair_kernel() && dev.num_sms >= 2; }
 
@@ -824,6 +948,14 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     } else {
         mo2 = mo;
     }
+    // split K: raw fp32 slices into split_ws, then the reduction applies the epilogue
+    SplitK sk;
+    sk.kb_per = (int)(d.K / BK);
+    if (pair && !d.fold.parts && !d.extra.parts && d.split_ws && d.N % 64 == 0 && aligned16(d.split_ws)) {
+        const SplitK c = split_k_for(d.M, d.N, d.K, dev.num_sms);
+        if (c.ksplit > 1 && (int64_t)c.ksplit * d.M * d.N * 4 <= d.split_ws_bytes) sk = c;
+    }
+    if (sk.ksplit > 1 && !make_map_split(&mo, d.split_ws, d.M, d.N, sk.ksplit)) return cudaErrorInvalidValue;
     Params p;
     p.M = (int)d.M;
     p.N = (int)d.N;
@@ -839,14 +971,38 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     p.fold = d.fold;
     p.parts_out = d.extra.parts;
     p.parts_stride = (int)(2 * ((d.N + BN - 1) / BN));
+    p.ksplit = sk.ksplit;
+    p.kb_per = sk.kb_per;
     int grid;
     if (pair) {
-        const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN);
+        const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN) * sk.ksplit;
         const int64_t clusters = tiles < dev.num_sms / 2 ? tiles : dev.num_sms / 2;
         grid = (int)(2 * clusters);
     } else {
         const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
         grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
+    }
+    if (sk.ksplit > 1) {
+        p.bias = nullptr;
+        cudaError_t e = launch_any<TC_EPI_STORE, float, float>(true, ma, mb, mo, mo2, p, grid, s);
+        if (e != cudaSuccess) return e;
+        switch (d.epi) {
+            case TC_EPI_STORE:
+                return d.out_f32 ? launch_split_reduce<TC_EPI_STORE, float, float>(d, sk.ksplit, dev, s)
+                                 : launch_split_reduce<TC_EPI_STORE, __nv_bfloat16, float>(d, sk.ksplit, dev, s);
+            case TC_EPI_GELU:
+                return d.out_f32 ? launch_split_reduce<TC_EPI_GELU, float, float>(d, sk.ksplit, dev, s)
+                                 : launch_split_reduce<TC_EPI_GELU, __nv_bfloat16, float>(d, sk.ksplit, dev, s);
+            case TC_EPI_RESID:
+                if (d.out_f32)
+                    return d.residual_f32
+                               ? launch_split_reduce<TC_EPI_RESID, float, float>(d, sk.ksplit, dev, s)
+                               : launch_split_reduce<TC_EPI_RESID, float, __nv_bfloat16>(d, sk.ksplit, dev, s);
+                return d.residual_f32
+                           ? launch_split_reduce<TC_EPI_RESID, __nv_bfloat16, float>(d, sk.ksplit, dev, s)
+                           : launch_split_reduce<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(d, sk.ksplit, dev, s);
+        }
+        return cudaErrorInvalidValue;
     }
     switch (d.epi) {
         case TC_EPI_STORE:

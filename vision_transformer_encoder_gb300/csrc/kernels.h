@@ -65,6 +65,12 @@ struct TcGemmDesc {
     bool out_f32;
     TcLnFold fold;         // fold.parts != nullptr: LayerNorm folded (pair kernel)
     TcExtraOut extra;      // extra.parts != nullptr: extra outputs (pair kernel)
+    // Split K for GEMMs with too few output tiles to fill the GPU (pair kernel, no fold or
+    // extra outputs): with split_ws holding tc_split_ws_bytes(...) bytes, the K range is
+    // cut into slices whose fp32 sums land in split_ws and a second kernel adds them in
+    // slice order and applies the epilogue. nullptr: no split.
+    float* split_ws;
+    int64_t split_ws_bytes;
 };
 
 // True when the pair kernel is in use (the fused LayerNorm needs it).
@@ -94,6 +100,8 @@ cudaError_t launch_fold_prep(const FoldPrep& d, float* scratch, cudaStream_t s);
 
 // True when the tensor-core GEMM takes this shape and these pointers.
 bool tc_gemm_supported(const TcGemmDesc& d);
+// Bytes of split_ws a GEMM of this shape uses on this device (0: it is not split).
+int64_t tc_split_ws_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev);
 cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStream_t s);
 
 // ---- CUDA-core GEMM (generic.cu) ----------------------------------------------

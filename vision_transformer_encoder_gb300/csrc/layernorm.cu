@@ -58,6 +58,21 @@ template <> __device__ __forceinline__ void store_bf16<4>(__nv_bfloat16* p, cons
     *reinterpret_cast<uint2*>(p) = u;
 }
 
+// V consecutive bf16 gains or biases as floats, in one 16-byte (V = 8) or 8-byte (V = 4)
+// load; the vectors start at multiples of V elements.
+template <int V> __device__ __forceinline__ void load_param_bf16(const __nv_bfloat16* p, float (&o)[V]);
+template <> __device__ __forceinline__ void load_param_bf16<8>(const __nv_bfloat16* p, float (&o)[8]) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+    const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    o[4] = c.x; o[5] = c.y; o[6] = d.x; o[7] = d.y;
+}
+template <> __device__ __forceinline__ void load_param_bf16<4>(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y);
+    o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+}
+
 template <typename TIn, int MAXV>
 __global__ void __launch_bounds__(LN_THREADS)
 ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
@@ -104,12 +119,16 @@ ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
 #pragma unroll
             for (int e = 0; e < V; ++e) o[e] = (v[j][e] - mean) * rstd;
             if (gamma) {
+                float gv[V];
+                load_param_bf16<V>(gamma + idx * V, gv);
 #pragma unroll
-                for (int e = 0; e < V; ++e) o[e] *= __bfloat162float(gamma[idx * V + e]);
+                for (int e = 0; e < V; ++e) o[e] *= gv[e];
             }
             if (beta) {
+                float bv[V];
+                load_param_bf16<V>(beta + idx * V, bv);
 #pragma unroll
-                for (int e = 0; e < V; ++e) o[e] += __bfloat162float(beta[idx * V + e]);
+                for (int e = 0; e < V; ++e) o[e] += bv[e];
             }
             store_bf16<V>(orow + idx * V, o);
         }
@@ -203,7 +222,9 @@ cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt, co
     const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     const bool vec_ok = D % 8 == 0 && D <= 2048 && aligned16(x) && aligned16(out);
-    const bool gb_bf16 = (!gamma && !beta) || gb_dt == DT_BF16;
+    // gains and biases: bf16, read in 16-byte vectors
+    const bool gb_bf16 = ((!gamma && !beta) || gb_dt == DT_BF16) && (!gamma || aligned16(gamma)) &&
+                         (!beta || aligned16(beta));
     if (out_dt == DT_BF16 && vec_ok && gb_bf16 && (in_dt == DT_BF16 || in_dt == DT_F32)) {
         // registers hold ceil(D / (32 lanes * vector width)) vectors per lane
         const int per_lane = (int)((D / (in_dt == DT_BF16 ? 8 : 4) + 31) / 32);

@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* 
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* tm, const void* src, int32_t c0, int32_t c1,
+                                             int32_t c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

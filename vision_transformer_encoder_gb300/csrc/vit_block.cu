@@ -572,10 +572,11 @@ struct ClsWorkspace {
     bool fast, tf32;
     int acc_dt;
     size_t sz_xn, sz_kv, sz_row, sz_y, sz_h, sz_lo, sz_wt;
+    size_t sz_split;   // fp32 K-slice sums of the tensor-core GEMMs over few rows
     size_t total;
 };
 
-ClsWorkspace cls_workspace_layout(const BlockArgs& a) {
+ClsWorkspace cls_workspace_layout(const BlockArgs& a, const DeviceInfo& dev) {
     ClsWorkspace w;
     const int64_t M = a.N * a.T, N = a.N, D = a.D, F = a.F;
     w.fast = fast_path_ok(a);
@@ -593,7 +594,16 @@ ClsWorkspace cls_workspace_layout(const BlockArgs& a) {
         w.sz_lo = round_up((size_t)lo * 4, 256);
         w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
     }
-    w.total = w.sz_xn + w.sz_kv + 3 * w.sz_row + w.sz_y + w.sz_h + w.sz_lo + w.sz_wt;
+    w.sz_split = 0;
+    if (w.fast) {
+        const int64_t sizes[5][3] = {{M, 2 * D, D}, {N, D, D}, {N, F, D}, {N, D, F}, {N, D, D}};
+        for (const auto& sz : sizes) {
+            const size_t b = (size_t)tc_split_ws_bytes(sz[0], sz[1], sz[2], dev);
+            if (b > w.sz_split) w.sz_split = b;
+        }
+        w.sz_split = round_up(w.sz_split, 256);
+    }
+    w.total = w.sz_xn + w.sz_kv + 3 * w.sz_row + w.sz_y + w.sz_h + w.sz_lo + w.sz_wt + w.sz_split;
     return w;
 }
 
@@ -611,6 +621,8 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
     void* yn = p;  p += w.sz_row;
     void* y = p;   p += w.sz_y;
     void* h = p;   p += w.sz_h;
+    float* split = w.sz_split ? reinterpret_cast<float*>(p) : nullptr;
+    p += w.sz_split;
     uint8_t* tail = p;
     void* v_of_kv = static_cast<uint8_t*>(kv) + D * ea;
     cudaError_t e = cudaSuccess;
@@ -637,6 +649,7 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         g.M = M; g.N = 2 * D; g.K = D;
         g.epi = TC_EPI_STORE; g.bias = bkv;
         g.out = kv; g.ldo = 2 * D; g.out_f32 = false;
+        g.split_ws = split; g.split_ws_bytes = (int64_t)w.sz_split;
         step(run(K_KV, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{xn, DT_BF16, D, a.w_k, DT_BF16, D, a.b_k, DT_BF16, nullptr, 0, 0,
@@ -651,6 +664,7 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         g.M = N; g.N = D; g.K = D;
         g.epi = TC_EPI_STORE; g.bias = a.b_q;
         g.out = q; g.ldo = D; g.out_f32 = false;
+        g.split_ws = split; g.split_ws_bytes = (int64_t)w.sz_split;
         step(run(K_CLS_Q, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{xn, DT_BF16, T * D, a.w_q, DT_BF16, D, a.b_q, DT_BF16, nullptr, 0, 0,
@@ -663,6 +677,7 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         g.M = N; g.N = D; g.K = D;
         g.epi = TC_EPI_RESID; g.bias = a.b_o; g.residual = a.x; g.ldr = T * D; g.residual_f32 = xdt == DT_F32;
         g.out = y; g.ldo = D; g.out_f32 = true;
+        g.split_ws = split; g.split_ws_bytes = (int64_t)w.sz_split;
         step(run(K_CLS_WO, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{o, DT_BF16, D, a.w_o, DT_BF16, D, a.b_o, DT_BF16, a.x, xdt, T * D,
@@ -677,6 +692,7 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         g.M = N; g.N = F; g.K = D;
         g.epi = TC_EPI_GELU; g.bias = a.b1;
         g.out = h; g.ldo = F; g.out_f32 = false;
+        g.split_ws = split; g.split_ws_bytes = (int64_t)w.sz_split;
         step(run(K_CLS_W1, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{yn, DT_BF16, D, a.w1, DT_BF16, F, a.b1, DT_BF16, nullptr, 0, 0,
@@ -688,6 +704,7 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         g.M = N; g.N = D; g.K = F;
         g.epi = TC_EPI_RESID; g.bias = a.b2; g.residual = y; g.ldr = D; g.residual_f32 = true;
         g.out = a.out; g.ldo = D; g.out_f32 = odt == DT_F32;
+        g.split_ws = split; g.split_ws_bytes = (int64_t)w.sz_split;
         step(run(K_CLS_W2, s, [&] {
             if (tc_gemm_supported(g)) return launch_gemm_tc(g, dev, s);
             SimtGemmDesc sd{h, DT_BF16, F, a.w2, DT_BF16, D, a.b2, DT_BF16, y, DT_F32, D,
@@ -899,7 +916,7 @@ int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* 
         BlockArgs a = layer_args(l, l == 0 ? x : probe, probe);
         size_t need;
         if (cls_only && l == L - 1) {
-            wc = cls_workspace_layout(a);
+            wc = cls_workspace_layout(a, dev);
             if (!attention_cls_supported(N, T, D, H, wc.acc_dt)) return VIT_ERR_UNSUPPORTED;
             need = wc.total;
         } else {
