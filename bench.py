@@ -225,7 +225,9 @@ def cpu_baseline(name, c):
     """The float64 oracle on the host cores, on a bounded sample of the workload."""
     import oracle
     cores = oracle.max_threads()
-    n = max(1, min(cores, c["N"]))
+    # sixteen sequences per host core (the whole ViT-B/16 batch on a 16-core host): about
+    # ten seconds of oracle time
+    n = max(1, min(16 * cores, c["N"]))
     inp = make_config_inputs(name, dtype=torch.bfloat16, N=n)
     t = time.perf_counter()
     oracle.vit_block(inp.x, *inp.weights(), c["H"], c["eps"], nthreads=cores)
