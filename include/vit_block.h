@@ -96,11 +96,16 @@ int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_
 
 /*
  * vit_block_host -- vit_block_ex on HOST arrays: copies the inputs to the device,
- * runs the block and copies `out_host` back, all on `stream`, then synchronises
- * the stream before returning (so out_host is ready on return). Host arrays that
- * are page-locked (cudaHostAlloc / pinned) copy at full link speed; pageable ones
- * work but copy slower. Device buffers come from the library's pool. The optional
- * affine pointers are host pointers or NULL. Errors as vit_block.
+ * runs the block and copies `out_host` back, then synchronises `stream` before
+ * returning (so out_host is ready on return). Host arrays that are page-locked
+ * (cudaHostAlloc / pinned) copy at full link speed; pageable ones work but copy slower.
+ * Device buffers come from the library's pool. The optional affine pointers are host
+ * pointers or NULL. Errors as vit_block.
+ * Large batches (12,288 tokens or more) are cut into up to 8 chunks of whole sequences
+ * (sequences are independent: "ViT Encoder Block" (crackedaicode), "Inputs and output");
+ * the copy in, the block and the copy out of successive chunks overlap on three
+ * library-owned streams that start after, and end before, the work already queued on
+ * `stream`. Results are those of one vit_block_ex call on the whole batch, bit for bit.
  */
 int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_host,
                    const void* w_v_host, const void* w_o_host, const void* w_mlp1_host,

@@ -155,6 +155,45 @@ def test_host_buffer_entry_point_matches_device_call():
     assert torch.equal(host_out, dev_out)
 
 
+def _host_vs_device(name, N, affine=False, pageable=False):
+    c = CONFIGS[name]
+    inp = make_config_inputs(name, dtype=torch.bfloat16, N=N, affine=affine)
+    dev_out, _ = _run(inp, c["H"], c["eps"], affine=affine)
+    cpu = inp.to(device="cpu")
+    pin = (lambda t: t) if pageable else (lambda t: t.pin_memory())
+    args = [pin(t) for t in [cpu.x] + cpu.weights()]
+    aff = {k: pin(v) for k, v in cpu.affine().items()} if affine else {}
+    out = pin(torch.full_like(args[0], float("nan")))
+    host_out = api.vit_block_host(*args, c["H"], c["eps"], **aff, out=out)
+    return host_out, dev_out
+
+
+def test_host_pipeline_full_size_matches_device_call():
+    # 256 ViT-B/16 sequences: the host entry point cuts them into chunks whose copies in,
+    # blocks and copies out overlap on three streams; every sequence's result is the
+    # device call's, bit for bit
+    host_out, dev_out = _host_vs_device("vit_b16", 256)
+    assert torch.equal(host_out, dev_out)
+
+
+def test_host_pipeline_pageable_buffers():
+    host_out, dev_out = _host_vs_device("vit_ti16", 128, affine=True, pageable=True)
+    assert torch.equal(host_out, dev_out)
+
+
+def test_host_pipeline_uneven_chunks_in_a_subprocess():
+    # VIT_HOST_CHUNKS is read once per process: three chunks of 7 sequences (3, 2, 2)
+    import subprocess
+    import sys
+    code = ("import torch, sys; sys.path.insert(0, %r); import test_gpu_block as t; "
+            "h, d = t._host_vs_device('vit_ti16', 7, affine=True); "
+            "assert torch.equal(h, d); print('ok')" % os.path.dirname(__file__))
+    env = dict(os.environ, VIT_HOST_CHUNKS="3")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                       cwd=os.path.dirname(os.path.dirname(__file__)), timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
 def test_stream_argument_is_honoured():
     d = _dev()
     c = CONFIGS["vit_ti16"]

@@ -42,6 +42,8 @@ struct DeviceState {
     bool ready = false;
     DeviceInfo info;
     cudaMemPool_t pool = nullptr;
+    // vit_block_host's pipeline: host-to-device copies, compute, device-to-host copies
+    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
 };
 
 std::mutex g_mu;
@@ -968,6 +970,40 @@ int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* 
     return VIT_OK;
 }
 
+// vit_block_host cuts the batch into chunks of whole sequences so that copies in, blocks
+// and copies out of successive chunks overlap on three streams. Chunks keep at least
+// 12,288 tokens (enough rows to fill the GEMMs' tiles); at most 8. VIT_HOST_CHUNKS=k
+// forces k (1: one chunk on the caller's stream).
+int64_t host_chunks(int64_t N, int64_t T) {
+    static const int64_t forced = [] {
+        const char* e = std::getenv("VIT_HOST_CHUNKS");
+        return e ? (int64_t)std::atoll(e) : (int64_t)0;
+    }();
+    int64_t c = forced > 0 ? forced : (N * T) / 12288;
+    if (c > 8 && forced <= 0) c = 8;
+    if (c > N) c = N;
+    return c < 1 ? 1 : c;
+}
+
+// The device's three pipeline streams, created on first use (non-blocking).
+int pipeline_streams(DeviceState* st) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (st->h2d) return VIT_OK;
+    cudaStream_t a = nullptr, b = nullptr, c = nullptr;
+    if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) {
+        if (a) cudaStreamDestroy(a);
+        if (b) cudaStreamDestroy(b);
+        cudaGetLastError();
+        return VIT_ERR_CUDA;
+    }
+    st->comp = b;
+    st->d2h = c;
+    st->h2d = a;
+    return VIT_OK;
+}
+
 }  // namespace
 }  // namespace vit
 
@@ -1126,6 +1162,15 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
         if (i < 13 && !src[i]) continue;
         total += round_up(sizes[i], 256);
     }
+    const int64_t chunks = host_chunks(N, T);
+    cudaStream_t sh = s, sc = s, sd = s;   // copy-in, compute, copy-out
+    if (chunks > 1) {
+        rc = pipeline_streams(st);
+        if (rc != VIT_OK) return rc;
+        sh = st->h2d;
+        sc = st->comp;
+        sd = st->d2h;
+    }
     void* dmem = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&dmem, total, st->pool, s);
     if (e != cudaSuccess) {
@@ -1134,21 +1179,74 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
     }
     uint8_t* base = static_cast<uint8_t*>(dmem);
     const void* dev_in[13];
-    for (int i = 0; i < 13; ++i) {
-        dev_in[i] = src[i] ? base + off[i] : nullptr;
-        if (src[i] && e == cudaSuccess)
-            e = cudaMemcpyAsync(base + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, s);
-    }
+    for (int i = 0; i < 13; ++i) dev_in[i] = src[i] ? base + off[i] : nullptr;
     void* dev_out = base + off[13];
-    if (e == cudaSuccess) {
-        BlockArgs d{dev_in[0], dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], dev_in[6],
+    // events: start, then per chunk x copied and block computed, then copies out done
+    std::vector<cudaEvent_t> ev;
+    auto new_event = [&](cudaEvent_t* out) {
+        cudaError_t r = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev.push_back(*out);
+        return r;
+    };
+    cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp = nullptr;
+    if (chunks > 1) {
+        e = new_event(&start);
+        if (e == cudaSuccess) e = cudaEventRecord(start, s);   // after the allocation
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sh, start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, start, 0);
+    }
+    // weights and affine terms first, then x chunk by chunk
+    for (int i = 1; i < 13 && e == cudaSuccess; ++i)
+        if (src[i]) e = cudaMemcpyAsync(base + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, sh);
+    const size_t seq_bytes = (size_t)(T * D) * es;
+    int64_t n0 = 0;
+    for (int64_t c = 0; c < chunks && e == cudaSuccess && rc == VIT_OK; ++c) {
+        const int64_t nc = N / chunks + (c < N % chunks ? 1 : 0);
+        const size_t o = (size_t)n0 * seq_bytes, nbytes = (size_t)nc * seq_bytes;
+        e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(x_host) + o, nbytes,
+                            cudaMemcpyHostToDevice, sh);
+        cudaEvent_t in_ready = nullptr, done = nullptr;
+        if (chunks > 1) {
+            if (e == cudaSuccess) e = new_event(&in_ready);
+            if (e == cudaSuccess) e = cudaEventRecord(in_ready, sh);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, in_ready, 0);
+        }
+        if (e != cudaSuccess) break;
+        BlockArgs d{base + off[0] + o, dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], dev_in[6],
                     dev_in[7], dev_in[8], dev_in[9], dev_in[10], dev_in[11], dev_in[12],
-                    N, T, D, F, H, eps, dtype, dev_out};
-        rc = enqueue_block(d, st->info, s);
-        if (rc == VIT_OK) e = cudaMemcpyAsync(out_host, dev_out, xb, cudaMemcpyDeviceToHost, s);
+                    nc, T, D, F, H, eps, dtype, static_cast<uint8_t*>(dev_out) + o};
+        rc = enqueue_block(d, st->info, sc);
+        if (rc != VIT_OK) break;
+        if (chunks > 1) {
+            e = new_event(&done);
+            if (e == cudaSuccess) e = cudaEventRecord(done, sc);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, done, 0);
+            end_comp = done;
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + o, static_cast<uint8_t*>(dev_out) + o, nbytes,
+                                cudaMemcpyDeviceToHost, sd);
+        n0 += nc;
+    }
+    if (chunks > 1) {
+        // join: the caller's stream waits for the last copy out and the last block (and
+        // so for every copy in), then frees the buffers in its own order
+        cudaError_t je = new_event(&end_d2h);
+        if (je == cudaSuccess) je = cudaEventRecord(end_d2h, sd);
+        if (je == cudaSuccess) je = cudaStreamWaitEvent(s, end_d2h, 0);
+        if (je == cudaSuccess && end_comp) je = cudaStreamWaitEvent(s, end_comp, 0);
+        if (je == cudaSuccess) {
+            cudaEvent_t in_done = nullptr;
+            je = new_event(&in_done);
+            if (je == cudaSuccess) je = cudaEventRecord(in_done, sh);
+            if (je == cudaSuccess) je = cudaStreamWaitEvent(s, in_done, 0);
+        }
+        if (e == cudaSuccess) e = je;
     }
     cudaError_t fe = cudaFreeAsync(dmem, s);
     cudaError_t se = cudaStreamSynchronize(s);
+    for (cudaEvent_t x : ev) cudaEventDestroy(x);
     if (rc != VIT_OK) return rc;
     if (e == cudaSuccess) e = fe;
     if (e == cudaSuccess) e = se;
