@@ -395,7 +395,8 @@ __device__ __forceinline__ float2 merge_row_stats(const TcLnFold& f, int row) {
 // columns at a time. The residual of the next chunk is loaded into registers while the
 // current one is processed. With EXTRA, the same values are also stored as bf16 through
 // tmOut2 and the row's (mean, M2) over these columns is written to p.parts_out.
-template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS, bool FOLD, bool EXTRA>
+template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS, bool FOLD, bool EXTRA,
+          int STG = EPI_STAGE_BYTES>
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
                                                   const CUtensorMap* tmOut2, uint8_t* stage,
                                                   uint32_t t_row, int row, int row0, int n0,
@@ -442,7 +443,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
             for (int j = 0; j < 32; ++j) rv[j] = rnext[j];
         }
         if (col < p.N) {
-            uint8_t* buf = stage + (c % BUFS) * EPI_STAGE_BYTES;
+            uint8_t* buf = stage + (c % BUFS) * STG;
             // the store issued from this buffer BUFS chunks ago must have read it
             if (lane == 0) ptx::bulk_wait_group_read<BUFS - 1>();
             __syncwarp();
@@ -490,7 +491,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
         p.parts_out[(int64_t)row * p.parts_stride + part_index] = make_float2(cmean, cm2);
 }
 
-constexpr int P_STAGES = 5;
+// Ring depth and epilogue staging per output type: a bf16 staging tile is half the size
+// of an fp32 one, which leaves room for a sixth ring stage.
+template <typename OutT> struct PairCfg {
+    static constexpr int STAGES = sizeof(OutT) == 2 ? 6 : 5;
+    static constexpr int STAGE_TILE = sizeof(OutT) == 2 ? 32 * 64 : 32 * 128;
+};
 constexpr int P_EPI_WARPS = 8;
 constexpr int P_THREADS = 416;  // warp 0, 2, 3, 4: TMA (one 8 KB box each per stage);
                                 // warp 1: MMA; warps 5-12: epilogue
@@ -498,8 +504,12 @@ constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's 128 weight columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_EPI_BUFS = 1;   // staging tiles per epilogue warp
-constexpr int P_EPI_BYTES = P_EPI_WARPS * P_EPI_BUFS * EPI_STAGE_BYTES;
-constexpr int P_SMEM_BYTES = P_STAGES * P_STAGE_BYTES + P_EPI_BYTES + BAR_BYTES + 1024;
+template <typename OutT> __host__ __device__ constexpr int pair_epi_bytes() {
+    return P_EPI_WARPS * P_EPI_BUFS * PairCfg<OutT>::STAGE_TILE;
+}
+template <typename OutT> __host__ __device__ constexpr int pair_smem_bytes() {
+    return PairCfg<OutT>::STAGES * P_STAGE_BYTES + pair_epi_bytes<OutT>() + BAR_BYTES + 1024;
+}
 
 template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
@@ -507,13 +517,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOut2,
                     const Params p) {
+    constexpr int P_STAGES = PairCfg<OutT>::STAGES;
+    constexpr int P_STG = PairCfg<OutT>::STAGE_TILE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + P_STAGES * P_A_BYTES;
     uint8_t* sEpi = smem + P_STAGES * P_STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + P_EPI_BYTES);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + pair_epi_bytes<OutT>());
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -679,8 +691,8 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA>(
-                p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * EPI_STAGE_BYTES, t_row, row0 + lane, row0,
+            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA, P_STG>(
+                p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * P_STG, t_row, row0 + lane, row0,
                 n0 + half * 128, lane, (n0 / BN) * 2 + half, p.ksplit > 1 ? ks : -1);
             ptx::tc_fence_before();
             __syncwarp();
@@ -769,11 +781,11 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const C
     auto k = gemm_tc_pair_kernel<EPI, OutT, ResT, FOLD, EXTRA>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<OutT>());
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, P_THREADS, P_SMEM_BYTES, s>>>(a, b[0], b[1], b[2], out, out2, p);
+    k<<<grid, P_THREADS, pair_smem_bytes<OutT>(), s>>>(a, b[0], b[1], b[2], out, out2, p);
     return cudaGetLastError();
 }
 
