@@ -182,13 +182,13 @@ def test_host_pipeline_pageable_buffers():
 
 
 def test_host_pipeline_uneven_chunks_in_a_subprocess():
-    # VIT_HOST_CHUNKS is read once per process: three chunks of 7 sequences (3, 2, 2)
+    # VIT_HOST_SPLIT is read once per process: weights 1, 2, 1 over 7 sequences (2, 3, 2)
     import subprocess
     import sys
     code = ("import torch, sys; sys.path.insert(0, %r); import test_gpu_block as t; "
             "h, d = t._host_vs_device('vit_ti16', 7, affine=True); "
             "assert torch.equal(h, d); print('ok')" % os.path.dirname(__file__))
-    env = dict(os.environ, VIT_HOST_CHUNKS="3")
+    env = dict(os.environ, VIT_HOST_SPLIT="1,2,1")
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        cwd=os.path.dirname(os.path.dirname(__file__)), timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr

@@ -971,18 +971,49 @@ int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* 
 }
 
 // vit_block_host cuts the batch into chunks of whole sequences so that copies in, blocks
-// and copies out of successive chunks overlap on three streams. Chunks keep at least
-// 12,288 tokens (enough rows to fill the GEMMs' tiles); at most 8. VIT_HOST_CHUNKS=k
-// forces k (1: one chunk on the caller's stream).
-int64_t host_chunks(int64_t N, int64_t T) {
-    static const int64_t forced = [] {
-        const char* e = std::getenv("VIT_HOST_CHUNKS");
-        return e ? (int64_t)std::atoll(e) : (int64_t)0;
+// and copies out of successive chunks overlap on three streams. A block on fewer rows
+// fills the GPU less well, so the chunks are few and the first and last (whose copies
+// cannot be hidden) are the smallest: one chunk per 12,288 tokens, at most 4, with weights
+// 1, 1 / 1, 2, 1 / 1, 3, 3, 1 (the best of the schedules measured for 256 ViT-B/16
+// sequences). VIT_HOST_SPLIT="w1,w2,..." sets the weights ("1": one chunk on the caller's
+// stream).
+std::vector<int64_t> host_chunks(int64_t N, int64_t T) {
+    static const std::vector<double> forced = [] {
+        std::vector<double> w;
+        const char* e = std::getenv("VIT_HOST_SPLIT");
+        while (e && *e) {
+            char* end = nullptr;
+            const double v = std::strtod(e, &end);
+            if (end == e || !(v > 0)) return std::vector<double>();
+            w.push_back(v);
+            e = *end == ',' ? end + 1 : end;
+            if (*end != ',' && *end != 0) return std::vector<double>();
+        }
+        return w;
     }();
-    int64_t c = forced > 0 ? forced : (N * T) / 12288;
-    if (c > 8 && forced <= 0) c = 8;
-    if (c > N) c = N;
-    return c < 1 ? 1 : c;
+    std::vector<double> w = forced;
+    if (w.empty()) {
+        int64_t c = (N * T) / 12288;
+        if (c > 4) c = 4;
+        if (c < 1) c = 1;
+        for (int64_t i = 0; i < c; ++i) w.push_back(c > 2 && (i == 0 || i == c - 1) ? 1.0 : c - 1.0);
+    }
+    if ((int64_t)w.size() > N) w.resize((size_t)N);
+    double tot = 0;
+    for (double v : w) tot += v;
+    std::vector<int64_t> sizes;
+    int64_t used = 0;
+    double acc = 0;
+    for (size_t i = 0; i < w.size(); ++i) {
+        acc += w[i];
+        int64_t upto = i + 1 == w.size() ? N : (int64_t)(N * acc / tot + 0.5);
+        const int64_t left = (int64_t)(w.size() - i - 1);
+        if (upto > N - left) upto = N - left;   // every later chunk keeps a sequence
+        if (upto < used + 1) upto = used + 1;
+        sizes.push_back(upto - used);
+        used = upto;
+    }
+    return sizes;
 }
 
 // The device's three pipeline streams, created on first use (non-blocking).
@@ -1162,7 +1193,8 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
         if (i < 13 && !src[i]) continue;
         total += round_up(sizes[i], 256);
     }
-    const int64_t chunks = host_chunks(N, T);
+    const std::vector<int64_t> chunk_n = host_chunks(N, T);
+    const int64_t chunks = (int64_t)chunk_n.size();
     cudaStream_t sh = s, sc = s, sd = s;   // copy-in, compute, copy-out
     if (chunks > 1) {
         rc = pipeline_streams(st);
@@ -1202,7 +1234,7 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
     const size_t seq_bytes = (size_t)(T * D) * es;
     int64_t n0 = 0;
     for (int64_t c = 0; c < chunks && e == cudaSuccess && rc == VIT_OK; ++c) {
-        const int64_t nc = N / chunks + (c < N % chunks ? 1 : 0);
+        const int64_t nc = chunk_n[(size_t)c];
         const size_t o = (size_t)n0 * seq_bytes, nbytes = (size_t)nc * seq_bytes;
         e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(x_host) + o, nbytes,
                             cudaMemcpyHostToDevice, sh);
