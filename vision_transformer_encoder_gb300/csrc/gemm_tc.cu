@@ -491,10 +491,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
         p.parts_out[(int64_t)row * p.parts_stride + part_index] = make_float2(cmean, cm2);
 }
 
-// Ring depth and epilogue staging per output type: a bf16 staging tile is half the size
-// of an fp32 one, which leaves room for a sixth ring stage.
-template <typename OutT> struct PairCfg {
-    static constexpr int STAGES = sizeof(OutT) == 2 ? 6 : 5;
+// Ring depth and epilogue staging per epilogue and output type: a bf16 staging tile is
+// half the size of an fp32 one, which leaves room for a sixth ring stage; epilogues that
+// read a residual keep five (their residual loads go through L1, which gets the shared
+// memory the sixth stage would take).
+template <int EPI, typename OutT> struct PairCfg {
+    static constexpr int STAGES = sizeof(OutT) == 2 && EPI != TC_EPI_RESID ? 6 : 5;
     static constexpr int STAGE_TILE = sizeof(OutT) == 2 ? 32 * 64 : 32 * 128;
 };
 constexpr int P_EPI_WARPS = 8;
@@ -504,11 +506,11 @@ constexpr int P_A_BYTES = BM * BK * 2;          // 16 KB: this CTA's 128 rows
 constexpr int P_B_BYTES = (BN / 2) * BK * 2;    // 16 KB: this CTA's 128 weight columns
 constexpr int P_STAGE_BYTES = P_A_BYTES + P_B_BYTES;
 constexpr int P_EPI_BUFS = 1;   // staging tiles per epilogue warp
-template <typename OutT> __host__ __device__ constexpr int pair_epi_bytes() {
-    return P_EPI_WARPS * P_EPI_BUFS * PairCfg<OutT>::STAGE_TILE;
+template <int EPI, typename OutT> __host__ __device__ constexpr int pair_epi_bytes() {
+    return P_EPI_WARPS * P_EPI_BUFS * PairCfg<EPI, OutT>::STAGE_TILE;
 }
-template <typename OutT> __host__ __device__ constexpr int pair_smem_bytes() {
-    return PairCfg<OutT>::STAGES * P_STAGE_BYTES + pair_epi_bytes<OutT>() + BAR_BYTES + 1024;
+template <int EPI, typename OutT> __host__ __device__ constexpr int pair_smem_bytes() {
+    return PairCfg<EPI, OutT>::STAGES * P_STAGE_BYTES + pair_epi_bytes<EPI, OutT>() + BAR_BYTES + 1024;
 }
 
 template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
@@ -517,15 +519,15 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOut2,
                     const Params p) {
-    constexpr int P_STAGES = PairCfg<OutT>::STAGES;
-    constexpr int P_STG = PairCfg<OutT>::STAGE_TILE;
+    constexpr int P_STAGES = PairCfg<EPI, OutT>::STAGES;
+    constexpr int P_STG = PairCfg<EPI, OutT>::STAGE_TILE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + P_STAGES * P_A_BYTES;
     uint8_t* sEpi = smem + P_STAGES * P_STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + pair_epi_bytes<OutT>());
+    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + pair_epi_bytes<EPI, OutT>());
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
@@ -781,11 +783,11 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const C
     auto k = gemm_tc_pair_kernel<EPI, OutT, ResT, FOLD, EXTRA>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<OutT>());
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<EPI, OutT>());
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, P_THREADS, pair_smem_bytes<OutT>(), s>>>(a, b[0], b[1], b[2], out, out2, p);
+    k<<<grid, P_THREADS, pair_smem_bytes<EPI, OutT>(), s>>>(a, b[0], b[1], b[2], out, out2, p);
     return cudaGetLastError();
 }
 
