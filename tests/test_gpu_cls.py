@@ -85,6 +85,21 @@ def test_block_cls_vit_b16_full_size(dtype):
     assert err <= TOL[dtype]
 
 
+@pytest.mark.parametrize("shape", [(64, 577, 1024, 16, 4096), (32, 1025, 1280, 16, 5120)])
+def test_block_cls_vit_l_and_h_full_size(shape):
+    # ViT-L/16 at 384 px (577 tokens) and ViT-H/14 at 448 px (1025 tokens, head width 80):
+    # the full batches, four sequences recomputed by the oracle
+    d = _dev()
+    N, T, D, H, F = shape
+    x, lay = _block_case(N, T, D, H, F, torch.bfloat16, seed=T)
+    got = api.vit_block_cls(x.to(d), _to(lay, d), H, 1e-6).double().cpu().numpy()
+    rows = [0, 1, N // 2, N - 1]
+    err = float(np.abs(got[rows] - _oracle_block(x, lay, H, 1e-6, rows=rows)).max())
+    print("cls block %s max err %.3g" % (shape, err))
+    assert np.isfinite(got).all()
+    assert err <= TOL[torch.bfloat16]
+
+
 def test_block_cls_is_row0_of_the_block():
     # the readout against the whole block run through the library: same inputs, row 0
     d = _dev()
