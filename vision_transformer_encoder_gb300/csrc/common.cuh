@@ -72,6 +72,50 @@ __device__ __forceinline__ float gelu_tanh_fast(float z) {
     return fmaf(hz, tanh_approx(u), hz);
 }
 
+// Packed fp32 pairs (f32x2 arithmetic of sm_100 and later): one instruction computes two
+// lanes, each rounded exactly as the scalar instruction would, so results are bit for bit
+// those of the scalar code while the epilogues issue half the arithmetic instructions.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long x, unsigned long long y) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long x, unsigned long long y) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+// a += c, b += d
+__device__ __forceinline__ void f2_add_to(float& a, float& b, float c, float d) {
+    f2_unpack(f2_add(f2_pack(a, b), f2_pack(c, d)), a, b);
+}
+// gelu_tanh_fast of a and b, the same operations lane by lane
+__device__ __forceinline__ void gelu_tanh_fast2(float& a, float& b) {
+    const unsigned long long k0 = f2_pack(0.7978845608028654f, 0.7978845608028654f);
+    const unsigned long long k0k1 = f2_pack(0.7978845608028654f * 0.044715f, 0.7978845608028654f * 0.044715f);
+    const unsigned long long half = f2_pack(0.5f, 0.5f);
+    const unsigned long long z = f2_pack(a, b);
+    const unsigned long long u = f2_mul(z, f2_fma(k0k1, f2_mul(z, z), k0));
+    const unsigned long long hz = f2_mul(half, z);
+    float u0, u1;
+    f2_unpack(u, u0, u1);
+    f2_unpack(f2_fma(hz, f2_pack(tanh_approx(u0), tanh_approx(u1)), hz), a, b);
+}
+
 // Accurate forms (library tanh) for the fp32 / fp64 paths.
 __device__ __forceinline__ float gelu_tanh_acc(float z) {
     const float k0 = 0.7978845608028654f;

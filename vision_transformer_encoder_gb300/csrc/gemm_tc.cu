@@ -428,14 +428,14 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
                 float b[32];
                 load32(p.bias + col, b);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] += b[j];
+                for (int j = 0; j < 32; j += 2) f2_add_to(val[j], val[j + 1], b[j], b[j + 1]);
             }
             if (EPI == TC_EPI_GELU) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
+                for (int j = 0; j < 32; j += 2) gelu_tanh_fast2(val[j], val[j + 1]);
             } else if (EPI == TC_EPI_RESID) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] += rv[j];
+                for (int j = 0; j < 32; j += 2) f2_add_to(val[j], val[j + 1], rv[j], rv[j + 1]);
             }
         }
         if (EPI == TC_EPI_RESID && c + 1 < CHUNKS) {
@@ -698,7 +698,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 n0 + half * 128, lane, (n0 / BN) * 2 + half, p.ksplit > 1 ? ks : -1);
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive_cluster(tempty0 + acc * 8);
+            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(tempty0 + acc * 8);   // orders TMEM reads only
         }
         if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }

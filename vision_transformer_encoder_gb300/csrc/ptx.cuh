@@ -335,6 +335,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Relaxed variant: no release ordering of this thread's earlier memory writes (whose
+// completion the release form waits for, including global stores still in flight). For
+// hand-offs that only order tensor-memory accesses, which tcgen05 fences and waits order.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 // 2-D tile load into this CTA's shared memory whose byte count completes on an mbarrier
 // that may sit in the peer CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* tm,
