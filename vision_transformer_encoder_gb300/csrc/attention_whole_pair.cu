@@ -116,12 +116,16 @@ __device__ __forceinline__ float wp_chunk_max(const uint32_t (&v)[W], float m) {
 
 template <int W>
 __device__ __forceinline__ void wp_chunk_exp(const uint32_t (&v)[W], float sl2, float m, uint32_t (&pk)[W / 2],
-                                             float (&ls)[8]) {
+                                   unsigned long long (&ls)[4]) {
+    // exponent arguments and the row sums in packed fp32 pairs: half the instructions
+    const unsigned long long s2 = f2_pack(sl2, sl2), nm = f2_pack(-m, -m);
 #pragma unroll
     for (int e = 0; e < W; e += 2) {
-        const float p0 = exp2_approx(fmaf(__uint_as_float(v[e]), sl2, -m));
-        const float p1 = exp2_approx(fmaf(__uint_as_float(v[e + 1]), sl2, -m));
-        ls[(e >> 1) & 7] += p0 + p1;
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), s2, nm), x0, x1);
+        const float p0 = exp2_approx(x0);
+        const float p1 = exp2_approx(x1);
+        ls[(e >> 1) & 3] = f2_add(ls[(e >> 1) & 3], f2_pack(p0, p1));
         pk[e >> 1] = pack_bf16x2(p0, p1);
     }
 }
@@ -356,7 +360,7 @@ attention_whole_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
             if (live) {
                 const float m = fmaxf(mx, mx_other[row]) * sl2;
                 // pass 2: P over this half's consumed S columns
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};   // packed pairs of +0.0f
 #pragma unroll
                 for (int c = 0; c < 7; ++c) {
                     const int cc = c0 + c;
@@ -378,8 +382,14 @@ attention_whole_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __gri
                     ptx::tmem_st_32x32b_x8(tS + pbase + (c1 - c0) * 16, pk0);
                 }
                 ptx::tmem_st_wait();
-                sL[((u & 3) * 2 + half) * WP_ROWS + row] =
-                    ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                sL[((u & 3) * 2 + half) * WP_ROWS + row] = [&] {
+                    float a[8];
+                    f2_unpack(ls[0], a[0], a[1]);
+                    f2_unpack(ls[1], a[2], a[3]);
+                    f2_unpack(ls[2], a[4], a[5]);
+                    f2_unpack(ls[3], a[6], a[7]);
+                    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+                }();
             }
             ptx::tc_fence_before();
             __syncwarp();
