@@ -494,14 +494,16 @@ EncodeTiledFn wp_encode_fn() {
 
 }  // namespace
 
-// VIT_ATTN_WHOLE_PAIR=0 keeps these shapes on the single-CTA whole-row kernel.
+// Opt-in (VIT_ATTN_WHOLE_PAIR=1): at T = 197 the pair kernel's cross-CTA hand-offs (the
+// O slot and P of both CTAs must be released to the even CTA's MMA issuer) cost about what
+// its faster MMAs save, and the single-CTA kernel measures 2-3 % faster.
 bool attention_whole_pair_supported(int64_t T, int64_t D, int64_t H, const DeviceInfo& dev) {
     if (H <= 0 || D % H != 0 || D / H != WP_DH || T < 1 || T > WP_MAX_KEYS || dev.num_sms < 2) return false;
-    static const bool off = [] {
+    static const bool on = [] {
         const char* e = std::getenv("VIT_ATTN_WHOLE_PAIR");
-        return e && e[0] == '0';
+        return e && e[0] == '1';
     }();
-    return !off && wp_encode_fn() != nullptr;
+    return on && wp_encode_fn() != nullptr;
 }
 
 cudaError_t launch_attention_whole_pair(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
