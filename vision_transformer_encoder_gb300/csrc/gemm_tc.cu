@@ -340,6 +340,15 @@ template <> struct StageIO<float> {
             *reinterpret_cast<float4*>(row + ((u ^ (r & 7)) << 4)) =
                 make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
     }
+    // the inverse: row r of a tile a TMA load wrote with the same swizzle
+    __device__ static void read(const uint8_t* buf, int r, float (&v)[32]) {
+        const uint8_t* row = buf + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float4 f = *reinterpret_cast<const float4*>(row + ((u ^ (r & 7)) << 4));
+            v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+        }
+    }
 };
 template <> struct StageIO<__nv_bfloat16> {
     static constexpr int ROW_BYTES = 64;
@@ -353,6 +362,17 @@ template <> struct StageIO<__nv_bfloat16> {
             w.z = pack_bf16x2(v[8 * u + 4], v[8 * u + 5]);
             w.w = pack_bf16x2(v[8 * u + 6], v[8 * u + 7]);
             *reinterpret_cast<uint4*>(row + ((u ^ ((r >> 1) & 3)) << 4)) = w;
+        }
+    }
+    __device__ static void read(const uint8_t* buf, int r, float (&v)[32]) {
+        const uint8_t* row = buf + r * 64;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const uint4 w = *reinterpret_cast<const uint4*>(row + ((u ^ ((r >> 1) & 3)) << 4));
+            const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y), c = unpack_bf16x2(w.z),
+                         d = unpack_bf16x2(w.w);
+            v[8 * u + 0] = a.x; v[8 * u + 1] = a.y; v[8 * u + 2] = b.x; v[8 * u + 3] = b.y;
+            v[8 * u + 4] = c.x; v[8 * u + 5] = c.y; v[8 * u + 6] = d.x; v[8 * u + 7] = d.y;
         }
     }
 };
@@ -371,6 +391,22 @@ template <typename T> __device__ __forceinline__ void load32f(const float* p, fl
         v[4 * i + 0] = u.x; v[4 * i + 1] = u.y; v[4 * i + 2] = u.z; v[4 * i + 3] = u.w;
     }
 }
+
+// Residual tiles through TMA (pair kernel): each epilogue warp keeps one 32 x 32 residual
+// tile in shared memory (the swizzle of StageIO). A chunk's tile is copied into registers
+// as soon as it lands, and the load of the next chunk's tile (or of the next output tile's
+// first one) is issued into the same buffer while the chunk is computed and stored.
+struct ResStream {
+    const CUtensorMap* tm = nullptr;
+    uint8_t* buf = nullptr;
+    uint64_t* bar = nullptr;
+    volatile int* abort = nullptr;
+    uint32_t phase = 0;
+    int inflight = 0;          // loads issued and not yet waited for (0 or 1)
+    bool failed = false;       // a wait ran out: no further loads, residual values invalid
+    bool next = false;         // after the last chunk, load the next output tile's first
+    int next_col = 0, next_row0 = 0;
+};
 
 // Mean and 1/sqrt(var + eps) of one row from its partials (mean_k, M2_k) over column
 // ranges of part_cols (the last one may be shorter), merged with Chan's formula.
@@ -396,13 +432,13 @@ __device__ __forceinline__ float2 merge_row_stats(const TcLnFold& f, int row) {
 // current one is processed. With EXTRA, the same values are also stored as bf16 through
 // tmOut2 and the row's (mean, M2) over these columns is written to p.parts_out.
 template <int EPI, typename OutT, typename ResT, int CHUNKS, int BUFS, bool FOLD, bool EXTRA,
-          int STG = EPI_STAGE_BYTES>
+          int STG = EPI_STAGE_BYTES, bool RES_TMA = false>
 __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtensorMap* tmOut,
                                                   const CUtensorMap* tmOut2, uint8_t* stage,
                                                   uint32_t t_row, int row, int row0, int n0,
-                                                  int lane, int part_index, int zk = -1) {
+                                                  int lane, int part_index, int zk, ResStream& rs) {
     float rv[32];
-    epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
+    if (!RES_TMA) epilogue_prefetch<EPI, ResT>(p, row, n0, rv);
     float2 st = make_float2(0.f, 1.f);
     if (FOLD && row < p.M) st = merge_row_stats(p.fold, row);
     float cnt = 0.f, cmean = 0.f, cm2 = 0.f;   // EXTRA: running statistics of this row
@@ -412,7 +448,34 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
         ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
         const int col = n0 + c * 32;
         float rnext[32];
-        if (c + 1 < CHUNKS) epilogue_prefetch<EPI, ResT>(p, row, col + 32, rnext);
+        if constexpr (RES_TMA) {
+            if (!rs.failed) {
+                const bool landed = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(rs.bar, rs.phase, rs.abort));
+                rs.phase ^= 1;
+                rs.inflight = 0;
+                if (!landed) {
+                    rs.failed = true;
+                    if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
+                    *rs.abort = 1;
+                }
+            }
+            StageIO<ResT>::read(rs.buf, lane, rv);
+            ptx::fence_proxy_async_smem();   // these reads before the next copy into the buffer
+            __syncwarp();
+            const bool more = c + 1 < CHUNKS || rs.next;
+            if (more && !rs.failed) {
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(rs.bar, 32 * StageIO<ResT>::ROW_BYTES);
+                    if (c + 1 < CHUNKS)
+                        ptx::tma_load_2d(rs.buf, rs.tm, rs.bar, col + 32, row0);
+                    else
+                        ptx::tma_load_2d(rs.buf, rs.tm, rs.bar, rs.next_col, rs.next_row0);
+                }
+                rs.inflight = 1;
+            }
+        } else if (c + 1 < CHUNKS) {
+            epilogue_prefetch<EPI, ResT>(p, row, col + 32, rnext);
+        }
         ptx::tmem_ld_wait();
         float val[32];
 #pragma unroll
@@ -438,7 +501,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
                 for (int j = 0; j < 32; j += 2) f2_add_to(val[j], val[j + 1], rv[j], rv[j + 1]);
             }
         }
-        if (EPI == TC_EPI_RESID && c + 1 < CHUNKS) {
+        if (EPI == TC_EPI_RESID && !RES_TMA && c + 1 < CHUNKS) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) rv[j] = rnext[j];
         }
@@ -493,8 +556,7 @@ __device__ __forceinline__ void epilogue_tile_tma(const Params& p, const CUtenso
 
 // Ring depth and epilogue staging per epilogue and output type: a bf16 staging tile is
 // half the size of an fp32 one, which leaves room for a sixth ring stage; epilogues that
-// read a residual keep five (their residual loads go through L1, which gets the shared
-// memory the sixth stage would take).
+// read a residual keep five (their residual tiles take the shared memory of the sixth).
 template <int EPI, typename OutT> struct PairCfg {
     static constexpr int STAGES = sizeof(OutT) == 2 && EPI != TC_EPI_RESID ? 6 : 5;
     static constexpr int STAGE_TILE = sizeof(OutT) == 2 ? 32 * 64 : 32 * 128;
@@ -509,8 +571,13 @@ constexpr int P_EPI_BUFS = 1;   // staging tiles per epilogue warp
 template <int EPI, typename OutT> __host__ __device__ constexpr int pair_epi_bytes() {
     return P_EPI_WARPS * P_EPI_BUFS * PairCfg<EPI, OutT>::STAGE_TILE;
 }
-template <int EPI, typename OutT> __host__ __device__ constexpr int pair_smem_bytes() {
-    return PairCfg<EPI, OutT>::STAGES * P_STAGE_BYTES + pair_epi_bytes<EPI, OutT>() + BAR_BYTES + 1024;
+// one 32 x 32 residual tile per epilogue warp (residual epilogues)
+template <int EPI, typename ResT> __host__ __device__ constexpr int pair_res_tile() {
+    return EPI == TC_EPI_RESID ? 32 * StageIO<ResT>::ROW_BYTES : 0;
+}
+template <int EPI, typename OutT, typename ResT> __host__ __device__ constexpr int pair_smem_bytes() {
+    return PairCfg<EPI, OutT>::STAGES * P_STAGE_BYTES + pair_epi_bytes<EPI, OutT>() +
+           P_EPI_WARPS * pair_res_tile<EPI, ResT>() + BAR_BYTES + 1024;
 }
 
 template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
@@ -518,21 +585,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOut2,
-                    const Params p) {
+                    const __grid_constant__ CUtensorMap tmRes, const Params p) {
     constexpr int P_STAGES = PairCfg<EPI, OutT>::STAGES;
     constexpr int P_STG = PairCfg<EPI, OutT>::STAGE_TILE;
+    constexpr int RES_TILE = pair_res_tile<EPI, ResT>();
+    constexpr bool RES_TMA = EPI == TC_EPI_RESID;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + P_STAGES * P_A_BYTES;
     uint8_t* sEpi = smem + P_STAGES * P_STAGE_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + pair_epi_bytes<EPI, OutT>());
+    uint8_t* sRes = sEpi + pair_epi_bytes<EPI, OutT>();   // 1 KB aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(sRes + P_EPI_WARPS * RES_TILE);
     uint64_t* empty = full + P_STAGES;
     uint64_t* tfull = empty + P_STAGES;
     uint64_t* tempty = tfull + 2;
     uint64_t* done = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    uint64_t* rbar = done + 1;   // [epilogue warp]: residual tile landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + P_EPI_WARPS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -554,6 +625,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             ptx::mbar_init(tempty + a, 2 * P_EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
+        for (int e = 0; e < P_EPI_WARPS; ++e) ptx::mbar_init(rbar + e, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -564,6 +636,7 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
         ptx::prefetch_tensormap(&tmOut);
         if (EXTRA) ptx::prefetch_tensormap(&tmOut2);
+        if (RES_TMA) ptx::prefetch_tensormap(&tmRes);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -677,6 +750,23 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int quarter = warp & 3;               // TMEM lane quarter this warp may read
         const int half = (warp - 5) >> 2;           // which 128 of the 256 columns
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);  // leader's
+        // this warp's residual rows and columns of item w
+        auto res_row0 = [&](int w) { return ((w / p.ksplit) / n_tiles) * 2 * BM + (int)rank * BM + quarter * 32; };
+        auto res_col = [&](int w) { return ((w / p.ksplit) % n_tiles) * BN + half * 128; };
+        ResStream rs;
+        if constexpr (RES_TMA) {
+            rs.tm = &tmRes;
+            rs.buf = sRes + (warp - 5) * RES_TILE;
+            rs.bar = rbar + (warp - 5);
+            rs.abort = abort_flag;
+            if (cluster < num_items) {   // the first tile's first residual chunk
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(rs.bar, RES_TILE);
+                    ptx::tma_load_2d(rs.buf, rs.tm, rs.bar, res_col(cluster), res_row0(cluster));
+                }
+                rs.inflight = 1;
+            }
+        }
         int local = 0;
         for (int w = cluster; w < num_items; w += nclusters, ++local) {
             const int tile = w / p.ksplit, ks = w - tile * p.ksplit;
@@ -693,14 +783,26 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             ptx::tc_fence_after();
             const uint32_t t_row = tmem_base + acc * ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA, P_STG>(
+            if constexpr (RES_TMA) {
+                rs.next = w + nclusters < num_items;
+                if (rs.next) {
+                    rs.next_col = res_col(w + nclusters);
+                    rs.next_row0 = res_row0(w + nclusters);
+                }
+            }
+            epilogue_tile_tma<EPI, OutT, ResT, 4, P_EPI_BUFS, FOLD, EXTRA, P_STG, RES_TMA>(
                 p, &tmOut, &tmOut2, sEpi + (warp - 5) * P_EPI_BUFS * P_STG, t_row, row0 + lane, row0,
-                n0 + half * 128, lane, (n0 / BN) * 2 + half, p.ksplit > 1 ? ks : -1);
+                n0 + half * 128, lane, (n0 / BN) * 2 + half, p.ksplit > 1 ? ks : -1, rs);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster_relaxed(tempty0 + acc * 8);   // orders TMEM reads only
         }
         if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
+        if (RES_TMA && rs.inflight && !rs.failed) {
+            // a residual copy issued before an early exit lands before the CTA leaves
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(rs.bar, rs.phase, nullptr)) && lane == 0)
+                set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+        }
     }
 
     __syncthreads();
@@ -779,27 +881,29 @@ cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params
 
 template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
 cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
-                             const CUtensorMap& out2, const Params& p, int grid, cudaStream_t s) {
+                             const CUtensorMap& out2, const CUtensorMap& res, const Params& p, int grid,
+                             cudaStream_t s) {
     auto k = gemm_tc_pair_kernel<EPI, OutT, ResT, FOLD, EXTRA>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<EPI, OutT>());
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<EPI, OutT, ResT>());
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, P_THREADS, pair_smem_bytes<EPI, OutT>(), s>>>(a, b[0], b[1], b[2], out, out2, p);
+    k<<<grid, P_THREADS, pair_smem_bytes<EPI, OutT, ResT>(), s>>>(a, b[0], b[1], b[2], out, out2, res, p);
     return cudaGetLastError();
 }
 
 template <int EPI, typename OutT, typename ResT>
 cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
-                       const CUtensorMap& out2, const Params& p, int grid, cudaStream_t s) {
+                       const CUtensorMap& out2, const CUtensorMap& res, const Params& p, int grid,
+                       cudaStream_t s) {
     if (!pair) return launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
     if (p.fold.parts)
-        return launch_inst_pair<EPI, OutT, ResT, true, false>(a, b, out, out2, p, grid, s);
+        return launch_inst_pair<EPI, OutT, ResT, true, false>(a, b, out, out2, res, p, grid, s);
     if (p.parts_out)
-        return launch_inst_pair<EPI, OutT, ResT, false, true>(a, b, out, out2, p, grid, s);
-    return launch_inst_pair<EPI, OutT, ResT, false, false>(a, b, out, out2, p, grid, s);
+        return launch_inst_pair<EPI, OutT, ResT, false, true>(a, b, out, out2, res, p, grid, s);
+    return launch_inst_pair<EPI, OutT, ResT, false, false>(a, b, out, out2, res, p, grid, s);
 }
 
 // The CTA-pair kernel is the default; VIT_GEMM_PAIR=0 selects the single-CTA kernel.
@@ -970,6 +1074,12 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
         if (c.ksplit > 1 && (int64_t)c.ksplit * d.M * d.N * 4 <= d.split_ws_bytes) sk = c;
     }
     if (sk.ksplit > 1 && !make_map_split(&mo, d.split_ws, d.M, d.N, sk.ksplit)) return cudaErrorInvalidValue;
+    // residual tiles for the pair kernel's TMA-fed residual epilogue (same boxes and swizzle
+    // as the output staging tiles)
+    alignas(64) CUtensorMap mres = mo;
+    if (pair && d.epi == TC_EPI_RESID && sk.ksplit == 1 &&
+        !make_map_out(&mres, const_cast<void*>(d.residual), d.M, d.N, d.ldr, d.residual_f32))
+        return cudaErrorInvalidValue;
     Params p;
     p.M = (int)d.M;
     p.N = (int)d.N;
@@ -998,7 +1108,7 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     }
     if (sk.ksplit > 1) {
         p.bias = nullptr;
-        cudaError_t e = launch_any<TC_EPI_STORE, float, float>(true, ma, mb, mo, mo2, p, grid, s);
+        cudaError_t e = launch_any<TC_EPI_STORE, float, float>(true, ma, mb, mo, mo2, mres, p, grid, s);
         if (e != cudaSuccess) return e;
         switch (d.epi) {
             case TC_EPI_STORE:
@@ -1020,19 +1130,19 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     }
     switch (d.epi) {
         case TC_EPI_STORE:
-            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
-                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
+                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s);
         case TC_EPI_GELU:
-            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
-                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
+                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s);
         case TC_EPI_RESID:
             if (d.out_f32)
                 return d.residual_f32
-                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, mo2, p, grid, s)
-                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, mo2, p, grid, s);
+                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
+                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, mo2, mres, p, grid, s);
             return d.residual_f32
-                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, p, grid, s)
-                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, mo2, p, grid, s);
+                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
+                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, mo2, mres, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
