@@ -34,6 +34,12 @@ from vision_transformer_encoder_gb300 import api  # noqa: E402
 from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs, make_encoder_inputs  # noqa: E402
 
 METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf16, 1 GPU"
+METRIC_F32 = "ViT block tokens/s and TFLOP/s at ViT-B/16 fp32 (3xTF32 tensor-core products), 1 GPU"
+# fp32 path: its products are three TF32 tensor-core products each, so its contraction peak
+# is the measured bf16 peak x the nominal TF32 / BF16 dense ratio (1.1 / 2.25) / 3; its
+# attention runs on the CUDA cores: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz.
+TF32X3_OF_BF16 = (1.1 / 2.25) / 3.0
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
 PATCH_METRIC = "ViT patch-embedding front end tokens/s at ViT-B/16 width bf16, 1 GPU"
 ENCODER_METRIC = "ViT encoder (%d blocks + final LN) tokens/s at ViT-B/16 width bf16, 1 GPU"
@@ -64,10 +70,23 @@ def cls_flops_per_step(c):
     return 2 * N * T * D * 2 * D + 2 * N * (2 * D * D + 2 * D * F) + 4 * N * T * D
 
 
-def kernel_work(c):
-    """Algorithmic work per launch of each kernel: (bound, amount, unit)."""
+def kernel_work(c, f32=False):
+    """Algorithmic work per launch of each kernel: (bound, amount, unit). f32: the fp32
+    path (fp32 activations, 3xTF32 products, CUDA-core attention)."""
     N, T, D, F = c["N"], c["T"], c["D"], c["F"]
     M = N * T
+    if f32:
+        return {
+            "ln1": ("hbm", M * D * (4 + 4), "bytes"),
+            "qkv_gemm": ("tensor", 2 * M * D * 3 * D, "flops"),
+            "attention": ("alu", 4 * N * T * T * D, "flops"),
+            "wo_gemm_residual": ("tensor", 2 * M * D * D, "flops"),
+            "ln2": ("hbm", M * D * (4 + 4), "bytes"),
+            "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),
+            "w2_gemm_residual": ("tensor", 2 * M * F * D, "flops"),
+            # weights read once, written twice (transposed high and low parts)
+            "tf32_weight_split": ("hbm", (4 * D * D + 2 * D * F) * 4 * 3, "bytes"),
+        }
     return {
         "ln1": ("hbm", M * D * (2 + 2), "bytes"),          # read x bf16, write xn bf16
         "qkv_gemm": ("tensor", 2 * M * D * 3 * D, "flops"),
@@ -294,6 +313,8 @@ def main():
     ap.add_argument("--encoder-layers", type=int, default=0,
                     help="time vit_encoder: this many blocks with Q/K/V/O biases, LN affine "
                          "terms and the final LayerNorm, instead of one block")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "f32"],
+                    help="f32: time the fp32 path of the block (3xTF32 products)")
     ap.add_argument("--cls-only", action="store_true",
                     help="the last block computes the CLS rows alone: vit_block_cls (with "
                          "--encoder-layers 0) or vit_encoder_cls")
@@ -310,7 +331,10 @@ def main():
         c["N"] = args.n_seq
     H, eps = c["H"], c["eps"]
     dev = torch.device("cuda", torch.cuda.current_device())
-    inp = make_config_inputs(name, seed=rank, dtype=torch.bfloat16, N=c["N"])
+    f32 = args.dtype == "f32"
+    if f32 and (args.patch_embed or args.cls_only or args.encoder_layers):
+        ap.error("--dtype f32 times the single block only")
+    inp = make_config_inputs(name, seed=rank, dtype=torch.float32 if f32 else torch.bfloat16, N=c["N"])
     d = inp.to(device=dev)
     out = torch.empty_like(d.x)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -408,17 +432,24 @@ def main():
         return 0
 
     peaks, peak_src = load_peaks()
-    work = kernel_work(c)
+    work = kernel_work(c, f32)
     per_kernel = {k: v for k, v in per_kernel.items() if v[1] > 0}
     dom = max(per_kernel, key=lambda k: per_kernel[k][0])
     kms, kn = per_kernel[dom]
     bound, amount, _unit = work[dom]
     avg_s = kms / kn / 1e3
-    traffic = load_traffic().get(dom)
+    # the committed DRAM counters were taken on the bf16 path's kernels
+    traffic = None if f32 else load_traffic().get(dom)
+    tc_scale = TF32X3_OF_BF16 if f32 else 1.0   # contraction peak of this path's dtype
     if bound == "tensor":
-        peak = peaks["bf16_tflops"]
+        peak = peaks["bf16_tflops"] * tc_scale
         achieved = amount / avg_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak}
+    elif bound == "alu":
+        peak = FP32_ALU_TFLOPS
+        achieved = amount / avg_s / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak}
     else:
         peak = peaks["hbm_gbs"]
@@ -428,8 +459,12 @@ def main():
     roof.update({"traffic": traffic, "kernel": dom, "launches": kn,
                  "avg_launch_us": avg_s * 1e6,
                  "algorithmic_per_launch": amount,
-                 "peak_source": "%s (%s)" % (peak_src, "bf16 burst" if bound == "tensor" else "copy"),
-                 "frac_of_sustained": (achieved / peaks["bf16_tflops_sustained"]
+                 "peak_source": ("%s (%s)" % (peak_src, "bf16 burst" if not f32 else
+                                              "bf16 burst x 1.1 / 2.25 TF32/BF16 nominal / 3 products")
+                                 if bound == "tensor" else
+                                 "%s (copy)" % peak_src if bound == "hbm" else
+                                 "152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz"),
+                 "frac_of_sustained": (achieved / (peaks["bf16_tflops_sustained"] * tc_scale)
                                        if bound == "tensor" else None)})
     if args.patch_embed:
         step_flops = 2 * c["N"] * 196 * 768 * c["D"]
@@ -454,7 +489,7 @@ def main():
         workload = ("%d-block encoder (Q/K/V/O and MLP biases, LN gains, final LayerNorm) of %s"
                     % (L, workload_name(name, c)))
     else:
-        metric, workload = METRIC, workload_name(name, c)
+        metric, workload = (METRIC_F32 if f32 else METRIC), workload_name(name, c)
     step_tflops = step_flops / (ms_per_step / 1e3) / 1e12
     kernels = {k: {"avg_us": 1e3 * v[0] / v[1] if v[1] else None, "launches": v[1],
                    "share": v[0] / sum(x[0] for x in per_kernel.values())}
@@ -464,15 +499,15 @@ def main():
         "value": value, "unit": UNIT,
         "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
         "config": {"workload": workload,
                    "tokens_per_step_per_gpu": tokens,
-                   "inputs": "seeded synthetic: x ~ N(0,1), weights ~ N(0, 1/fan_in), bf16",
+                   "inputs": "seeded synthetic: x ~ N(0,1), weights ~ N(0, 1/fan_in), %s" % args.dtype,
                    "l2": "512 MiB written between timed steps (flush); per-step working set "
                          "about 0.9 GB, larger than L2",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tflops": step_tflops,
-        "frac_of_peak": step_tflops / peaks["bf16_tflops"],
+        "frac_of_peak": step_tflops / (peaks["bf16_tflops"] * (TF32X3_OF_BF16 if f32 else 1.0)),
         "roofline": roof,
         "kernels": kernels,
         "gpu_launches": launches,
