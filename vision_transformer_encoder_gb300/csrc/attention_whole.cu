@@ -42,6 +42,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace vit {
@@ -173,6 +174,9 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
+    // the set-up above overlaps the previous kernel's tail; Q, K and V are its output
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp >= AW_LOAD_WARP) {
         if (lane == 0) {
@@ -496,8 +500,7 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
         attr = true;
     }
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
-    attention_whole_kernel<<<grid, AW_THREADS, AW_SMEM, s>>>(tm, p);
-    return cudaGetLastError();
+    return launch_dependent(attention_whole_kernel, dim3(grid), dim3(AW_THREADS), AW_SMEM, s, tm, p);
 }
 
 }  // namespace vit

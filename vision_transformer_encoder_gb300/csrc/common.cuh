@@ -22,6 +22,15 @@ enum : uint32_t {
 // seconds at 2 GHz; longer at lower clocks).
 constexpr long long kWaitTimeoutCycles = 4000000000ll;
 
+// Programmatic dependent launch (PTX griddepcontrol): griddep_wait blocks until the grids
+// this one depends on in its stream have completed and their memory writes are visible (a
+// no-op for a plain launch); griddep_launch_dependents lets the next launch in the stream,
+// if made with programmatic serialisation, schedule its CTAs from now on.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

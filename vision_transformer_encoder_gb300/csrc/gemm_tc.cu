@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace vit {
@@ -646,6 +647,9 @@ gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     ptx::cluster_sync();  // barriers of both CTAs initialised before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the set-up above overlaps the previous kernel's tail; A and the residual are its output
+    griddep_wait();
+    griddep_launch_dependents();
 
     // TMA issue from one thread is serialised (roughly one box at a time), so four warps
     // each issue one 64-row box per stage: A rows 0-63, A rows 64-127, weight columns
@@ -890,8 +894,8 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const C
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    k<<<grid, P_THREADS, pair_smem_bytes<EPI, OutT, ResT>(), s>>>(a, b[0], b[1], b[2], out, out2, res, p);
-    return cudaGetLastError();
+    return launch_dependent(k, dim3(grid), dim3(P_THREADS), pair_smem_bytes<EPI, OutT, ResT>(), s, a, b[0], b[1],
+                            b[2], out, out2, res, p);
 }
 
 template <int EPI, typename OutT, typename ResT>

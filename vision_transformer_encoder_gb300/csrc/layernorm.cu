@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace vit {
 namespace {
@@ -79,6 +80,8 @@ ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
                const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ beta,
                int64_t rows, int D, float eps) {
     constexpr int V = VecIO<TIn>::N;
+    griddep_wait();                 // x is the previous kernel's output
+    griddep_launch_dependents();
     const int64_t row = (int64_t)blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -186,11 +189,10 @@ template <typename TIn, int MAXV>
 cudaError_t launch_fast_v(const void* x, void* out, const void* g, const void* b, int64_t rows,
                           int64_t D, double eps, cudaStream_t s) {
     const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
-    ln_fast_kernel<TIn, MAXV><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
-        static_cast<const TIn*>(x), static_cast<__nv_bfloat16*>(out),
-        static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), rows, (int)D,
-        (float)eps);
-    return cudaGetLastError();
+    return launch_dependent(ln_fast_kernel<TIn, MAXV>, dim3((unsigned)blocks), dim3(LN_THREADS), 0, s,
+                            static_cast<const TIn*>(x), static_cast<__nv_bfloat16*>(out),
+                            static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), rows,
+                            (int)D, (float)eps);
 }
 
 template <typename TIn>
