@@ -131,6 +131,24 @@ def test_layernorm_wide_types(dtype):
     _close(out, oracle.layernorm(x, 1e-5), atol=tol, rtol=tol)
 
 
+def _close_attention(out, q, k, v, H):
+    """Bound from the bf16 arithmetic of the tensor-core attention kernels: each softmax
+    weight enters P V as P rounded to bf16 (unit roundoff 2^-8) under a common offset, the
+    row sum is taken before that rounding, and out is rounded to bf16 once, so per element
+    |out - ref| <= 2^-8 sum_j w_j |v_j| + 2^-8 |ref| (w the exact weights); fp32
+    accumulation over at most a few thousand keys adds well under 2^-14 of the same."""
+    ref = oracle.attention(q, k, v, H)
+    wabs = oracle.attention(q, k, v.abs(), H)
+    g = out.double().cpu().numpy()
+    assert np.isfinite(g).all(), "non-finite output (unwritten or overflowed element)"
+    err = np.abs(g - ref)
+    bound = (2.0 ** -8 + 2.0 ** -14) * (wabs + np.abs(ref)) + 1e-6
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert (err <= bound).all(), "max excess at %s: gpu %g ref %g bound %g" % (
+        worst, g[worst], ref[worst], bound[worst])
+    return float((err / bound).max())
+
+
 @pytest.mark.parametrize("N,T,D,H", [(2, 197, 128, 2), (1, 65, 64, 1), (3, 77, 160, 2),
                                      (1, 1, 64, 1), (2, 129, 256, 4), (1, 300, 96, 3),
                                      (2, 577, 128, 2), (1, 1025, 160, 2), (3, 256, 64, 1),
@@ -143,8 +161,30 @@ def test_attention_bf16(N, T, D, H):
     out = api.attention(qkv.to(d), H)
     torch.cuda.synchronize()
     q, k, v = qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:]
-    ref = oracle.attention(q, k, v, H)
-    _close(out, ref, atol=4e-3, rtol=2.0 ** -6)
+    print("attention %s: max err / bound %.3f" % ((N, T, D, H), _close_attention(out, q, k, v, H)))
+
+
+@pytest.mark.parametrize("T", [197, 224, 40, 100])
+def test_attention_bf16_dominant_later_keys(T):
+    # Keys scaled up so that, for many query rows, a key past the first 32 scores far
+    # above every key in [0, 32): in the first half of the keys, in the second half, in
+    # the 16-key tail, and by thousands (every earlier term underflows). Softmax is the
+    # same under any common offset, so the result must match the oracle exactly as for
+    # ordinary scores.
+    d = _dev()
+    N, D, H = 3, 128, 2
+    qkv = _rand((N, T, 3 * D), 70 + T, std=1.5)
+    k = qkv[..., D:2 * D].view(N, T, H, 64)
+    spikes = [(0, 0, 50, 10.0), (0, 1, 150, 10.0), (1, 0, 200, 10.0), (1, 0, 100, 30.0),
+              (1, 1, 60, 1000.0), (1, 1, 170, 1000.0), (2, 0, 33, -1000.0), (2, 1, 120, 6.0)]
+    for n, h, t, a in spikes:
+        if t < T:
+            k[n, t, h] *= a
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    q, k, v = qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:]
+    print("dominant keys T=%d: max err / bound %.3f" % (T, _close_attention(out, q, k, v, H)))
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float64])

@@ -7,18 +7,24 @@
 //
 // With T <= 224, all keys of a query row fit in one S tile: S = Q K^T for 128 query
 // rows is a single M 128 x N ns MMA chain (ns = T rounded up to 16), so the row maximum
-// is known before any exponent is taken. The softmax is one exact pass per row -- no
-// running maximum, no rescaling of O -- and O = P V is one MMA chain over ns keys.
+// is in TMEM before any exponent is taken. The softmax is one pass per row with no
+// rescaling of O, and O = P V is one MMA chain over ns keys.
 //
 // A unit is (sequence, head, 128-row query tile); the units of one (sequence, head)
 // item share its K and V. Persistent kernel, one CTA per SM, 24 warps:
 //   warps 0-7 / 8-15  softmax of even / odd units. Two warps per TMEM lane quarter
 //                    split the keys of their 32 rows: warp "half" 0 takes the first
-//                    `split` keys, half 1 the rest. Pass 1: each takes the maximum over
-//                    its valid keys, and the pair exchange it through shared memory.
-//                    Pass 2: P = exp2(S log2(e)/sqrt(dh) - max) in bf16, written into the
-//                    half's own S columns already consumed (32 keys fill 16 columns),
-//                    and the half's row sum to shared memory.
+//                    `split` keys, half 1 the rest. One pass over S: P = exp2(S
+//                    log2(e)/sqrt(dh) - r) in bf16, written into the half's own S columns
+//                    already consumed (32 keys fill 16 columns), and the half's row sum to
+//                    shared memory. Softmax is unchanged by any common offset r; r starts
+//                    as the maximum over keys [0, 32), which both halves read, and a half
+//                    raises its own r, by whole log2 units, only when a chunk's maximum
+//                    passes r by more than 8 (so P <= 2^8); the P it has written is then
+//                    rescaled by an exact power of two. At the end the two halves take the
+//                    larger of their offsets (a named barrier per quarter); the one below
+//                    rescales. With typical scores no chunk passes the start by 8 and the
+//                    row costs one read of S, each P rounded once.
 //   warps 16-19      epilogue, one per TMEM lane quarter: O into registers, O's slot
 //                    released at once, then O / (l0 + l1) in bf16 to global memory.
 //   warp 20          TMEM owner and MMA issuer. MMA stream: S(0), S(1), PV(0), S(2),
@@ -78,7 +84,6 @@ struct AwParams {
 struct AwBars {
     uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], l_full[4];
-    uint64_t mx_full[2][4];   // [group][lane quarter]: both halves' maxima written
     uint64_t o_done, o_free, done;
     uint32_t tmem_slot;
     int abort_flag;
@@ -128,6 +133,80 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&v)[W], float sl2, flo
     }
 }
 
+// An offset is raised only when a chunk's maximum passes it by more than this (log2
+// units), so P stays at most 2^kRaise and is seldom rescaled.
+constexpr float kRaise = 8.f;
+
+// 2^k for an integer-valued k <= 0, exactly (0 below the normal range).
+__device__ __forceinline__ float pow2_int(float k) {
+    return k < -126.f ? 0.f : __int_as_float(((int)k + 127) << 23);
+}
+
+__device__ __forceinline__ void f2_scale(unsigned long long (&ls)[4], float f) {
+    const unsigned long long ff = f2_pack(f, f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ls[i] = f2_mul(ls[i], ff);
+}
+
+// Multiplies the bf16 P this thread's half has written -- `full` 16-column chunks from
+// tP on, then 8 columns if `tail` -- by f, a power of two <= 1 (exact but for values
+// pushed below the normal range). Rare: only when an offset changes.
+__device__ __noinline__ void rescale_p(uint32_t tP, int full, bool tail, float f) {
+    ptx::tmem_st_wait();   // the P stores being read back have landed
+    for (int i = 0; i < full; ++i) {
+        uint32_t r[16];
+        ptx::tmem_ld_32x32b_x16(tP + i * 16, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float2 a = unpack_bf16x2(r[e]);
+            r[e] = pack_bf16x2(a.x * f, a.y * f);
+        }
+        ptx::tmem_st_32x32b_x16(tP + i * 16, r);
+    }
+    if (tail) {
+        uint32_t r[8];
+        ptx::tmem_ld_32x32b_x8(tP + full * 16, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 a = unpack_bf16x2(r[e]);
+            r[e] = pack_bf16x2(a.x * f, a.y * f);
+        }
+        ptx::tmem_st_32x32b_x8(tP + full * 16, r);
+    }
+}
+
+// P of W keys (maximum cm, masked keys at -inf) for chunk j of this half: if cm sl2
+// passes the offset by more than kRaise, raises the offset by the whole number of log2
+// units that brings it to cm sl2 or above (the partial row sums and, after this chunk,
+// the P already written are scaled by the exact power of two), then writes
+// exp2(s sl2 - mrun) in bf16 to the W / 2 columns from tP + 16 j.
+template <int W>
+__device__ __forceinline__ void p_chunk(const uint32_t (&v)[W], float cm, float sl2, float& mrun,
+                                        unsigned long long (&ls)[4], uint32_t tP, int j) {
+    const float cms = cm * sl2;
+    const bool up = cms > mrun + kRaise;
+    const bool any_up = __any_sync(0xffffffffu, up);
+    float f = 1.f;
+    if (any_up) {
+        const float n = up ? ceilf(cms - mrun) : 0.f;
+        f = pow2_int(-n);
+        f2_scale(ls, f);
+        mrun += n;
+    }
+    {
+        uint32_t pk[W / 2];
+        chunk_exp(v, sl2, mrun, pk, ls);
+        if constexpr (W == 32)
+            ptx::tmem_st_32x32b_x16(tP + j * 16, pk);
+        else
+            ptx::tmem_st_32x32b_x8(tP + j * 16, pk);
+    }
+    // the chunks written under the old offset, once this chunk's values are no longer live
+    if (any_up) rescale_p(tP, j, false, f);
+}
+
 __global__ void __launch_bounds__(AW_THREADS, 1)
 attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -156,7 +235,6 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::mbar_init(&bars->v_empty[b], 1);
             ptx::mbar_init(&bars->s_full[b], 1);
             ptx::mbar_init(&bars->p_full[b], 8);     // the eight softmax warps of a group
-            for (int q = 0; q < 4; ++q) ptx::mbar_init(&bars->mx_full[b][q], 2);
         }
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 8);
         ptx::mbar_init(&bars->o_done, 1);
@@ -294,29 +372,57 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             if (!ok) break;
             ptx::tc_fence_after();
             // a warp whose 32 query rows all lie past T has no output; it only keeps the
-            // barrier protocol
+            // barrier protocol (both halves of a lane quarter agree on this)
             const bool live = qt * AW_ROWS + quarter * 32 < T;
-            float mx = -INFINITY;
             if (live) {
-                // pass 1: maximum over this half's keys < T (one 32-key chunk per TMEM
-                // wait: two would not fit the register budget of 24 warps). A chunk of
-                // valid keys only is reduced by the load itself (tcgen05.ld.red).
+                const uint32_t bar_id = 1 + g * 4 + quarter;   // this quarter's two halves
+                const uint32_t tP = tS + pbase;                  // this half's P columns
+                unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};   // packed pairs of +0.0f
+                float mrun;        // this half's offset (log2 units): the start + whole steps
+                int j = 0;         // 32-key chunks of this half whose P is written
+                int cfirst = c0;   // first chunk still to load
+                {
+                    // the common starting offset: the maximum over keys [0, 32), read by
+                    // both halves from the same columns
+                    uint32_t vr[32];
+                    float cm;
+                    if (T >= 32) {
+                        cm = ptx::tmem_ld_red_max_32x32b_x32(tS, vr);
+                        ptx::tmem_ld_wait();
+                    } else {
+                        ptx::tmem_ld_32x32b_x32(tS, vr);
+                        ptx::tmem_ld_wait();
+                        mask_tail(vr, T);
+                        cm = chunk_max(vr, -INFINITY);
+                    }
+                    mrun = cm * sl2;
+                    // both halves hold it before P overwrites the columns of keys [0, 32)
+                    ptx::named_bar_sync(bar_id, 64);
+                    if (c0 == 0 && c1 > 0) {   // this half owns keys [0, 32): no second load
+                        p_chunk(vr, cm, sl2, mrun, ls, tP, 0);
+                        j = 1;
+                        cfirst = 1;
+                    } else {
+                        ptx::regs_keep(vr);
+                    }
+                }
 #pragma unroll
                 for (int c = 0; c < 7; ++c) {
-                    const int cc = c0 + c;
+                    const int cc = cfirst + c;
                     if (cc < c1) {
                         uint32_t v0[32];
+                        float cm;
                         if (T - cc * 32 >= 32) {
-                            const float cm = ptx::tmem_ld_red_max_32x32b_x32(tS + cc * 32, v0);
+                            cm = ptx::tmem_ld_red_max_32x32b_x32(tS + cc * 32, v0);
                             ptx::tmem_ld_wait();
-                            ptx::regs_keep(v0);
-                            mx = fmaxf(mx, cm);
                         } else {
                             ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
                             ptx::tmem_ld_wait();
                             mask_tail(v0, T - cc * 32);
-                            mx = chunk_max(v0, mx);
+                            cm = chunk_max(v0, -INFINITY);
                         }
+                        p_chunk(v0, cm, sl2, mrun, ls, tP, j);
+                        ++j;
                     }
                 }
                 if (tail) {
@@ -324,40 +430,17 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                     ptx::tmem_ld_32x32b_x16(tS + c1 * 32, v0);
                     ptx::tmem_ld_wait();
                     mask_tail(v0, T - c1 * 32);
-                    mx = chunk_max(v0, mx);
+                    p_chunk(v0, chunk_max(v0, -INFINITY), sl2, mrun, ls, tP, j);
                 }
-                mx_mine[row] = mx;
-            }
-            // exchange the two halves' maxima
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars->mx_full[g][quarter]);
-            ok = __all_sync(0xffffffffu,
-                            ptx::mbar_wait_bounded(&bars->mx_full[g][quarter], (u >> 1) & 1, abort_flag));
-            if (!ok) break;
-            if (live) {
-                const float m = fmaxf(mx, mx_other[row]) * sl2;
-                // pass 2: P over this half's consumed S columns (keys of chunk c go to
-                // columns pbase + 16 (c - c0))
-                unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};   // packed pairs of +0.0f
-#pragma unroll
-                for (int c = 0; c < 7; ++c) {
-                    const int cc = c0 + c;
-                    if (cc < c1) {
-                        uint32_t v0[32], pk0[16];
-                        ptx::tmem_ld_32x32b_x32(tS + cc * 32, v0);
-                        ptx::tmem_ld_wait();
-                        mask_tail(v0, T - cc * 32);
-                        chunk_exp(v0, sl2, m, pk0, ls);
-                        ptx::tmem_st_32x32b_x16(tS + pbase + c * 16, pk0);
-                    }
-                }
-                if (tail) {
-                    uint32_t v0[16], pk0[8];
-                    ptx::tmem_ld_32x32b_x16(tS + c1 * 32, v0);
-                    ptx::tmem_ld_wait();
-                    mask_tail(v0, T - c1 * 32);
-                    chunk_exp(v0, sl2, m, pk0, ls);
-                    ptx::tmem_st_32x32b_x8(tS + pbase + (c1 - c0) * 16, pk0);
+                // one offset for the row: the larger of the two halves' (they differ only
+                // where a half has raised its own, and then by whole steps)
+                mx_mine[row] = mrun;
+                ptx::named_bar_sync(bar_id, 64);
+                const float mo = mx_other[row];
+                if (__any_sync(0xffffffffu, mo > mrun + 0.5f)) {
+                    const float f = mo > mrun + 0.5f ? pow2_int(-rintf(mo - mrun)) : 1.f;
+                    rescale_p(tP, j, tail, f);
+                    f2_scale(ls, f);
                 }
                 ptx::tmem_st_wait();
                 sL[((u & 3) * 2 + half) * AW_ROWS + row] = [&] {
@@ -487,7 +570,14 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
     p.nq = (int)((T + AW_ROWS - 1) / AW_ROWS);
     p.ns = (int)((T + 15) / 16 * 16);
     p.nkb = (p.ns + AW_ROWS - 1) / AW_ROWS;
-    p.split = (p.ns >> 5) / 2 * 32;   // half 0: the first floor(full chunks / 2) chunks
+    {
+        // half 0 takes the first ceil((full chunks + 1) / 2) 32-key chunks (it reads key
+        // chunk 0 once; half 1 reads it for the offset and then takes the rest and the
+        // 16-key tail)
+        const int full = p.ns >> 5;
+        const int sc = (full + 2) / 2 < full ? (full + 2) / 2 : full;
+        p.split = sc * 32;
+    }
     p.items = (int)(N * H);
     p.scale_log2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
     p.o = static_cast<__nv_bfloat16*>(o);
