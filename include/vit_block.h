@@ -101,7 +101,7 @@ int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_
  * (cudaHostAlloc / pinned) copy at full link speed; pageable ones work but copy slower.
  * Device buffers come from the library's pool. The optional affine pointers are host
  * pointers or NULL. Errors as vit_block.
- * Large batches (24,576 tokens or more) are cut into up to 4 chunks of whole sequences
+ * Large batches (20,000 tokens or more) are cut into up to 5 chunks of whole sequences
  * (sequences are independent: "ViT Encoder Block" (crackedaicode), "Inputs and output");
  * the copy in, the block and the copy out of successive chunks overlap on three
  * library-owned streams that start after, and end before, the work already queued on

@@ -973,10 +973,10 @@ int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* 
 // vit_block_host cuts the batch into chunks of whole sequences so that copies in, blocks
 // and copies out of successive chunks overlap on three streams. A block on fewer rows
 // fills the GPU less well, so the chunks are few and the first and last (whose copies
-// cannot be hidden) are the smallest: one chunk per 12,288 tokens, at most 4, with weights
-// 1, 1 / 1, 2, 1 / 1, 3, 3, 1 (the best of the schedules measured for 256 ViT-B/16
-// sequences). VIT_HOST_SPLIT="w1,w2,..." sets the weights ("1": one chunk on the caller's
-// stream).
+// cannot be hidden) are the smallest: one chunk per 10,000 tokens, at most 5, with weights
+// 1, 1 / 1, 2, 1 / 1, 3, 3, 1 / 1, 2, 2, 2, 1 (1, 2, 2, 2, 1 measured best for 256 ViT-B/16
+// sequences, 4 % ahead of 1, 3, 3, 1). VIT_HOST_SPLIT="w1,w2,..." sets the weights ("1": one
+// chunk on the caller's stream).
 std::vector<int64_t> host_chunks(int64_t N, int64_t T) {
     static const std::vector<double> forced = [] {
         std::vector<double> w;
@@ -993,10 +993,11 @@ std::vector<int64_t> host_chunks(int64_t N, int64_t T) {
     }();
     std::vector<double> w = forced;
     if (w.empty()) {
-        int64_t c = (N * T) / 12288;
-        if (c > 4) c = 4;
+        int64_t c = (N * T) / 10000;
+        if (c > 5) c = 5;
         if (c < 1) c = 1;
-        for (int64_t i = 0; i < c; ++i) w.push_back(c > 2 && (i == 0 || i == c - 1) ? 1.0 : c - 1.0);
+        const double mid = c == 5 ? 2.0 : (double)(c - 1);   // 1,2,1 / 1,3,3,1 / 1,2,2,2,1
+        for (int64_t i = 0; i < c; ++i) w.push_back(c > 2 && (i == 0 || i == c - 1) ? 1.0 : mid);
     }
     if ((int64_t)w.size() > N) w.resize((size_t)N);
     double tot = 0;
