@@ -183,6 +183,7 @@ def test_host_pipeline_pageable_buffers():
 
 def test_host_pipeline_uneven_chunks_in_a_subprocess():
     # VIT_HOST_SPLIT is read once per process: weights 1, 2, 1 over 7 sequences (2, 3, 2)
+    _dev()
     import subprocess
     import sys
     code = ("import torch, sys; sys.path.insert(0, %r); import test_gpu_block as t; "
@@ -192,6 +193,36 @@ def test_host_pipeline_uneven_chunks_in_a_subprocess():
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
                        cwd=os.path.dirname(os.path.dirname(__file__)), timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+
+
+def test_dependent_launch_changes_no_result():
+    # Programmatic dependent launch only lets a kernel's set-up overlap the previous
+    # kernel's tail; every kernel waits for its predecessor before touching memory. Two
+    # chained blocks (the second reads the first's output) and the host pipeline give the
+    # same bits with it switched off (VIT_PDL=0, read once per process: a child process).
+    _dev()
+    import subprocess
+    import sys
+    code = ("import torch, sys; sys.path.insert(0, %r); import test_gpu_block as t; "
+            "from vision_transformer_encoder_gb300 import api; "
+            "from vision_transformer_encoder_gb300.inputs import make_config_inputs, CONFIGS; "
+            "c = CONFIGS['vit_b16']; inp = make_config_inputs('vit_b16', dtype=torch.bfloat16, N=48); "
+            "d = inp.to(device='cuda'); y = api.vit_block(d.x, *d.weights(), c['H'], c['eps']); "
+            "z = api.vit_block(y, *d.weights(), c['H'], c['eps']); "
+            "h, _ = t._host_vs_device('vit_ti16', 64); "
+            "torch.save((y.cpu(), z.cpu(), h), sys.argv[1]); print('ok')" % os.path.dirname(__file__))
+    import tempfile
+    outs = []
+    for flag in ("1", "0"):
+        path = os.path.join(tempfile.gettempdir(), "vit_pdl_%d_%s.pt" % (os.getpid(), flag))
+        r = subprocess.run([sys.executable, "-c", code, path], env=dict(os.environ, VIT_PDL=flag),
+                           capture_output=True, text=True, cwd=os.path.dirname(os.path.dirname(__file__)),
+                           timeout=600)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
+        outs.append(torch.load(path))
+        os.remove(path)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def test_stream_argument_is_honoured():
