@@ -103,9 +103,9 @@ int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_
  * pointers or NULL. Errors as vit_block.
  * Large batches (20,000 tokens or more) are cut into up to 5 chunks of whole sequences
  * (sequences are independent: "ViT Encoder Block" (crackedaicode), "Inputs and output");
- * the copy in, the block and the copy out of successive chunks overlap on three
- * library-owned streams that start after, and end before, the work already queued on
- * `stream`. Results are those of one vit_block_ex call on the whole batch, bit for bit.
+ * the copy in, the block and the copy out of successive chunks overlap on library-owned
+ * streams (one for copies in, two for blocks, one for copies out) that start after, and
+ * end before, the work already queued on `stream`. Results are those of one vit_block_ex call on the whole batch, bit for bit.
  */
 int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_host,
                    const void* w_v_host, const void* w_o_host, const void* w_mlp1_host,

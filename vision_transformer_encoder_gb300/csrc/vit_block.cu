@@ -42,8 +42,9 @@ struct DeviceState {
     bool ready = false;
     DeviceInfo info;
     cudaMemPool_t pool = nullptr;
-    // vit_block_host's pipeline: host-to-device copies, compute, device-to-host copies
-    cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+    // vit_block_host's pipeline: host-to-device copies, compute (two streams, chunks
+    // alternating), device-to-host copies
+    cudaStream_t h2d = nullptr, comp = nullptr, comp2 = nullptr, d2h = nullptr;
 };
 
 std::mutex g_mu;
@@ -977,6 +978,16 @@ int encoder_impl(const void* x, const vit_layer* layers, int64_t L, const void* 
 // 1, 1 / 1, 2, 1 / 1, 3, 3, 1 / 1, 2, 2, 2, 1 (1, 2, 2, 2, 1 measured best for 256 ViT-B/16
 // sequences, 4 % ahead of 1, 3, 3, 1). VIT_HOST_SPLIT="w1,w2,..." sets the weights ("1": one
 // chunk on the caller's stream).
+// Compute streams of the host pipeline: 2 (chunks alternate), or 1 with
+// VIT_HOST_COMPUTE_STREAMS=1.
+int host_compute_streams() {
+    static const int n = [] {
+        const char* e = std::getenv("VIT_HOST_COMPUTE_STREAMS");
+        return e && e[0] == '1' ? 1 : 2;
+    }();
+    return n;
+}
+
 std::vector<int64_t> host_chunks(int64_t N, int64_t T) {
     static const std::vector<double> forced = [] {
         std::vector<double> w;
@@ -1021,16 +1032,19 @@ std::vector<int64_t> host_chunks(int64_t N, int64_t T) {
 int pipeline_streams(DeviceState* st) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (st->h2d) return VIT_OK;
-    cudaStream_t a = nullptr, b = nullptr, c = nullptr;
+    cudaStream_t a = nullptr, b = nullptr, c = nullptr, b2 = nullptr;
     if (cudaStreamCreateWithFlags(&a, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&b, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&b2, cudaStreamNonBlocking) != cudaSuccess ||
         cudaStreamCreateWithFlags(&c, cudaStreamNonBlocking) != cudaSuccess) {
         if (a) cudaStreamDestroy(a);
         if (b) cudaStreamDestroy(b);
+        if (b2) cudaStreamDestroy(b2);
         cudaGetLastError();
         return VIT_ERR_CUDA;
     }
     st->comp = b;
+    st->comp2 = b2;
     st->d2h = c;
     st->h2d = a;
     return VIT_OK;
@@ -1196,12 +1210,16 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
     }
     const std::vector<int64_t> chunk_n = host_chunks(N, T);
     const int64_t chunks = (int64_t)chunk_n.size();
-    cudaStream_t sh = s, sc = s, sd = s;   // copy-in, compute, copy-out
+    // copy-in, compute (successive chunks alternate between two streams, so that one
+    // chunk's kernels can fill the SMs another's leave idle at their ends), copy-out
+    cudaStream_t sh = s, sd = s;
+    cudaStream_t scs[2] = {s, s};
     if (chunks > 1) {
         rc = pipeline_streams(st);
         if (rc != VIT_OK) return rc;
         sh = st->h2d;
-        sc = st->comp;
+        scs[0] = st->comp;
+        scs[1] = host_compute_streams() > 1 ? st->comp2 : st->comp;
         sd = st->d2h;
     }
     void* dmem = nullptr;
@@ -1221,12 +1239,13 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
         if (r == cudaSuccess) ev.push_back(*out);
         return r;
     };
-    cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp = nullptr;
+    cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp[2] = {nullptr, nullptr};
     if (chunks > 1) {
         e = new_event(&start);
         if (e == cudaSuccess) e = cudaEventRecord(start, s);   // after the allocation
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sh, start, 0);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(scs[0], start, 0);
+        if (e == cudaSuccess && scs[1] != scs[0]) e = cudaStreamWaitEvent(scs[1], start, 0);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, start, 0);
     }
     // weights and affine terms first, then x chunk by chunk
@@ -1237,6 +1256,7 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
     for (int64_t c = 0; c < chunks && e == cudaSuccess && rc == VIT_OK; ++c) {
         const int64_t nc = chunk_n[(size_t)c];
         const size_t o = (size_t)n0 * seq_bytes, nbytes = (size_t)nc * seq_bytes;
+        cudaStream_t sc = scs[c & 1];
         e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(x_host) + o, nbytes,
                             cudaMemcpyHostToDevice, sh);
         cudaEvent_t in_ready = nullptr, done = nullptr;
@@ -1255,7 +1275,7 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
             e = new_event(&done);
             if (e == cudaSuccess) e = cudaEventRecord(done, sc);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, done, 0);
-            end_comp = done;
+            end_comp[c & 1] = done;
         }
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + o, static_cast<uint8_t*>(dev_out) + o, nbytes,
@@ -1268,7 +1288,8 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
         cudaError_t je = new_event(&end_d2h);
         if (je == cudaSuccess) je = cudaEventRecord(end_d2h, sd);
         if (je == cudaSuccess) je = cudaStreamWaitEvent(s, end_d2h, 0);
-        if (je == cudaSuccess && end_comp) je = cudaStreamWaitEvent(s, end_comp, 0);
+        for (int i = 0; i < 2; ++i)
+            if (je == cudaSuccess && end_comp[i]) je = cudaStreamWaitEvent(s, end_comp[i], 0);
         if (je == cudaSuccess) {
             cudaEvent_t in_done = nullptr;
             je = new_event(&in_done);
