@@ -21,10 +21,10 @@
 //                    as the maximum over keys [0, 32), which both halves read, and a half
 //                    raises its own r, by whole log2 units, only when a chunk's maximum
 //                    passes r by more than 8 (so P <= 2^8); the P it has written is then
-//                    rescaled by an exact power of two. The half whose P lands on the
-//                    columns of keys [0, 32) waits (mbarrier) until the other half has read
-//                    them. At the end the two halves exchange offsets through shared memory
-//                    and an mbarrier per quarter and take the larger; the one below
+//                    rescaled by an exact power of two. At the end the two halves take the
+//                    larger of their offsets (a named barrier per quarter; a warp whose
+//                    wait fails still passes it for each remaining unit, as its partner
+//                    does, so it never waits for a warp that has left); the one below
 //                    rescales. With typical scores no chunk passes the start by 8 and the
 //                    row costs one read of S, each P rounded once.
 //   warps 16-19      epilogue, one per TMEM lane quarter: O into registers, O's slot
@@ -66,9 +66,9 @@ constexpr int AW_OFF_Q = 0;                        // [buffer][query tile]
 constexpr int AW_OFF_K = AW_OFF_Q + 4 * AW_BOX;    // [buffer][128-key box]
 constexpr int AW_OFF_V = AW_OFF_K + 4 * AW_BOX;    // [buffer][128-key box]
 constexpr int AW_OFF_L = AW_OFF_V + 4 * AW_BOX;    // row sums [unit % 4][half][row]
-constexpr int AW_OFF_MX = AW_OFF_L + 4 * 2 * AW_ROWS * 4;   // offsets [group][exchange % 2][half][row]
-constexpr int AW_OFF_BAR = AW_OFF_MX + 2 * 2 * 2 * AW_ROWS * 4;
-constexpr int AW_SMEM = AW_OFF_BAR + 512 + 1024;   // + alignment slack
+constexpr int AW_OFF_MX = AW_OFF_L + 4 * 2 * AW_ROWS * 4;   // row maxima [group][half][row]
+constexpr int AW_OFF_BAR = AW_OFF_MX + 2 * 2 * AW_ROWS * 4;
+constexpr int AW_SMEM = AW_OFF_BAR + 256 + 1024;   // + alignment slack
 constexpr uint32_t AW_TMEM_O = 448;
 
 struct AwParams {
@@ -86,13 +86,11 @@ struct AwParams {
 struct AwBars {
     uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], l_full[4];
-    uint64_t ref_read[2][4];   // [group][lane quarter]: the other half has read keys [0, 32)
-    uint64_t mx_full[2][4];    // [group][lane quarter]: both halves' offsets written
     uint64_t o_done, o_free, done;
     uint32_t tmem_slot;
     int abort_flag;
 };
-static_assert(sizeof(AwBars) <= 512, "barrier block");
+static_assert(sizeof(AwBars) <= 256, "barrier block");
 static_assert(AW_SMEM <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ void aw_error(uint32_t* err, uint32_t bit) {
@@ -241,11 +239,6 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::mbar_init(&bars->p_full[b], 8);     // the eight softmax warps of a group
         }
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 8);
-        for (int b = 0; b < 2; ++b)
-            for (int q = 0; q < 4; ++q) {
-                ptx::mbar_init(&bars->ref_read[b][q], 1);
-                ptx::mbar_init(&bars->mx_full[b][q], 2);
-            }
         ptx::mbar_init(&bars->o_done, 1);
         ptx::mbar_init(&bars->o_free, 4);            // the four epilogue warps
         ptx::mbar_init(&bars->done, 1);
@@ -372,15 +365,23 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
         const int c0 = half ? p.split >> 5 : 0, c1 = half ? p.ns >> 5 : p.split >> 5;
         const bool tail = half && (p.ns & 16) != 0;
         const uint32_t pbase = half ? (uint32_t)p.split : 0u;   // P columns of this half
-        // the half whose P lands on the columns of keys [0, 32): half 0 when it has keys,
-        // otherwise half 1 (then both start at column 0)
-        const bool writes0 = half ? p.split == 0 : p.split >= 32;
-        int nx = 0;   // offset exchanges of this group so far (the same count in both halves)
+        float* mx_mine = sMx + (g * 2 + half) * AW_ROWS;
+        const float* mx_other = sMx + (g * 2 + (half ^ 1)) * AW_ROWS;
         bool ok = true;
+        const uint32_t bar_id = 1 + g * 4 + quarter;   // named barrier of this quarter's two halves
         for (int u = g; u < units; u += 2) {
             const int k = u / nq, qt = u - k * nq;
             ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->s_full[g], (u >> 1) & 1, abort_flag));
-            if (!ok) break;
+            if (!ok) {
+                // The named barrier below waits without limit: pass it for this and every
+                // later unit the quarter works on, as the other half does, then leave.
+                for (int v = u; v < units; v += 2)
+                    if ((v - (v / nq) * nq) * AW_ROWS + quarter * 32 < T) {
+                        ptx::named_bar_sync(bar_id, 64);
+                        ptx::named_bar_sync(bar_id, 64);
+                    }
+                break;
+            }
             ptx::tc_fence_after();
             // a warp whose 32 query rows all lie past T has no output; it only keeps the
             // barrier protocol (both halves of a lane quarter agree on this)
@@ -406,17 +407,8 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                         cm = chunk_max(vr, -INFINITY);
                     }
                     mrun = cm * sl2;
-                    // the other half holds it before P overwrites the columns of keys [0, 32)
-                    if (writes0) {
-                        ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->ref_read[g][quarter], nx & 1,
-                                                                            abort_flag));
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    } else {
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(&bars->ref_read[g][quarter]);
-                    }
+                    // both halves hold it before P overwrites the columns of keys [0, 32)
+                    ptx::named_bar_sync(bar_id, 64);
                     if (c0 == 0 && c1 > 0) {   // this half owns keys [0, 32): no second load
                         p_chunk(vr, cm, sl2, mrun, ls, tP, 0);
                         j = 1;
@@ -453,14 +445,9 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                 }
                 // one offset for the row: the larger of the two halves' (they differ only
                 // where a half has raised its own, and then by whole steps)
-                float* mxb = sMx + (g * 2 + (nx & 1)) * 2 * AW_ROWS;   // [group][exchange % 2]
-                mxb[half * AW_ROWS + row] = mrun;
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&bars->mx_full[g][quarter]);
-                ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->mx_full[g][quarter], nx & 1, abort_flag));
-                ++nx;
-                if (!ok) break;
-                const float mo = mxb[(half ^ 1) * AW_ROWS + row];
+                mx_mine[row] = mrun;
+                ptx::named_bar_sync(bar_id, 64);
+                const float mo = mx_other[row];
                 if (__any_sync(0xffffffffu, mo > mrun + 0.5f)) {
                     const float f = mo > mrun + 0.5f ? pow2_int(-rintf(mo - mrun)) : 1.f;
                     rescale_p(tP, j, tail, f);

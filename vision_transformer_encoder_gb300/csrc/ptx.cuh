@@ -81,6 +81,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Named barrier `id` (1-15; 0 is __syncthreads) over `count` threads, a multiple of 32:
+// the warps that reach it wait for one another; shared-memory writes before it are
+// visible to the participants after it. It has no time limit, so every participant must
+// reach each use of it on every path, error paths included.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
