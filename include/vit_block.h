@@ -30,6 +30,12 @@
  *  - Scratch memory is taken from a library-owned, stream-ordered memory pool on the
  *    current device and returned to it on `stream`; the caller owns every pointer it
  *    passes.
+ *  - Kernels are launched with programmatic dependent launch: each waits for the
+ *    previous kernel in the stream (griddepcontrol.wait) before touching memory and
+ *    lets the next one start its set-up early. Stream order is kept for every caller
+ *    kernel launched normally. A caller kernel launched after a call with programmatic
+ *    stream serialisation must wait on the grid dependency before reading the results,
+ *    as CUDA requires of any such launch. VIT_PDL=0 turns it off.
  *  - Every call returns a vit_status (0 = success). No call aborts, traps or throws.
  *  - Results are deterministic: the same inputs give bit-identical outputs.
  */
