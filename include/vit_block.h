@@ -307,6 +307,17 @@ const char* vit_status_string(int status);
  */
 int vit_device_error(uint32_t* word);
 
+/*
+ * vit_selftest_wait -- exercises the device-side failure detection: one kernel waits
+ * on a barrier that nothing completes, with the same bounded wait every kernel of the
+ * library uses, and sets a bit (1 << 5) in the device error word when the wait gives up
+ * -- after the wait limit (about two seconds of SM clock) or, with abort_first != 0, at
+ * once, as when another part of a kernel has already failed. The GPU stays usable.
+ * Read the result with vit_device_error. Enqueued on `stream`; returns VIT_ERR_CUDA if
+ * the launch fails.
+ */
+int vit_selftest_wait(int abort_first, void* stream);
+
 /* Number of kernels this library has launched in this process (all devices). */
 int64_t vit_launch_count(void);
 

@@ -49,6 +49,7 @@ SIGNATURES = {
     "vit_status_string": (ctypes.c_char_p, [_int]),
     "vit_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "vit_launch_count": (_i64, []),
+    "vit_selftest_wait": (_int, [_int, _vp]),
     "vit_timing_enable": (_int, [_int]),
     "vit_timing_collect": (_int, []),
     "vit_timing_kernels": (_int, []),
@@ -323,6 +324,13 @@ def device_error() -> int:
     if rc not in (0, -4):
         raise VitError(rc, "vit_device_error")
     return int(w.value)
+
+
+def selftest_wait(abort_first: bool = False, stream=None):
+    """Enqueue the bounded-wait self test (a wait that must give up); read the outcome
+    with device_error(): bit 1 << 5 is set when the wait ended by its limit or abort."""
+    _check(load_library().vit_selftest_wait(1 if abort_first else 0, _stream(stream)),
+           "vit_selftest_wait")
 
 
 def launch_count() -> int:

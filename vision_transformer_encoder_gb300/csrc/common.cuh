@@ -16,6 +16,7 @@ enum : uint32_t {
     ERRBIT_TIMEOUT_EPILOGUE = 1u << 2,
     ERRBIT_TIMEOUT_TEARDOWN = 1u << 3,
     ERRBIT_TIMEOUT_ATTENTION = 1u << 4,
+    ERRBIT_SELFTEST = 1u << 5,   // vit_selftest_wait: the deliberate wait ran out
 };
 
 // One bounded device-side wait gives up after this many SM clock cycles (about two

@@ -19,6 +19,11 @@ struct DeviceInfo {
     uint32_t* err_word = nullptr;  // device address of the error word
 };
 
+// ---- bounded-wait self test (selftest.cu) -------------------------------------
+// One CTA waits on an mbarrier nothing completes and sets ERRBIT_SELFTEST in *err when
+// the wait gives up: after the library's wait limit, or at once with abort_first != 0.
+cudaError_t launch_selftest_wait(int abort_first, uint32_t* err, cudaStream_t s);
+
 // ---- LayerNorm (layernorm.cu) -------------------------------------------------
 // out = LN(x) [* gamma + beta] row by row. Pairs: bf16->bf16, f32->bf16, f32->f32,
 // f64->f64, bf16->f32. gamma/beta (either may be null) have element type gb_dt.

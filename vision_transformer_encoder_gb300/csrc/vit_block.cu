@@ -1450,6 +1450,18 @@ const char* vit_version(void) { return "vit_block 0.1 (sm_103a)"; }
 
 int64_t vit_launch_count(void) { return g_launches.load(); }
 
+int vit_selftest_wait(int abort_first, void* stream) {
+    DeviceState* st = nullptr;
+    const int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    if (launch_selftest_wait(abort_first != 0, st->info.err_word, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return VIT_ERR_CUDA;
+    }
+    return VIT_OK;
+}
+
 int vit_device_error(uint32_t* word) {
     if (cudaDeviceSynchronize() != cudaSuccess) return VIT_ERR_CUDA;
     uint32_t w = 0, zero = 0;
