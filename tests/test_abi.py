@@ -143,3 +143,12 @@ def test_patch_embed_argument_checks(lib):
     # tokens overlapping the images
     assert lib.vit_patch_embed(_fake(0), 2, 3, 32, 32, 16, 0, _fake(1), None, None, None, 8, 1,
                                ctypes.c_void_p(_fake(0).value + 64), None) == -1
+
+
+def test_selftest_without_a_device_reports_a_cuda_error(lib):
+    # no GPU here: the self test cannot launch and says so with a status, not a crash
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present; tests/test_gpu_failure.py covers it")
+    assert lib.vit_selftest_wait(0, None) == -3
+    assert lib.vit_selftest_wait(1, None) == -3
