@@ -95,7 +95,7 @@ def kernel_work(c, f32=False):
         "ln2": ("hbm", M * D * (4 + 2), "bytes"),          # read y fp32, write yn bf16
         "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),
         "w2_gemm_residual": ("tensor", 2 * M * F * D, "flops"),
-        # LayerNorm folded into the GEMMs (default bf16 path): LN1 reduces to row
+        # LayerNorm folded into the GEMMs (opt-in, VIT_LN_FOLD=1): LN1 reduces to row
         # statistics of x; the fold's column terms are computed once per call
         "ln1_row_stats": ("hbm", M * D * 2 + M * 8, "bytes"),
         "ln_fold_prep": ("hbm", (3 * D * D + D * F) * 2 + (3 * D + F) * 8, "bytes"),
@@ -295,6 +295,64 @@ def run_reference(args):
     return 0
 
 
+OTHER_CONFIGS = ("vit_ti16", "vit_l16_384", "vit_h14_448")
+
+
+def time_other_configs(K, W, flush, stream, sampler):
+    """The other block shapes of the workload list (bf16), after the headline: per shape W
+    warm-up steps, K steps timed with events on the launching stream (L2 flushed between
+    steps, outside the events), then K steps with per-kernel events for the slowest
+    kernel. Returns {name: figures}."""
+    peaks, _ = load_peaks()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    res = {}
+    for name in OTHER_CONFIGS:
+        c = CONFIGS[name]
+        d = make_config_inputs(name, seed=0, dtype=torch.bfloat16).to(device=dev)
+        out = torch.empty_like(d.x)
+
+        def step():
+            api.vit_block(d.x, *d.weights(), c["H"], c["eps"], out=out, stream=stream)
+
+        for _ in range(W):
+            step()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t1 = time.time()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        api.timing_reset()
+        api.timing_enable(True)
+        for _ in range(K):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        api.timing_enable(False)
+        pk = {k: v for k, v in api.timing_collect().items() if v[1] > 0}
+        dom = max(pk, key=lambda k: pk[k][0])
+        bound, amount, _u = kernel_work(c)[dom]
+        dom_s = pk[dom][0] / pk[dom][1] / 1e3
+        tfl = flops_per_step(c) / (ms / 1e3) / 1e12
+        dom_fig = amount / dom_s / (1e12 if bound == "tensor" else 1e9)
+        dom_peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
+        res[name] = {"workload": workload_name(name, c), "ms_per_step": ms,
+                     "tokens_per_s": c["N"] * c["T"] / (ms / 1e3), "tflops": tfl,
+                     "frac_of_peak": tfl / peaks["bf16_tflops"], "steps": K, "warmup": W,
+                     "dominant_kernel": {"kernel": dom, "avg_us": dom_s * 1e6, "bound": bound,
+                                         "achieved": dom_fig, "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                                         "frac": dom_fig / dom_peak},
+                     "kernels_us": {k: 1e3 * v[0] / v[1] for k, v in pk.items()},
+                     "clocks": sampler.summary(t0, t1)}
+        del d, out
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -318,6 +376,10 @@ def main():
     ap.add_argument("--cls-only", action="store_true",
                     help="the last block computes the CLS rows alone: vit_block_cls (with "
                          "--encoder-layers 0) or vit_encoder_cls")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the Ti, L/16@384 and H/14@448 block timings added after the headline")
+    ap.add_argument("--other-steps", type=int, default=50,
+                    help="timed steps per other block configuration")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -415,9 +477,14 @@ def main():
     step_ms_sum, launches = timed_pass(False)
     t1 = time.time()
     kernel_pass_ms, _ = timed_pass(True)
+    per_kernel = api.timing_collect()
+    single_block = L == 0 and not args.patch_embed and not args.cls_only
+    others = None
+    if (single_block and not f32 and world == 1 and not args.n_seq and name == "vit_b16"
+            and not args.no_other_configs):
+        others = time_other_configs(args.other_steps, args.warmup, flush, stream, sampler)
     time.sleep(0.1)
     sampler.stop()
-    per_kernel = api.timing_collect()
     total_ms = reduce_max(step_ms_sum, world)
     kernel_pass_total = reduce_max(kernel_pass_ms, world)
     tokens = c["N"] * c["T"]
@@ -426,7 +493,6 @@ def main():
 
     # end to end through the host-buffer entry point (pinned host memory)
     e2e = None
-    single_block = L == 0 and not args.patch_embed and not args.cls_only
     if args.e2e_steps > 0 and single_block:
         pinned = [t.pin_memory() for t in [inp.x] + inp.weights()]
         hout = torch.empty_like(pinned[0]).pin_memory()
@@ -529,6 +595,8 @@ def main():
         "e2e": e2e,
         "clocks": sampler.summary(t0, t1),
     }
+    if others is not None:
+        line["configs"] = others
     if world == 1 and not args.no_cpu_baseline and single_block:
         line["cpu_baseline"] = cpu_baseline(name, c)
     if args.n_seq:

@@ -2,28 +2,21 @@
 
 The library runs its GEMMs on the CTA-pair kernel by default; VIT_GEMM_PAIR=0 selects
 the single-CTA kernel. The choice is read once per process, so the stage tests are
-re-run in a child process with the variable set.
+re-run in a child process with the variable set; the child must report passed tests
+and no skipped ones.
 """
-import os
-import subprocess
-import sys
-
 import pytest
 
-pytestmark = pytest.mark.gpu
+from _child import run_child_pytest
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+pytestmark = pytest.mark.gpu
 
 
 def test_linear_stages_on_single_cta_kernel():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    env = dict(os.environ, VIT_GEMM_PAIR="0")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_gpu_stages.py"), "-k", "linear"],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    run_child_pytest("test_gpu_stages.py", {"VIT_GEMM_PAIR": "0"}, k="linear", timeout=600)
 
 
 def test_fp32_block_on_cuda_core_gemm():
@@ -32,8 +25,4 @@ def test_fp32_block_on_cuda_core_gemm():
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    env = dict(os.environ, VIT_FP32_TC="0")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_gpu_block.py")],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+    run_child_pytest("test_gpu_block.py", {"VIT_FP32_TC": "0"})

@@ -532,6 +532,21 @@ def test_patch_embed_printed_flat_index():
     assert np.flatnonzero(out[0, 0]).tolist() == [g["flat_index"]]
 
 
+def test_patchify_printed_example_order_p1_p2_c():
+    """The page's printed patchify example pins flatten order 1, (p1, p2, c)."""
+    g = _load("p3_patchify_example.json")
+    shape = tuple(g["image_shape"])
+    im = np.arange(float(np.prod(shape))).reshape(shape)
+    N, C, H, W = shape
+    P = g["patch"]
+    K = C * P * P
+    out = oracle.patch_embed(im, P, np.eye(K), order=1)   # identity projection, no CLS row
+    assert out.shape == tuple(g["out_shape"])
+    np.testing.assert_array_equal(out[0, 0], np.array(g["first_patch"], dtype=float))
+    # and order 0 (channel by channel) differs from the printed patch
+    assert not np.array_equal(oracle.patch_embed(im, P, np.eye(K), order=0)[0, 0], out[0, 0])
+
+
 def test_patch_embed_cls_and_positions():
     N, C, H, W, P, D = 2, 3, 16, 16, 8, 6
     im, _, _, cls, pos = _rand_images(N, C, H, W, P, D, seed=4)

@@ -3,10 +3,15 @@
 Some callers cannot allocate device memory while the block runs (all memory reserved
 up front, or allocation not allowed where the call is made). For them the library
 offers vit_block_noalloc, which takes the same arguments as vit_block_ex but keeps its
-scratch in one fixed 64 MiB array instead of a memory pool. These tests call it
-through the C ABI and compare it with vit_block_ex on the same inputs, twice in a row
-(the array keeps the previous call's contents), within the tolerances the other block
-tests use. This file is collected last on purpose.
+scratch in one fixed 64 MiB array instead of a memory pool.
+
+The array keeps whatever the previous call left in it. So each test first runs the
+entry point on OTHER inputs (another seed, and one more sequence when that still fits,
+which shifts every scratch region), and only then on the inputs it checks, twice in a
+row. Both entry points run the same deterministic kernels on the same inputs, so the
+result must equal vit_block_ex's bit for bit; a stale scratch byte read anywhere would
+break that. A small case is also checked against the float64 oracle at the block
+tolerances (3e-2 bf16, 2e-4 fp32). This file is collected last on purpose.
 """
 import ctypes
 
@@ -14,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from vision_transformer_encoder_gb300 import api
 from vision_transformer_encoder_gb300.inputs import make_inputs
 
@@ -22,6 +28,7 @@ pytestmark = pytest.mark.gpu
 SCRATCH_BYTES = 64 << 20
 TOL = {torch.bfloat16: 3e-2, torch.float32: 2e-4}
 DTYPE = {torch.float32: 0, torch.bfloat16: 1}
+VIT_ERR_UNSUPPORTED = -6
 
 
 def _dev():
@@ -44,28 +51,68 @@ def _noalloc(d, H, eps, out, affine):
                                  N, T, D, F, H, float(eps), DTYPE[d.x.dtype], _p(out), stream)
 
 
+def _ex(d, H, eps, affine):
+    return api.vit_block_ex(d.x, *d.weights(), H, eps, **(d.affine() if affine else {}))
+
+
+def _fill_with_other_call(dev, shape, dtype, affine, eps):
+    """Runs vit_block_noalloc on other inputs, checked bitwise against vit_block_ex, so
+    the scratch array holds that call's values when the checked call starts."""
+    N, T, D, H, F = shape
+    for n_other in (N + 1, N):
+        d = make_inputs(n_other, T, D, F, seed=29, dtype=dtype, affine=affine).to(device=dev)
+        out = torch.full_like(d.x, float("nan"))
+        rc = _noalloc(d, H, eps, out, affine)
+        if rc == VIT_ERR_UNSUPPORTED and n_other > N:
+            continue   # one more sequence does not fit the array on this path
+        assert rc == 0, api.status_string(rc)
+        ref = _ex(d, H, eps, affine)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), "other-input call differs from vit_block_ex"
+        return
+    raise AssertionError("unreachable")
+
+
 @pytest.mark.parametrize("dtype,shape,affine", [
     (torch.bfloat16, (16, 197, 768, 12, 3072), False),   # ViT-B/16 block shape, 16 sequences
     (torch.bfloat16, (16, 197, 768, 12, 3072), True),
-    (torch.float32, (8, 197, 192, 3, 768), False),       # ViT-Ti/16 block shape, CUDA cores
+    (torch.float32, (8, 197, 192, 3, 768), False),       # ViT-Ti/16 block shape, fp32 path
 ])
-def test_noalloc_matches_vit_block_twice(dtype, shape, affine):
+def test_noalloc_equals_vit_block_ex_after_other_inputs(dtype, shape, affine):
     dev = _dev()
     N, T, D, H, F = shape
     eps = 1e-6
-    inp = make_inputs(N, T, D, F, seed=11, dtype=dtype, affine=affine)
-    d = inp.to(device=dev)
-    ref = api.vit_block_ex(d.x, *d.weights(), H, eps, **(d.affine() if affine else {}))
+    _fill_with_other_call(dev, shape, dtype, affine, eps)
+    d = make_inputs(N, T, D, F, seed=11, dtype=dtype, affine=affine).to(device=dev)
+    ref = _ex(d, H, eps, affine)
     torch.cuda.synchronize()
     for call in range(2):
         out = torch.full_like(d.x, float("nan"))
         rc = _noalloc(d, H, eps, out, affine)
         assert rc == 0, api.status_string(rc)
         torch.cuda.synchronize()
-        got = out.double().cpu().numpy()
-        assert np.isfinite(got).all(), "call %d left elements unwritten" % call
-        err = np.abs(got - ref.double().cpu().numpy()).max()
-        assert err <= TOL[dtype], "call %d differs from vit_block_ex by %g" % (call, err)
+        assert torch.isfinite(out.float()).all(), "call %d left elements unwritten" % call
+        assert torch.equal(out, ref), "call %d differs from vit_block_ex: max |diff| %g" % (
+            call, (out.double() - ref.double()).abs().max().item())
+    assert api.device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_noalloc_matches_oracle(dtype):
+    dev = _dev()
+    N, T, D, H, F = 2, 197, 192, 3, 768
+    eps = 1e-5
+    _fill_with_other_call(dev, (N, T, D, H, F), dtype, True, eps)
+    inp = make_inputs(N, T, D, F, seed=13, dtype=dtype, affine=True)
+    d = inp.to(device=dev)
+    for call in range(2):
+        out = torch.full_like(d.x, float("nan"))
+        rc = _noalloc(d, H, eps, out, True)
+        assert rc == 0, api.status_string(rc)
+        torch.cuda.synchronize()
+        ref = oracle.vit_block(inp.x, *inp.weights(), H, eps, **inp.affine())
+        err = np.abs(out.double().cpu().numpy() - ref).max()
+        assert err <= TOL[dtype], "call %d differs from the oracle by %g" % (call, err)
     assert api.device_error() == 0
 
 
@@ -78,6 +125,6 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     d = inp.to(device=dev)
     out = torch.full_like(d.x, float("nan"))
     rc = _noalloc(d, H, 1e-6, out, False)
-    assert rc == -6   # VIT_ERR_UNSUPPORTED, and nothing launched
+    assert rc == VIT_ERR_UNSUPPORTED   # and nothing launched
     torch.cuda.synchronize()
     assert torch.isnan(out.float()).all()

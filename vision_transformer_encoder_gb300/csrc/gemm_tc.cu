@@ -8,15 +8,25 @@
 //   W1  : h   = GELU_tanh(yn @ w_mlp1 [+ b1])     epilogue: GELU -> bf16
 //   W2  : out = y + h @ w_mlp2 [+ b2]             epilogue: + residual (fp32) -> bf16
 //
-// Design (sm_103a): one CTA per SM, persistent over 128 x 256 output tiles.
-//   warp 0      TMA producer: A tile 128 x 64 (K-major, 128B swizzle) and four
-//               64(N) x 64(K) boxes of the row-major weight (MN-major, 128B swizzle)
-//               per stage, 4-stage ring, completion counted on mbarriers.
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and
-//               issues tcgen05.mma (M 128, N 256, K 16) from one thread; commits
-//               free ring slots and announce finished accumulators.
-//   warps 2-5   epilogue: tcgen05.ld 32 columns at a time (one output row per
-//               thread), fused bias / GELU / residual, vector stores.
+// Default kernel (sm_103a): gemm_tc_pair_kernel, a persistent CTA-pair GEMM. The two
+// CTAs of a cluster (one TPC) compute a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M 256 split 128/128 across the CTAs, N 256 split 128/128 in
+// their shared memory, K 16 per instruction, bf16 in, fp32 accumulators in TMEM):
+//   warps 0, 2, 3, 4  TMA producers, one 8 KB box each per ring stage (A rows 0-63, A
+//                     rows 64-127, weight columns 0-63, 64-127 of this CTA's half); the
+//                     completions of both CTAs are counted on the leader's barrier. Five
+//                     or six ring stages of 32 KB per CTA.
+//   warp 1            allocates 512 TMEM columns (two 256-column accumulators) on both
+//                     CTAs; the leader's lane 0 issues the pair MMAs and multicasts its
+//                     commits (ring slot free, accumulator ready) to both CTAs.
+//   warps 5-12        epilogue, two warps per TMEM lane quarter (128 columns each):
+//                     tcgen05.ld 32 columns at a time, bias / GELU / residual in packed
+//                     fp32 pairs, a swizzled 32 x 32 staging tile in shared memory and a
+//                     TMA store; residual tiles arrive by TMA one chunk ahead.
+// GEMMs whose tiles fill at most half of the CTA pairs split K over the pairs and reduce
+// the fp32 slices in a second kernel that applies the epilogue.
+// gemm_tc_kernel, a single-CTA variant (M 128 x N 256 tiles, one producer warp, four
+// epilogue warps with direct vector stores), is selected with VIT_GEMM_PAIR=0.
 // The weights are read in their (in, out) storage order directly: the B operand is
 // MN-major, so no transposed copy is made. Every wait is bounded; on expiry the
 // kernel sets a bit in the device error word, lets its copies and MMAs drain, frees

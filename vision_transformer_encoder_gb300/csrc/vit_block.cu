@@ -1422,7 +1422,7 @@ int vit_block_noalloc(const void* x, const void* w_q, const void* w_k, const voi
     cudaError_t e = launch_block_steps(a, st->info, s, w, st->scratch);
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return VIT_ERR_CUDA;
+        return status_from(e);
     }
     if (debug_sync()) {
         if (cudaStreamSynchronize(s) != cudaSuccess) return VIT_ERR_CUDA;
