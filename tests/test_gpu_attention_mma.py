@@ -2,8 +2,7 @@
 
 Head widths 64 and 80 run on tcgen05 kernels by default: for head width 64 and at most
 224 tokens the whole-row kernel (all keys in one S tile), otherwise the key-streaming
-kernel. VIT_ATTN_WHOLE_PAIR=1 selects the whole-row kernel on CTA pairs,
-VIT_ATTN_TC=0 the mma.sync flash kernel, VIT_ATTN_WHOLE=0 the streaming kernel at every
+kernel. VIT_ATTN_TC=0 selects the mma.sync flash kernel, VIT_ATTN_WHOLE=0 the streaming kernel at every
 length, and VIT_ATTN_PAIR=1 (with VIT_ATTN_WHOLE=0) the streaming CTA-pair kernel.
 The switches are read once per process, so the stage tests are re-run in a child
 process with them set; the child must report passed tests and no skipped ones.
@@ -18,7 +17,6 @@ VARIANTS = {
     "mma_sync": {"VIT_ATTN_TC": "0"},
     "cta_pair_streaming": {"VIT_ATTN_PAIR": "1", "VIT_ATTN_WHOLE": "0"},
     "key_streaming": {"VIT_ATTN_WHOLE": "0"},
-    "cta_pair_whole_row": {"VIT_ATTN_WHOLE_PAIR": "1"},
 }
 
 

@@ -956,11 +956,7 @@ cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, 
     if (N <= 0 || T <= 0) return cudaSuccess;
     switch (D / H) {
         case 64:
-            if (attention_whole_supported(T, D, H)) {
-                if (attention_whole_pair_supported(T, D, H, dev))
-                    return launch_attention_whole_pair(qkv, o, N, T, D, H, dev, s);
-                return launch_attention_whole(qkv, o, N, T, D, H, dev, s);
-            }
+            if (attention_whole_supported(T, D, H)) return launch_attention_whole(qkv, o, N, T, D, H, dev, s);
             if (use_pair_attention() && dev.num_sms >= 2) return launch_pair64(qkv, o, N, T, D, H, dev, s);
             return launch_tc_dh<64, true>(qkv, o, N, T, D, H, dev, s);
         case 80: return launch_tc_dh<80, false>(qkv, o, N, T, D, H, dev, s);

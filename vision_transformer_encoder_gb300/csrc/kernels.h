@@ -169,11 +169,6 @@ cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T,
                                  cudaStream_t s);
 // Head width 64 and T <= 224: all keys of a row in one S tile, exact one-pass softmax.
 bool attention_whole_supported(int64_t T, int64_t D, int64_t H);
-// The same on CTA pairs (attention_whole_pair.cu): an item's two query tiles share every
-// MMA (cta_group::2). Opt-in: VIT_ATTN_WHOLE_PAIR=1.
-bool attention_whole_pair_supported(int64_t T, int64_t D, int64_t H, const DeviceInfo& dev);
-cudaError_t launch_attention_whole_pair(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                        const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
                                    const DeviceInfo& dev, cudaStream_t s);
 bool attention_tc_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv,
