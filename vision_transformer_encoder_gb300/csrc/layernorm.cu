@@ -78,7 +78,7 @@ template <typename TIn, int MAXV>
 __global__ void __launch_bounds__(LN_THREADS)
 ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
                const __nv_bfloat16* __restrict__ gamma, const __nv_bfloat16* __restrict__ beta,
-               int64_t rows, int D, float eps) {
+               int64_t rows, int D, float inv_d, float eps) {
     constexpr int V = VecIO<TIn>::N;
     griddep_wait();                 // x is the previous kernel's output
     griddep_launch_dependents();
@@ -98,6 +98,9 @@ ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
             for (int e = 0; e < V; ++e) sum += v[j][e];
         }
     }
+    // the mean by a correctly rounded division, so that a constant row whose sum is
+    // exact gets its own value back and normalises to exactly 0; the variance, 0 for such
+    // a row either way, by a multiply with 1 / D from the host
     const float mean = warp_sum(sum) / (float)D;
     float sq = 0.f;
 #pragma unroll
@@ -106,12 +109,12 @@ ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
         if (idx < nvec) {
 #pragma unroll
             for (int e = 0; e < V; ++e) {
-                const float d = v[j][e] - mean;
-                sq += d * d;
+                v[j][e] -= mean;   // the centred values, kept for the output
+                sq = fmaf(v[j][e], v[j][e], sq);
             }
         }
     }
-    const float var = warp_sum(sq) / (float)D;
+    const float var = warp_sum(sq) * inv_d;
     const float rstd = rsqrtf(var + eps);
     __nv_bfloat16* orow = out + row * D;
 #pragma unroll
@@ -120,7 +123,7 @@ ln_fast_kernel(const TIn* __restrict__ x, __nv_bfloat16* __restrict__ out,
         if (idx < nvec) {
             float o[V];
 #pragma unroll
-            for (int e = 0; e < V; ++e) o[e] = (v[j][e] - mean) * rstd;
+            for (int e = 0; e < V; ++e) o[e] = v[j][e] * rstd;
             if (gamma) {
                 float gv[V];
                 load_param_bf16<V>(gamma + idx * V, gv);
@@ -192,7 +195,7 @@ cudaError_t launch_fast_v(const void* x, void* out, const void* g, const void* b
     return launch_dependent(ln_fast_kernel<TIn, MAXV>, dim3((unsigned)blocks), dim3(LN_THREADS), 0, s,
                             static_cast<const TIn*>(x), static_cast<__nv_bfloat16*>(out),
                             static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), rows,
-                            (int)D, (float)eps);
+                            (int)D, (float)(1.0 / (double)D), (float)eps);
 }
 
 template <typename TIn>
