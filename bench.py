@@ -36,8 +36,9 @@ from vision_transformer_encoder_gb300.inputs import CONFIGS, make_config_inputs,
 METRIC = "ViT block tokens/s and TFLOP/s (% of GB300 dense peak) at ViT-B/16 bf16, 1 GPU"
 METRIC_F32 = "ViT block tokens/s and TFLOP/s at ViT-B/16 fp32 (3xTF32 tensor-core products), 1 GPU"
 # fp32 path: its products are three TF32 tensor-core products each, so its contraction peak
-# is the measured bf16 peak x the nominal TF32 / BF16 dense ratio (1.1 / 2.25) / 3; its
-# attention runs on the CUDA cores: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz.
+# is the measured bf16 peak x the nominal TF32 / BF16 dense ratio (1.1 / 2.25) / 3; an
+# attention the tensor-core kernel does not take (head width other than 64, or T > 224)
+# runs on the CUDA cores: 152 SMs x 128 FP32 lanes x 2 flop x 2.07 GHz.
 TF32X3_OF_BF16 = (1.1 / 2.25) / 3.0
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 UNIT = "tokens/s"
@@ -72,14 +73,15 @@ def cls_flops_per_step(c):
 
 def kernel_work(c, f32=False):
     """Algorithmic work per launch of each kernel: (bound, amount, unit). f32: the fp32
-    path (fp32 activations, 3xTF32 products, CUDA-core attention)."""
+    path (fp32 activations, 3xTF32 tensor-core products in the GEMMs and, at head width 64
+    and T <= 224, in the attention; CUDA-core attention otherwise)."""
     N, T, D, F = c["N"], c["T"], c["D"], c["F"]
     M = N * T
     if f32:
         return {
             "ln1": ("hbm", M * D * (4 + 4), "bytes"),
             "qkv_gemm": ("tensor", 2 * M * D * 3 * D, "flops"),
-            "attention": ("alu", 4 * N * T * T * D, "flops"),
+            "attention": ("tensor" if D // c["H"] == 64 and T <= 224 else "alu", 4 * N * T * T * D, "flops"),
             "wo_gemm_residual": ("tensor", 2 * M * D * D, "flops"),
             "ln2": ("hbm", M * D * (4 + 4), "bytes"),
             "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),

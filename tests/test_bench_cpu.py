@@ -36,9 +36,16 @@ def test_kernel_work_adds_up_to_the_step(f32):
     es = 4 if f32 else 2
     assert w["ln1"] == ("hbm", M * D * (es + es), "bytes")   # read x, write xn
     assert w["ln2"][1] == M * D * ((4 + 4) if f32 else (4 + 2))   # read fp32 y, write yn
-    assert w["attention"][0] == ("alu" if f32 else "tensor")
+    assert w["attention"][0] == "tensor"   # head width 64, T <= 224: tensor cores on both paths
     for k in block_gemms:
         assert w[k][0] == "tensor"
+
+
+def test_fp32_attention_bound_off_the_tensor_core_shapes():
+    # the fp32 path's attention runs on the CUDA cores at head width 80 or above 224 tokens
+    assert bench.kernel_work(CONFIGS["vit_h14_448"], True)["attention"][0] == "alu"
+    assert bench.kernel_work(CONFIGS["vit_l16_384"], True)["attention"][0] == "alu"
+    assert bench.kernel_work(CONFIGS["vit_ti16"], True)["attention"][0] == "tensor"
 
 
 def test_fp32_path_peaks():

@@ -211,6 +211,57 @@ def test_attention_fp32_tiled(N, T, D, H):
     _close(out, ref, atol=1e-5, rtol=1e-5)
 
 
+@pytest.mark.parametrize("N,T,H", [(3, 1, 2), (2, 17, 3), (2, 128, 2), (2, 129, 1), (4, 197, 12), (2, 224, 4)])
+def test_attention_fp32_tensor_cores(N, T, H):
+    # head width 64 and T <= 224: the 3xTF32 tensor-core kernel, checked against the bound
+    # its arithmetic allows (_close_attention_tf32)
+    d = _dev()
+    D = 64 * H
+    qkv = _rand((N, T, 3 * D), 31 + T, std=1.5, dtype=torch.float32)
+    out = torch.full((N, T, D), float("nan"), device=d)
+    api.attention(qkv.to(d), H, out=out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    r = _close_attention_tf32(out, qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H)
+    print("T=%d: max err / bound %.3f" % (T, r))
+    assert api.device_error() == 0
+
+
+def test_attention_fp32_tensor_cores_dominant_key():
+    # one key far above the others in every row: the softmax is nearly one-hot, P_lo of
+    # the large weight carries most of the correction, and the masked tail keys stay 0
+    d = _dev()
+    N, T, H = 2, 197, 3
+    D = 64 * H
+    qkv = _rand((N, T, 3 * D), 41, dtype=torch.float32)
+    qkv[:, 100, D:2 * D] *= 12.0   # key 100 of every head
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    _close_attention_tf32(out, qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:], H)
+
+
+def _close_attention_tf32(out, q, k, v, H):
+    """Bound from the 3xTF32 arithmetic: each product term q_i k_i (and p_j v_j) is off by
+    at most 4 * 2^-20 of its size (the dropped lo x lo term, the TF32 rounding of the lo
+    parts and the fp32 sums), so a score moves by e <= 4 * 2^-20 sum_i |q_i k_i| / sqrt(dh),
+    each softmax weight by a factor within exp(+-2 e_max) of the row, and per element
+    |out - ref| <= (2 e_max + 4 * 2^-20) sum_j w_j |v_j| + 2^-24 |ref|."""
+    N, T, D = q.shape
+    dh = D // H
+    ref = oracle.attention(q, k, v, H)
+    wabs = oracle.attention(q, k, v.abs(), H)
+    qa = q.double().abs().numpy().reshape(N, T, H, dh).transpose(0, 2, 1, 3)
+    ka = k.double().abs().numpy().reshape(N, T, H, dh).transpose(0, 2, 3, 1)
+    emax = (4 * 2.0 ** -20) * (qa @ ka).max(axis=-1) / np.sqrt(dh)        # (N, H, T)
+    emax = np.repeat(emax.transpose(0, 2, 1), dh, axis=2)                  # (N, T, D)
+    bound = (2 * emax + 4 * 2.0 ** -20) * wabs + 2.0 ** -24 * np.abs(ref)
+    g = out.double().cpu().numpy()
+    assert np.isfinite(g).all()
+    err = np.abs(g - ref)
+    assert (err <= bound).all(), "max err / bound %.3f" % (err / bound).max()
+    return (err / bound).max()
+
+
 def test_attention_bf16_generic_head_width():
     # head width 24 is not one the tensor-core kernel takes: CUDA-core kernel, bf16 I/O
     d = _dev()

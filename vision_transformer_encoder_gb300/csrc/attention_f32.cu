@@ -1,4 +1,5 @@
-// attention_f32.cu -- fp32 multi-head attention on the CUDA cores (the fp32 path).
+// attention_f32.cu -- fp32 multi-head attention on the CUDA cores (the fp32 path), for the
+// shapes the 3xTF32 tensor-core kernel (attention_tf32.cu) does not take.
 //
 // "ViT Encoder Block" (crackedaicode), "Multi-head attention": per sequence n and head
 // h, out_h = softmax(Q_h K_h^T / sqrt(D/H)) V_h with every key visible; heads written
@@ -125,8 +126,10 @@ bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const v
 }
 
 cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                 cudaStream_t s) {
+                                 const DeviceInfo& dev, cudaStream_t s) {
     if (N <= 0 || T <= 0) return cudaSuccess;
+    // head width 64 and at most 224 tokens: the 3xTF32 tensor-core kernel
+    if (attention_tf32_supported(N, T, D, H, qkv, o)) return launch_attention_tf32(qkv, o, N, T, D, H, dev, s);
     switch (D / H) {
         case 32: return launch_dh<32, 1>(qkv, o, N, T, D, s);
         case 48: return launch_dh<48, 1>(qkv, o, N, T, D, s);

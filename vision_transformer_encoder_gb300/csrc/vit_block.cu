@@ -497,7 +497,7 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         step(run(K_QKV, s, [&] { return gemm(fbuf, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, bqkv, nullptr, fqkv); }));
         step(run(K_ATTN, s, [&] {
             if (attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
-                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, s);
+                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s);
             return launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
         }));
         step(run(K_WO, s, [&] { return gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy); }));
@@ -530,7 +530,7 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
         step(run(K_ATTN, s, [&] {
             if (acc_dt == DT_F32 && attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
-                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, s);
+                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s);
             return launch_attention_simt(qkv, acc_dt, buf, a.N, a.T, D, a.H, s);
         }));
         step(run(K_WO, s, [&] {
@@ -1394,7 +1394,7 @@ int vit_attention(const void* qkv, int64_t N, int64_t T, int64_t D, int64_t H, i
         if (dtype == DT_BF16 && attention_fast_supported(D, H, qkv, o) && (D * 2) % 16 == 0)
             return launch_attention_fast(qkv, o, N, T, D, H, s);
         if (dtype == DT_F32 && attention_f32_supported(N, T, D, H, qkv, o))
-            return launch_attention_f32(qkv, o, N, T, D, H, s);
+            return launch_attention_f32(qkv, o, N, T, D, H, st->info, s);
         return launch_attention_simt(qkv, dtype, o, N, T, D, H, s);
     });
     if (e != cudaSuccess) {
