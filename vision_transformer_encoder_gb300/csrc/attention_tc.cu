@@ -437,389 +437,6 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
 }
 
 
-// ------------------------------------------------------------------ CTA-pair kernel
-// Head width 64. Two CTAs of a cluster (one TPC's two SMs) share every MMA
-// (tcgen05 cta_group::2, M 256 = 128 query rows per CTA), which runs at the full
-// tensor rate where the single-CTA M 128 form runs at about half. A work item is
-// (sequence, head, 256 query rows); CTA r owns query rows 128 r .. 128 r + 127 of it.
-// Two items are in flight per pair ("groups" g = 0, 1), so one group's softmax runs
-// while the other group's MMAs do. Per 128-key tile, CTA r loads keys 64 r .. 64 r + 63
-// (the N half of S = Q K^T) and value columns 32 r .. 32 r + 31 (the N half of
-// O = P V, 64-byte swizzle); every load completes on the leader CTA's barriers.
-//   warp 0: Q loads, warp 10: K loads, warp 11: V loads (TMA issue is serialised per
-//   thread, so each stream has its own warp); warp 1: TMEM and, in the leader, the pair
-//   MMAs; warps 2-5 / 6-9: softmax of group 0 / 1 on this CTA's 128 rows (S read from
-//   this CTA's TMEM, P written to this CTA's shared memory, O rescaled in TMEM).
-// Static order of the MMA stream, t = key tile of a group's item stream:
-//   S(0,0) S(1,0) | PV(0,0) S(0,1) | PV(1,0) S(1,1) | PV(0,1) S(0,2) | ...
-// K/V ring stage of (t, g) = position of S(g, t) in that order, modulo the ring depth.
-constexpr int AP_KVS = 4;
-constexpr int AP_Q_BYTES = AT_ROWS * 128;            // 128 rows x 64 columns: 16 KB
-constexpr int AP_K_BYTES = 64 * 128;                 // 64 keys x 64 columns: 8 KB
-constexpr int AP_V_BYTES = AT_KEYS * 64;             // 128 keys x 32 columns: 8 KB
-constexpr int AP_P_BYTES = AT_ROWS * AT_KEYS * 2;    // 32 KB
-constexpr int AP_OFF_Q = 0;                                  // [group][buffer]
-constexpr int AP_OFF_K = AP_OFF_Q + 2 * 2 * AP_Q_BYTES;      // 64 KB
-constexpr int AP_OFF_V = AP_OFF_K + AP_KVS * AP_K_BYTES;     // +32 KB
-constexpr int AP_OFF_P = AP_OFF_V + AP_KVS * AP_V_BYTES;     // +32 KB
-constexpr int AP_OFF_BAR = AP_OFF_P + 2 * AP_P_BYTES;        // +64 KB = 192 KB
-constexpr int AP_SMEM = AP_OFF_BAR + 512 + 1024;
-
-struct ApBars {
-    uint64_t q_full[2][2], q_empty[2][2];
-    uint64_t kv_full[AP_KVS], kv_empty[AP_KVS];
-    uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
-    uint64_t p_gather[2], o_gather[2];   // this CTA's four softmax warps of a group
-    uint64_t done;
-    uint32_t tmem_slot;
-    int abort_flag;
-};
-
-// Items of cluster c, group g: c * 2 + g, then every 2 * nclusters.
-__device__ __forceinline__ int ap_items(const AtParams& p, int cluster, int nclusters, int g) {
-    const int first = cluster * 2 + g;
-    return first < p.items ? (p.items - 1 - first) / (2 * nclusters) + 1 : 0;
-}
-
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(AT_THREADS, 1)
-attention_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const AtParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sQ = smem + AP_OFF_Q;
-    uint8_t* sK = smem + AP_OFF_K;
-    uint8_t* sV = smem + AP_OFF_V;
-    uint8_t* sP = smem + AP_OFF_P;
-    ApBars* bars = reinterpret_cast<ApBars*>(smem + AP_OFF_BAR);
-    volatile int* abort_flag = &bars->abort_flag;
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = ptx::cluster_ctarank();
-    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
-    const int nit[2] = {ap_items(p, cluster, nclusters, 0), ap_items(p, cluster, nclusters, 1)};
-    const int nkt = p.nkt;
-    const int D = p.D;
-    // (t, g) sequence: position of S(g, t) = 2 t + g while both groups have tiles left,
-    // positions counted over existing tiles only.
-    const int tiles0 = nit[0] * nkt, tiles1 = nit[1] * nkt;
-    auto seq_pos = [&](int t, int g) -> uint32_t {   // tiles1 <= tiles0
-        return (uint32_t)(t < tiles1 ? 2 * t + g : tiles1 * 2 + (t - tiles1));
-    };
-
-    if (threadIdx.x == 0) {
-        for (int g = 0; g < 2; ++g)
-            for (int b = 0; b < 2; ++b) {
-                ptx::mbar_init(&bars->q_full[g][b], 1);
-                ptx::mbar_init(&bars->q_empty[g][b], 1);
-            }
-        for (int s = 0; s < AP_KVS; ++s) {
-            ptx::mbar_init(&bars->kv_full[s], 1);
-            ptx::mbar_init(&bars->kv_empty[s], 1);
-        }
-        for (int g = 0; g < 2; ++g) {
-            ptx::mbar_init(&bars->s_full[g], 1);
-            ptx::mbar_init(&bars->p_full[g], 2);     // one arrival per CTA and group
-            ptx::mbar_init(&bars->o_done[g], 1);
-            ptx::mbar_init(&bars->o_free[g], 2);
-            ptx::mbar_init(&bars->p_gather[g], 4);
-            ptx::mbar_init(&bars->o_gather[g], 4);
-        }
-        ptx::mbar_init(&bars->done, 1);
-        bars->abort_flag = 0;
-        ptx::fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmQ);
-        ptx::prefetch_tensormap(&tmK);
-        ptx::prefetch_tensormap(&tmV);
-    }
-    if (warp == 1) {
-        ptx::tmem_alloc_pair(&bars->tmem_slot, 512);
-        ptx::tmem_relinquish_pair();
-    }
-    ptx::tc_fence_before();
-    ptx::cluster_sync();   // barriers of both CTAs exist before any remote arrive
-    ptx::tc_fence_after();
-    const uint32_t tmem = bars->tmem_slot;   // S_g at 128 g, O_g at 256 + 128 g
-
-    auto leader = [&](const void* local) {   // shared::cluster address in the leader CTA
-        return ptx::mapa_shared(ptx::smem_addr(local), 0);
-    };
-
-    if (warp == 0 || warp >= 10) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producers (both CTAs)
-            const int role = warp == 0 ? 0 : warp - 9;   // 0 Q, 1 K, 2 V
-            bool ok = true;
-            if (role == 0) {
-                int u_of[2] = {0, 0};
-                for (int u = 0; ok && (u < nit[0] || u < nit[1]); ++u)
-                    for (int g = 0; g < 2 && ok; ++g) {
-                        if (u >= nit[g]) continue;
-                        const int item = cluster * 2 + g + u * 2 * nclusters;
-                        int n, h, q0, nact;
-                        item_decode(p, item, n, h, q0, nact);
-                        const int b = u & 1;
-                        if (!ptx::mbar_wait_bounded(&bars->q_empty[g][b], ((u >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(&bars->q_full[g][b], 2 * AP_Q_BYTES);
-                        ptx::tma_load_3d_pair(sQ + (g * 2 + b) * AP_Q_BYTES, &tmQ, leader(&bars->q_full[g][b]),
-                                              h * 64, q0 + (int)rank * AT_ROWS, n);
-                        ++u_of[g];
-                    }
-                if (rank == 0)
-                    for (int g = 0; g < 2; ++g)
-                        for (int b = 0; b < 2; ++b)
-                            if (u_of[g] > b && !ptx::mbar_wait_bounded(&bars->q_full[g][b], (((u_of[g] - 1 - b) / 2) & 1), nullptr))
-                                at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-            } else {
-                uint32_t pos = 0;
-                const int tmax = tiles0 > tiles1 ? tiles0 : tiles1;
-                for (int t = 0; t < tmax && ok; ++t)
-                    for (int g = 0; g < 2 && ok; ++g) {
-                        if (t >= (g ? tiles1 : tiles0)) continue;
-                        const int item = cluster * 2 + g + (t / nkt) * 2 * nclusters;
-                        const int j = t % nkt;
-                        int n, h, q0, nact;
-                        item_decode(p, item, n, h, q0, nact);
-                        const uint32_t st = pos % AP_KVS, u = pos / AP_KVS;
-                        ++pos;
-                        if (!ptx::mbar_wait_bounded(&bars->kv_empty[st], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
-                        const uint32_t fb = leader(&bars->kv_full[st]);
-                        if (role == 1) {
-                            if (rank == 0) ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * (AP_K_BYTES + AP_V_BYTES));
-                            ptx::tma_load_3d_pair(sK + st * AP_K_BYTES, &tmK, fb, D + h * 64,
-                                                  j * AT_KEYS + (int)rank * 64, n);
-                        } else {
-                            ptx::tma_load_3d_pair(sV + st * AP_V_BYTES, &tmV, fb, 2 * D + h * 64 + (int)rank * 32,
-                                                  j * AT_KEYS, n);
-                        }
-                    }
-                if (role == 1 && rank == 0)
-                    for (uint32_t s = 0; s < AP_KVS; ++s)
-                        if (pos > s && !ptx::mbar_wait_bounded(&bars->kv_full[s], ((pos - 1 - s) / AP_KVS) & 1, nullptr))
-                            at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-            }
-            if (!ok) {
-                at_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
-                *abort_flag = 1;
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------------------ pair MMA issuer
-            constexpr uint32_t idS = ptx::idesc_bf16_f32(2 * AT_ROWS, AT_KEYS, false, false);
-            constexpr uint32_t idO = ptx::idesc_bf16_f32(2 * AT_ROWS, 64, false, true);
-            uint32_t sc[2] = {0, 0}, pc[2] = {0, 0};
-            bool ok = true;
-            auto issue_S = [&](int g, int t) -> bool {
-                const uint32_t pos = seq_pos(t, g);
-                const uint32_t st = pos % AP_KVS, u = pos / AP_KVS;
-                const int uu = t / nkt;   // item of this group
-                if (t % nkt == 0 &&
-                    !ptx::mbar_wait_bounded(&bars->q_full[g][uu & 1], (uu >> 1) & 1, abort_flag)) return false;
-                if (!ptx::mbar_wait_bounded(&bars->kv_full[st], u & 1, abort_flag)) return false;
-                // S_g is free: S(g, t) follows P.V(g, t - 1), which waited for p_full
-                ptx::tc_fence_after();
-                const uint32_t qa = ptx::smem_addr(sQ + (g * 2 + (uu & 1)) * AP_Q_BYTES);
-                const uint32_t ka = ptx::smem_addr(sK + st * AP_K_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = ptx::smem_desc(qa + kk * 32, 16, 1024, ptx::kLayoutSw128);
-                    const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 1024, ptx::kLayoutSw128);
-                    ptx::mma_bf16_ss_pair(tmem + g * AT_KEYS, ad, bd, idS, kk > 0);
-                }
-                ptx::mma_commit_pair_mc(&bars->s_full[g], 0x3);
-                if (t % nkt == nkt - 1) ptx::mma_commit_pair_mc(&bars->q_empty[g][uu & 1], 0x3);
-                ++sc[g];
-                return true;
-            };
-            auto issue_PV = [&](int g, int t) -> bool {
-                const uint32_t pos = seq_pos(t, g);
-                const uint32_t st = pos % AP_KVS;
-                const int uu = t / nkt;
-                if (!ptx::mbar_wait_bounded(&bars->p_full[g], pc[g] & 1, abort_flag)) return false;
-                if (t % nkt == 0 && uu > 0 &&
-                    !ptx::mbar_wait_bounded(&bars->o_free[g], (uu - 1) & 1, abort_flag)) return false;
-                ptx::tc_fence_after();
-                const uint32_t pa = ptx::smem_addr(sP + g * AP_P_BYTES);
-                const uint32_t va = ptx::smem_addr(sV + st * AP_V_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < AT_KEYS / 16; ++kk) {
-                    const uint64_t ad = ptx::smem_desc(pa + (kk >> 2) * (AT_ROWS * 128) + (kk & 3) * 32, 16, 1024,
-                                                       ptx::kLayoutSw128);
-                    // V half: 32 columns = 64-byte rows, 16 keys = 1 KB, 8-row groups 512 B apart
-                    const uint64_t bd = ptx::smem_desc(va + kk * 1024, 16, 512, ptx::kLayoutSw64);
-                    ptx::mma_bf16_ss_pair(tmem + 256 + g * 128, ad, bd, idO, (t % nkt > 0 || kk > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit_pair_mc(&bars->o_done[g], 0x3);
-                ptx::mma_commit_pair_mc(&bars->kv_empty[st], 0x3);
-                ++pc[g];
-                return true;
-            };
-            if (tiles0 > 0) ok = issue_S(0, 0);
-            if (ok && tiles1 > 0) ok = issue_S(1, 0);
-            const int tmax = tiles0 > tiles1 ? tiles0 : tiles1;
-            for (int t = 0; t < tmax && ok; ++t)
-                for (int g = 0; g < 2 && ok; ++g) {
-                    const int tg = g ? tiles1 : tiles0;
-                    if (t >= tg) continue;
-                    ok = issue_PV(g, t);
-                    if (ok && t + 1 < tg) ok = issue_S(g, t + 1);
-                }
-            if (!ok) {
-                at_error(p.err, ERRBIT_TIMEOUT_MMA);
-                *abort_flag = 1;
-            }
-            ptx::mma_commit_pair(&bars->done);
-            if (!ptx::mbar_wait_bounded(&bars->done, 0, nullptr)) at_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-        }
-    } else {
-        // -------------------------------------------------- softmax groups (both CTAs)
-        const int g = (warp - 2) >> 2;
-        const int quarter = warp & 3;
-        const int r = quarter * 32 + lane;                     // query row within this CTA's tile
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + g * AT_KEYS + lane_off;
-        const uint32_t tO = tmem + 256 + g * 128 + lane_off;
-        uint8_t* prow = sP + g * AP_P_BYTES + r * 128;
-        const uint32_t p_full0 = leader(&bars->p_full[g]);
-        const uint32_t o_free0 = leader(&bars->o_free[g]);
-        // A cluster-scope arrive costs about a thousand cycles, so the group's four warps
-        // gather on a local barrier and one thread forwards a single arrive to the
-        // leader. `hand_off` returns false if the gather wait ran out.
-        uint32_t n_hand[2] = {0, 0};   // completed phases of p_gather / o_gather
-        auto hand_off = [&](uint64_t* gather, uint32_t& phase_count, uint32_t leader_bar) -> bool {
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(gather);
-            bool fine = true;
-            if (quarter == 0) {
-                fine = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(gather, phase_count & 1, abort_flag));
-                if (fine && lane == 0) ptx::mbar_arrive_cluster(leader_bar);
-            }
-            ++phase_count;
-            return fine;
-        };
-        const float sl2 = p.scale_log2;
-        uint32_t tt = 0;
-        bool ok = true;
-        for (int uu = 0; uu < nit[g] && ok; ++uu) {
-            const int item = cluster * 2 + g + uu * 2 * nclusters;
-            int n, h, q0, nact;
-            item_decode(p, item, n, h, q0, nact);
-            const int row_base = q0 + (int)rank * AT_ROWS;     // first query row of this CTA
-            const bool live = row_base + quarter * 32 < p.T;
-            float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < nkt; ++j, ++tt) {
-                ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->s_full[g], tt & 1, abort_flag));
-                if (!ok) break;
-                if (j > 0) {
-                    ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
-                    if (!ok) break;
-                }
-                ptx::tc_fence_after();
-                if (live) {
-                    const int valid = min(AT_KEYS, p.T - j * AT_KEYS);
-                    uint32_t sv[AT_KEYS];
-#pragma unroll
-                    for (int c = 0; c < AT_KEYS / 32; ++c)
-                        ptx::tmem_ld_32x32b_x32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-                    ptx::tmem_ld_wait();
-                    if (valid < AT_KEYS) {
-#pragma unroll
-                        for (int e = 0; e < AT_KEYS; ++e)
-                            if (e >= valid) sv[e] = __float_as_uint(-INFINITY);
-                    }
-                    float mx[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) mx[e] = __uint_as_float(sv[e]);
-#pragma unroll
-                    for (int e = 8; e < AT_KEYS; ++e) mx[e & 7] = fmaxf(mx[e & 7], __uint_as_float(sv[e]));
-                    const float mrow = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    const float m_new = fmaxf(m, mrow * sl2);
-                    const float alpha = exp2_approx(m - m_new);
-                    if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t ov[16];
-                            ptx::tmem_ld_32x32b_x16(tO + c * 16, ov);
-                            ptx::tmem_ld_wait();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                            ptx::tmem_st_32x32b_x16(tO + c * 16, ov);
-                        }
-                        ptx::tmem_st_wait();
-                    }
-                    m = m_new;
-                    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int c = 0; c < AT_KEYS / 32; ++c) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            const float p0 = exp2_approx(fmaf(__uint_as_float(sv[c * 32 + e]), sl2, -m));
-                            const float p1 = exp2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 1]), sl2, -m));
-                            ls[(e >> 1) & 7] += p0 + p1;
-                            pk[e >> 1] = pack_bf16x2(p0, p1);
-                        }
-                        uint8_t* base = prow + (c >> 1) * (AT_ROWS * 128);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int unit = (c & 1) * 4 + q;
-                            *reinterpret_cast<uint4*>(base + ((unit ^ (r & 7)) << 4)) =
-                                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-                        }
-                    }
-                    l = l * alpha + (((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7])));
-                }
-                ptx::tc_fence_before();
-                ptx::fence_proxy_async_smem();
-                ok = hand_off(&bars->p_gather[g], n_hand[0], p_full0);
-                if (!ok) break;
-            }
-            if (!ok) break;
-            ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded(&bars->o_done[g], (tt - 1) & 1, abort_flag));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            if (live) {
-                uint32_t ov[64];
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    ptx::tmem_ld_32x32b_x16(tO + c * 16, *reinterpret_cast<uint32_t(*)[16]>(&ov[c * 16]));
-                ptx::tmem_ld_wait();
-                const float inv = 1.f / l;
-                const int t_row = row_base + r;
-                if (t_row < p.T) {
-                    __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t_row) * D + h * 64;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
-                        *reinterpret_cast<uint4*>(orow + c * 8) = w;
-                    }
-                }
-            }
-            ptx::tc_fence_before();
-            ok = hand_off(&bars->o_gather[g], n_hand[1], o_free0);
-        }
-        if (!ok) {
-            if (lane == 0) at_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
-            *abort_flag = 1;
-        }
-    }
-
-    __syncthreads();
-    ptx::cluster_sync();   // neither CTA leaves while its peer may still touch its memory
-    if (warp == 1) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc_pair(tmem, 512);
-    }
-}
-
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -884,60 +501,6 @@ cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_pair64(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                          const DeviceInfo& dev, cudaStream_t s) {
-    EncodeTiledFn fn = at_encode_fn();
-    if (!fn) return cudaErrorNotSupported;
-    alignas(64) CUtensorMap tq, tk, tv;
-    cuuint64_t dims[3] = {(cuuint64_t)(3 * D), (cuuint64_t)T, (cuuint64_t)N};
-    cuuint64_t strides[2] = {(cuuint64_t)(3 * D * 2), (cuuint64_t)(T * 3 * D * 2)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    cuuint32_t bq[3] = {64, AT_ROWS, 1}, bk[3] = {64, 64, 1}, bv[3] = {32, AT_KEYS, 1};
-    if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, bq, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-        fn(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, bk, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-        fn(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, bv, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    AtParams p;
-    p.tail_maps = 0;
-    p.N = (int)N;
-    p.T = (int)T;
-    p.D = (int)D;
-    p.H = (int)H;
-    const int qt = (int)((T + AT_ROWS - 1) / AT_ROWS);
-    p.npairs = (qt + 1) / 2;
-    p.nkt = (int)((T + AT_KEYS - 1) / AT_KEYS);
-    p.items = (int)(N * H * p.npairs);
-    p.scale_log2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
-    p.o = static_cast<__nv_bfloat16*>(o);
-    p.err = dev.err_word;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             AP_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    const int64_t clusters_needed = (p.items + 1) / 2;
-    const int64_t clusters = clusters_needed < dev.num_sms / 2 ? clusters_needed : dev.num_sms / 2;
-    if (clusters < 1) return cudaErrorInvalidValue;
-    attention_pair_kernel<<<(unsigned)(2 * clusters), AT_THREADS, AP_SMEM, s>>>(tq, tk, tv, p);
-    return cudaGetLastError();
-}
-
-// The single-CTA kernel is the default: at T = 197 (two key tiles per item) the pair
-// kernel's cross-SM hand-offs cost more than its faster MMAs save. VIT_ATTN_PAIR=1
-// selects the pair kernel.
-bool use_pair_attention() {
-    const char* e = std::getenv("VIT_ATTN_PAIR");
-    return e && e[0] == '1';
-}
-
 }  // namespace
 
 bool attention_tc_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o) {
@@ -957,7 +520,6 @@ cudaError_t launch_attention_tc(const void* qkv, void* o, int64_t N, int64_t T, 
     switch (D / H) {
         case 64:
             if (attention_whole_supported(T, D, H)) return launch_attention_whole(qkv, o, N, T, D, H, dev, s);
-            if (use_pair_attention() && dev.num_sms >= 2) return launch_pair64(qkv, o, N, T, D, H, dev, s);
             return launch_tc_dh<64, true>(qkv, o, N, T, D, H, dev, s);
         case 80: return launch_tc_dh<80, false>(qkv, o, N, T, D, H, dev, s);
     }

@@ -25,8 +25,6 @@
 //                     TMA store; residual tiles arrive by TMA one chunk ahead.
 // GEMMs whose tiles fill at most half of the CTA pairs split K over the pairs and reduce
 // the fp32 slices in a second kernel that applies the epilogue.
-// gemm_tc_kernel, a single-CTA variant (M 128 x N 256 tiles, one producer warp, four
-// epilogue warps with direct vector stores), is selected with VIT_GEMM_PAIR=0.
 // The weights are read in their (in, out) storage order directly: the B operand is
 // MN-major, so no transposed copy is made. Every wait is bounded; on expiry the
 // kernel sets a bit in the device error word, lets its copies and MMAs drain, frees
@@ -47,16 +45,11 @@ namespace vit {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;        // 16 KB
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int B_BOX_BYTES = 64 * BK * 2;    // 8 KB: 64 N columns x 64 K rows
-constexpr int B_BYTES = BN * BK * 2;        // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;                // fp32 columns per accumulator
 constexpr int TMEM_COLS = 2 * ACC_COLS;     // double-buffered
-constexpr int THREADS = 192;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
 
 struct Params {
     int M, N, K;
@@ -97,237 +90,9 @@ __device__ __forceinline__ void load32(const float* p, float (&v)[32]) {
     }
 }
 
-__device__ __forceinline__ void store32(__nv_bfloat16* p, const float (&v)[32]) {
-    uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 u;
-        u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-        u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-        u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-        u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-        q[i] = u;
-    }
-}
-
-__device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
-    float4* q = reinterpret_cast<float4*>(p);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
     if (err) atomicOr(err, bit);
 }
-
-
-// Epilogue of one 128 x 256 accumulator: this thread owns output row `row` and reads
-// its 256 fp32 columns from TMEM (lane row, columns from t_row) 32 at a time.
-template <int EPI, typename OutT, typename ResT>
-__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t t_row, int row, int n0) {
-#pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
-        ptx::tmem_ld_wait();
-        const int col = n0 + c * 32;
-        if (row < p.M && col < p.N) {
-            float val[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) val[j] = __uint_as_float(r[j]);
-            if (p.bias) {
-                float b[32];
-                load32(p.bias + col, b);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] += b[j];
-            }
-            if (EPI == TC_EPI_GELU) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] = gelu_tanh_fast(val[j]);
-            } else if (EPI == TC_EPI_RESID) {
-                float rv[32];
-                load32(reinterpret_cast<const ResT*>(p.residual) + (int64_t)row * p.ldr + col, rv);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) val[j] += rv[j];
-            }
-            store32(reinterpret_cast<OutT*>(p.out) + (int64_t)row * p.ldo + col, val);
-        }
-    }
-}
-
-template <int EPI, typename OutT, typename ResT>
-__global__ void __launch_bounds__(THREADS, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-               const Params p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + STAGES * A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* done = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tiles = (p.M + BM - 1) / BM;
-    const int n_tiles = (p.N + BN - 1) / BN;
-    const int num_tiles = m_tiles * n_tiles;
-    const int kblocks = p.K / BK;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full + s, 1);
-            ptx::mbar_init(empty + s, 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            ptx::mbar_init(tfull + a, 1);
-            ptx::mbar_init(tempty + a, 128);
-        }
-        ptx::mbar_init(done, 1);
-        *abort_flag = 0;
-        ptx::fence_mbar_init();
-    }
-    if (warp == 0 && lane == 0) {
-        ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB0);
-        if (p.n_w > 1) ptx::prefetch_tensormap(&tmB1);
-        if (p.n_w > 2) ptx::prefetch_tensormap(&tmB2);
-    }
-    if (warp == 1) {
-        ptx::tmem_alloc(tmem_slot, TMEM_COLS);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem_base = *tmem_slot;
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int m0 = (tile / n_tiles) * BM;
-                const int n0 = (tile % n_tiles) * BN;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, u = it / STAGES;
-                    if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(full + s, STAGE_BYTES);
-                    ptx::tma_load_2d(sA + s * A_BYTES, &tmA, full + s, kb * BK, m0);
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j) {
-                        const int col = n0 + 64 * j;
-                        int wi = col / p.n_per_w;
-                        if (wi > p.n_w - 1) wi = p.n_w - 1;  // past N: zero-filled box
-                        const int lc = col - wi * p.n_per_w;
-                        const CUtensorMap* tb = wi == 0 ? &tmB0 : (wi == 1 ? &tmB1 : &tmB2);
-                        ptx::tma_load_2d(sB + s * B_BYTES + j * B_BOX_BYTES, tb, full + s, lc,
-                                         kb * BK);
-                    }
-                }
-            }
-            if (!ok) {
-                set_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
-                *abort_flag = 1;
-            }
-            // Let every copy this thread issued land before the CTA can exit.
-            for (uint32_t s = 0; s < STAGES; ++s) {
-                if (it > s) {
-                    const uint32_t u_last = (it - 1 - s) / STAGES;
-                    if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
-                        set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-                }
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, false, true);
-            uint32_t it = 0;
-            int local = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-                const int acc = local & 1;
-                const uint32_t v = (uint32_t)(local >> 1);
-                if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * ACC_COLS;
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const uint32_t s = it % STAGES, u = it / STAGES;
-                    if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t a_base = ptx::smem_addr(sA + s * A_BYTES);
-                    const uint32_t b_base = ptx::smem_addr(sB + s * B_BYTES);
-#pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
-                        const uint64_t adesc = ptx::smem_desc_sw128(a_base + k * 32, 16, 1024);
-                        // B: MN-major, advance 16 K rows = 2 groups of 8 rows (2048 bytes);
-                        // 64-column chunks are B_BOX_BYTES apart.
-                        const uint64_t bdesc =
-                            ptx::smem_desc_sw128(b_base + k * 2048, B_BOX_BYTES, 1024);
-                        ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, (kb | k) != 0);
-                    }
-                    ptx::mma_commit(empty + s);
-                }
-                if (!ok) break;
-                ptx::mma_commit(tfull + acc);
-            }
-            if (!ok) {
-                set_error(p.err, ERRBIT_TIMEOUT_MMA);
-                *abort_flag = 1;
-            }
-            // Every MMA issued must finish before TMEM is released.
-            ptx::mma_commit(done);
-            if (!ptx::mbar_wait_bounded(done, 0, nullptr)) set_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
-        }
-    } else {
-        // ---------------------------------------------------- epilogue warps 2..5
-        const int quarter = warp & 3;  // TMEM lane quarter this warp may read
-        int local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-            const int acc = local & 1;
-            const uint32_t v = (uint32_t)(local >> 1);
-            // The TMEM loads below are warp-collective: the whole warp goes on or stops.
-            const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
-            if (!ok) {
-                if (lane == 0) set_error(p.err, ERRBIT_TIMEOUT_EPILOGUE);
-                *abort_flag = 1;
-                break;
-            }
-            ptx::tc_fence_after();
-            const int m0 = (tile / n_tiles) * BM;
-            const int n0 = (tile % n_tiles) * BN;
-            const int row = m0 + quarter * 32 + lane;
-            const uint32_t t_row = tmem_base + acc * ACC_COLS + ((uint32_t)(quarter * 32) << 16);
-            epilogue_tile<EPI, OutT, ResT>(p, t_row, row, n0);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(tempty + acc);
-        }
-    }
-
-    __syncthreads();
-    if (warp == 1) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, TMEM_COLS);
-    }
-}
-
 
 
 // Residual values of 32 columns of one row (nothing for other epilogues or past M/N).
@@ -879,20 +644,6 @@ bool make_map_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_
     return r == CUDA_SUCCESS;
 }
 
-template <int EPI, typename OutT, typename ResT>
-cudaError_t launch_inst(const CUtensorMap& a, const CUtensorMap* b, const Params& p, int grid,
-                        cudaStream_t s) {
-    auto k = gemm_tc_kernel<EPI, OutT, ResT>;
-    static bool attr_set = false;  // per instantiation; idempotent, so a race is harmless
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    k<<<grid, THREADS, SMEM_BYTES, s>>>(a, b[0], b[1], b[2], p);
-    return cudaGetLastError();
-}
-
 template <int EPI, typename OutT, typename ResT, bool FOLD, bool EXTRA>
 cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
                              const CUtensorMap& out2, const CUtensorMap& res, const Params& p, int grid,
@@ -909,25 +660,14 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const C
 }
 
 template <int EPI, typename OutT, typename ResT>
-cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
+cudaError_t launch_any(const CUtensorMap& a, const CUtensorMap* b, const CUtensorMap& out,
                        const CUtensorMap& out2, const CUtensorMap& res, const Params& p, int grid,
                        cudaStream_t s) {
-    if (!pair) return launch_inst<EPI, OutT, ResT>(a, b, p, grid, s);
     if (p.fold.parts)
         return launch_inst_pair<EPI, OutT, ResT, true, false>(a, b, out, out2, res, p, grid, s);
     if (p.parts_out)
         return launch_inst_pair<EPI, OutT, ResT, false, true>(a, b, out, out2, res, p, grid, s);
     return launch_inst_pair<EPI, OutT, ResT, false, false>(a, b, out, out2, res, p, grid, s);
-}
-
-// The CTA-pair kernel is the default; VIT_GEMM_PAIR=0 selects the single-CTA kernel.
-bool use_pair_kernel() {
-    static int v = -1;
-    if (v < 0) {
-        const char* e = std::getenv("VIT_GEMM_PAIR");
-        v = (e && e[0] == '0') ? 0 : 1;
-    }
-    return v == 1;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -952,7 +692,7 @@ SplitK split_k_for(int64_t M, int64_t N, int64_t K, int num_sms) {
     SplitK r;
     const int kblocks = (int)(K / BK);
     r.kb_per = kblocks;
-    if (!split_k_enabled() || !use_pair_kernel() || num_sms < 4) return r;
+    if (!split_k_enabled() || num_sms < 4) return r;
     const int64_t tiles = ((M + 2 * BM - 1) / (2 * BM)) * ((N + BN - 1) / BN);
     const int64_t pairs = num_sms / 2;
     if (tiles * 2 > pairs || kblocks < 4) return r;
@@ -1045,7 +785,7 @@ int64_t tc_split_ws_bytes(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev
     return sk.ksplit > 1 ? (int64_t)sk.ksplit * M * N * 4 : 0;
 }
 
-bool tc_pair_enabled(const DeviceInfo& dev) { return use_pair_kernel() && dev.num_sms >= 2; }
+bool tc_pair_enabled(const DeviceInfo& dev) { return dev.num_sms >= 2; }
 
 bool tc_gemm_supported(const TcGemmDesc& d) {
     if (d.M <= 0 || d.N <= 0 || d.K <= 0) return false;
@@ -1066,9 +806,9 @@ bool tc_gemm_supported(const TcGemmDesc& d) {
 cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStream_t s) {
     alignas(64) CUtensorMap ma;
     alignas(64) CUtensorMap mb[3];
-    const bool pair = use_pair_kernel() && dev.num_sms >= 2;
-    // the pair kernel loads A as two 64-row boxes from two warps
-    if (!make_map(&ma, d.a, d.M, d.K, d.lda, BK, pair ? BM / 2 : BM)) return cudaErrorInvalidValue;
+    if (dev.num_sms < 2) return cudaErrorNotSupported;   // CTA pairs need two SMs
+    // A is loaded as two 64-row boxes from two warps
+    if (!make_map(&ma, d.a, d.M, d.K, d.lda, BK, BM / 2)) return cudaErrorInvalidValue;
     for (int i = 0; i < 3; ++i) {
         const void* w = d.w[i < d.n_w ? i : 0];
         if (!make_map(&mb[i], w, d.K, d.n_per_w, d.n_per_w, 64, BK)) return cudaErrorInvalidValue;
@@ -1083,7 +823,7 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     // split K: raw fp32 slices into split_ws, then the reduction applies the epilogue
     SplitK sk;
     sk.kb_per = (int)(d.K / BK);
-    if (pair && !d.fold.parts && !d.extra.parts && d.split_ws && d.N % 64 == 0 && aligned16(d.split_ws)) {
+    if (!d.fold.parts && !d.extra.parts && d.split_ws && d.N % 64 == 0 && aligned16(d.split_ws)) {
         const SplitK c = split_k_for(d.M, d.N, d.K, dev.num_sms);
         if (c.ksplit > 1 && (int64_t)c.ksplit * d.M * d.N * 4 <= d.split_ws_bytes) sk = c;
     }
@@ -1091,7 +831,7 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     // residual tiles for the pair kernel's TMA-fed residual epilogue (same boxes and swizzle
     // as the output staging tiles)
     alignas(64) CUtensorMap mres = mo;
-    if (pair && d.epi == TC_EPI_RESID && sk.ksplit == 1 &&
+    if (d.epi == TC_EPI_RESID && sk.ksplit == 1 &&
         !make_map_out(&mres, const_cast<void*>(d.residual), d.M, d.N, d.ldr, d.residual_f32))
         return cudaErrorInvalidValue;
     Params p;
@@ -1111,18 +851,12 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     p.parts_stride = (int)(2 * ((d.N + BN - 1) / BN));
     p.ksplit = sk.ksplit;
     p.kb_per = sk.kb_per;
-    int grid;
-    if (pair) {
-        const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN) * sk.ksplit;
-        const int64_t clusters = tiles < dev.num_sms / 2 ? tiles : dev.num_sms / 2;
-        grid = (int)(2 * clusters);
-    } else {
-        const int64_t tiles = ((d.M + BM - 1) / BM) * ((d.N + BN - 1) / BN);
-        grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
-    }
+    const int64_t tiles = ((d.M + 2 * BM - 1) / (2 * BM)) * ((d.N + BN - 1) / BN) * sk.ksplit;
+    const int64_t clusters = tiles < dev.num_sms / 2 ? tiles : dev.num_sms / 2;
+    const int grid = (int)(2 * clusters);
     if (sk.ksplit > 1) {
         p.bias = nullptr;
-        cudaError_t e = launch_any<TC_EPI_STORE, float, float>(true, ma, mb, mo, mo2, mres, p, grid, s);
+        cudaError_t e = launch_any<TC_EPI_STORE, float, float>(ma, mb, mo, mo2, mres, p, grid, s);
         if (e != cudaSuccess) return e;
         switch (d.epi) {
             case TC_EPI_STORE:
@@ -1144,19 +878,19 @@ cudaError_t launch_gemm_tc(const TcGemmDesc& d, const DeviceInfo& dev, cudaStrea
     }
     switch (d.epi) {
         case TC_EPI_STORE:
-            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
-                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_STORE, float, float>(ma, mb, mo, mo2, mres, p, grid, s)
+                             : launch_any<TC_EPI_STORE, __nv_bfloat16, float>(ma, mb, mo, mo2, mres, p, grid, s);
         case TC_EPI_GELU:
-            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
-                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s);
+            return d.out_f32 ? launch_any<TC_EPI_GELU, float, float>(ma, mb, mo, mo2, mres, p, grid, s)
+                             : launch_any<TC_EPI_GELU, __nv_bfloat16, float>(ma, mb, mo, mo2, mres, p, grid, s);
         case TC_EPI_RESID:
             if (d.out_f32)
                 return d.residual_f32
-                           ? launch_any<TC_EPI_RESID, float, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
-                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(pair, ma, mb, mo, mo2, mres, p, grid, s);
+                           ? launch_any<TC_EPI_RESID, float, float>(ma, mb, mo, mo2, mres, p, grid, s)
+                           : launch_any<TC_EPI_RESID, float, __nv_bfloat16>(ma, mb, mo, mo2, mres, p, grid, s);
             return d.residual_f32
-                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(pair, ma, mb, mo, mo2, mres, p, grid, s)
-                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(pair, ma, mb, mo, mo2, mres, p, grid, s);
+                       ? launch_any<TC_EPI_RESID, __nv_bfloat16, float>(ma, mb, mo, mo2, mres, p, grid, s)
+                       : launch_any<TC_EPI_RESID, __nv_bfloat16, __nv_bfloat16>(ma, mb, mo, mo2, mres, p, grid, s);
     }
     return cudaErrorInvalidValue;
 }
