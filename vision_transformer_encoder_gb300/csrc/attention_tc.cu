@@ -14,7 +14,9 @@
 //               so the three streams come from three warps. A 3-D tensor map (column, token, sequence) zero-fills tokens past
 //               T, so tiles never read the next sequence. A head slice is one 64-column
 //               box with the 128-byte swizzle, plus, for dh = 80, one 16-column box with
-//               the 32-byte swizzle (the MMAs for that part use a second descriptor).
+//               the 32-byte swizzle for Q and K (the S MMAs for that part use a second
+//               descriptor) and a second 64-column box for V, so that P.V is one N 80 MMA
+//               per 16 keys over two MN-major atoms rather than an N 64 and an N 16 one.
 //   warp 1      MMA: S_g = Q_g K^T (M 128, N 128, K dh) into TMEM, then O_g += P_g V
 //               (M 128, N dh, K 128) with V read MN-major. S and O live in TMEM. For
 //               dh = 64, P also lives in TMEM (the MMA reads A from tensor memory), which
@@ -56,17 +58,22 @@ template <int DH, bool PT>
 struct AtLayout {
     static_assert(DH == 64 || DH == 80, "head width 64 or 80");
     static constexpr bool TAIL = DH == 80;          // a 16-column second box
-    static constexpr int TILE = AT_BOX64 + (TAIL ? AT_BOX16 : 0);   // one Q, K or V tile
+    static constexpr int TILE = AT_BOX64 + (TAIL ? AT_BOX16 : 0);   // one Q or K tile
+    // one V tile: for dh = 80 two 64-column boxes with the 128-byte swizzle (the second
+    // holds columns 64..79 and 48 columns the MMA does not read), so that one N 80 MMA per
+    // 16 keys reads V as two MN-major atoms
+    static constexpr int VTILE = TAIL ? 2 * AT_BOX64 : AT_BOX64;
     static constexpr int QBUF = PT ? 2 : 1;         // query-pair buffers
     static constexpr int KVS = PT ? 4 : 2;          // K/V ring stages
     static constexpr int P_BYTES = PT ? 0 : AT_ROWS * AT_KEYS * 2;
     static constexpr int OFF_Q = 0;                 // QBUF x 2 query tiles
     static constexpr int OFF_K = OFF_Q + QBUF * 2 * TILE;
     static constexpr int OFF_V = OFF_K + KVS * TILE;
-    static constexpr int OFF_P = OFF_V + KVS * TILE;   // 2 groups (if staged)
+    static constexpr int OFF_P = OFF_V + KVS * VTILE;  // 2 groups (if staged)
     static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
     static constexpr int SMEM = OFF_BAR + 512 + 1024;
     static_assert(KVS <= AT_MAX_KV, "ring too deep");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(!PT || DH <= 64, "O and P share a 128-column TMEM slot");
 };
 
@@ -183,10 +190,15 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
                 for (int j = 0; j < p.nkt; ++j, ++kv_it) {
                     const uint32_t st = kv_it % KVS, u = kv_it / KVS;
                     if (!ptx::mbar_wait_bounded(&bars->kv_empty[st], (u & 1) ^ 1, abort_flag)) { ok = false; break; }
-                    if (role == 1) ptx::mbar_arrive_expect_tx(&bars->kv_full[st], 2 * L::TILE);
-                    uint8_t* dst = ring + st * L::TILE;
+                    if (role == 1) ptx::mbar_arrive_expect_tx(&bars->kv_full[st], L::TILE + L::VTILE);
+                    uint8_t* dst = ring + st * (role == 1 ? L::TILE : L::VTILE);
                     ptx::tma_load_3d(dst, &tm, &bars->kv_full[st], col, j * AT_KEYS, n);
-                    if (L::TAIL) ptx::tma_load_3d(dst + AT_BOX64, &tm16, &bars->kv_full[st], col + 64, j * AT_KEYS, n);
+                    if (L::TAIL) {
+                        if (role == 1)
+                            ptx::tma_load_3d(dst + AT_BOX64, &tm16, &bars->kv_full[st], col + 64, j * AT_KEYS, n);
+                        else   // columns past the last head's 80 read as zero
+                            ptx::tma_load_3d(dst + AT_BOX64, &tm, &bars->kv_full[st], col + 64, j * AT_KEYS, n);
+                    }
                 }
             }
             if (!ok) {
@@ -209,7 +221,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t idS = ptx::idesc_bf16_f32(AT_ROWS, AT_KEYS, false, false);
             constexpr uint32_t idO64 = ptx::idesc_bf16_f32(AT_ROWS, 64, false, true);
-            constexpr uint32_t idO16 = ptx::idesc_bf16_f32(AT_ROWS, 16, false, true);
+            constexpr uint32_t idO80 = ptx::idesc_bf16_f32(AT_ROWS, 80, false, true);
             uint32_t kv_base = 0, ii = 0;
             uint32_t sc[2] = {0, 0}, pc[2] = {0, 0}, ic[2] = {0, 0};
             bool ok = true;
@@ -252,7 +264,7 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
                         if (j == 0 && ic[g] > 0 &&
                             !ptx::mbar_wait_bounded(&bars->o_free[g], (ic[g] - 1) & 1, abort_flag)) { ok = false; break; }
                         ptx::tc_fence_after();
-                        const uint32_t va = ptx::smem_addr(sV + st * L::TILE);
+                        const uint32_t va = ptx::smem_addr(sV + st * L::VTILE);
                         const uint32_t tO = tmem + 256 + g * 128;
 #pragma unroll
                         for (int kk = 0; kk < AT_KEYS / 16; ++kk) {
@@ -267,12 +279,12 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
                                 const uint32_t pa = ptx::smem_addr(sP + g * L::P_BYTES);
                                 const uint64_t ad = ptx::smem_desc(pa + (kk >> 2) * (AT_ROWS * 128) + (kk & 3) * 32,
                                                                    16, 1024, ptx::kLayoutSw128);
-                                ptx::mma_bf16_ss(tO, ad, bd, idO64, acc);
                                 if (L::TAIL) {
-                                    // head columns 64..79 from the 16-column box (32-byte rows)
-                                    const uint64_t bt = ptx::smem_desc(va + AT_BOX64 + kk * 512, 16, 256,
-                                                                       ptx::kLayoutSw32);
-                                    ptx::mma_bf16_ss(tO + 64, ad, bt, idO16, acc);
+                                    // N 80: two MN-major atoms of 64 columns, a box (16 KB) apart
+                                    const uint64_t b80 = ptx::smem_desc(va + kk * 2048, AT_BOX64, 1024, ptx::kLayoutSw128);
+                                    ptx::mma_bf16_ss(tO, ad, b80, idO80, acc);
+                                } else {
+                                    ptx::mma_bf16_ss(tO, ad, bd, idO64, acc);
                                 }
                             }
                         }
