@@ -191,6 +191,81 @@ int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* l
                 const void* lnf_b, int final_ln, int64_t N, int64_t T, int64_t D, int64_t F,
                 int64_t H, double eps, int dtype, void* out, void* stream);
 
+/* ------------------------------------------------------------------------------
+ * Prepared weights: one block's weights held on the device across calls.
+ * ------------------------------------------------------------------------------ */
+
+/*
+ * vit_weights_create -- copies one block's weights into device memory owned by the
+ * library (on the current device) and prepares, once, what depends on the weights alone,
+ * so that repeated calls of vit_block_w / vit_block_w_host neither copy nor recompute it:
+ *  - the concatenated [b_q | b_k | b_v] of the fused QKV product, when any is given;
+ *  - with the LayerNorm fold, the per-column terms of "ViT Encoder Block"
+ *    (ai-engineer-exhaustive), Key Equations, Steps 1 and 4 (LayerNorm with gain and bias,
+ *    then a linear map): LN(x) @ W = rstd (x @ W' - mean c) + d with W' = diag(gamma) W,
+ *    c_j = sum_i W'_ij, d_j = sum_i beta_i W_ij + b_j, mean and rstd = 1/sqrt(var + eps)
+ *    of each row of x. Made for LN1 with [w_q | w_k | w_v] (b = [b_q | b_k | b_v]) and
+ *    for LN2 with w_mlp1 (b = b1); W' is stored in bf16 and c is summed from the rounded W'.
+ *
+ *   layer      a vit_layer record (as in vit_encoder): the six weights required, the ten
+ *              gains and biases nullable (absent = gain 1, bias 0); all in `dtype`
+ *   from_host  1: the record's pointers are host pointers (pinned or pageable);
+ *              0: device pointers on the current device
+ *   D, F, H, dtype  as vit_block; the handle serves any N, T and eps
+ *   fold       1: blocks run with both LayerNorms folded into the QKV and W1 products
+ *                 (bf16 with the tensor-core GEMM only; VIT_ERR_UNSUPPORTED otherwise).
+ *                 A call whose x is not 16-byte aligned runs the plain path instead.
+ *              0: blocks run the plain path: results bit-identical to vit_encoder with
+ *                 this one layer and no final LayerNorm (to vit_block_ex when the four
+ *                 projection biases are absent)
+ *              -1: the library's choice, currently 0 (VIT_PREPARED_FOLD=1 makes it 1
+ *                 where available). On a GB300 the folded ViT-B/16 block measured about
+ *                 0.5 % faster, too little to make it the default: the fold subtracts
+ *                 mean * c after the product, which loses accuracy when a row's mean is
+ *                 large against its spread.
+ *   out        receives the handle; unchanged on error
+ *   stream     the copies and the preparation are enqueued on it, and the call
+ *              synchronises it before returning: the caller may then free or change
+ *              its arrays
+ * Memory: 2 (4 D^2 + 2 D F) bytes of bf16 weights (4 for fp32) plus the gains and biases;
+ * with the fold another 8 (3 D + F) bytes and, with LN gains, 2 (3 D^2 + D F) bytes.
+ * Errors: VIT_ERR_ARG (null layer/out/weight, bad sizes, from_host or fold out of range),
+ * VIT_ERR_DTYPE, VIT_ERR_NOMEM, VIT_ERR_CUDA, VIT_ERR_UNSUPPORTED.
+ */
+typedef struct vit_weights_s vit_weights;
+
+int vit_weights_create(const vit_layer* layer, int from_host, int64_t D, int64_t F, int64_t H,
+                       int dtype, int fold, vit_weights** out, void* stream);
+
+/* vit_weights_destroy -- frees the handle and its device memory (cudaFree, which waits
+ * for work on the device). NULL is accepted. The handle must not be in use. */
+int vit_weights_destroy(vit_weights* w);
+
+/* vit_weights_info -- the handle's sizes, dtype, whether it runs the fold (1/0) and its
+ * device; each output pointer nullable. VIT_ERR_ARG for a null handle. */
+int vit_weights_info(const vit_weights* w, int64_t* D, int64_t* F, int64_t* H, int* dtype,
+                     int* fold, int* device);
+
+/*
+ * vit_block_w -- one block on prepared weights: vit_block_ex plus the projection biases
+ * b_q, b_k, b_v and b_o of the handle's layer (the block of vit_encoder).
+ *   x, out    (N, T, D) device arrays in the handle's dtype, on the handle's device (which
+ *             must be current); out must not overlap x
+ *   eps       LN epsilon, as vit_block
+ * Errors as vit_block; VIT_ERR_ARG also for a null handle or another current device.
+ */
+int vit_block_w(const void* x, const vit_weights* w, int64_t N, int64_t T, double eps,
+                void* out, void* stream);
+
+/*
+ * vit_block_w_host -- vit_block_w on HOST x and out, with the pipeline of vit_block_host
+ * (chunks of whole sequences; copy in, block and copy out overlapped on library streams;
+ * `stream` synchronised before returning). Only x and out cross the host link: the
+ * weights stay on the device. Results equal vit_block_w's on the same batch, bit for bit.
+ */
+int vit_block_w_host(const void* x_host, const vit_weights* w, int64_t N, int64_t T, double eps,
+                     void* out_host, void* stream);
+
 /*
  * vit_block_cls -- one block computed for the CLS row (row 0 of each sequence) alone.
  *

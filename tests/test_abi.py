@@ -152,3 +152,25 @@ def test_selftest_without_a_device_reports_a_cuda_error(lib):
         pytest.skip("a CUDA device is present; tests/test_gpu_failure.py covers it")
     assert lib.vit_selftest_wait(0, None) == -3
     assert lib.vit_selftest_wait(1, None) == -3
+
+
+def test_prepared_weights_argument_checks(lib):
+    layer = api.VitLayer(*[_fake(i + 1).value for i in range(6)] + [None] * 10)
+    arr = (api.VitLayer * 1)(layer)
+    h = ctypes.c_void_p()
+    create = lib.vit_weights_create
+    assert create(None, 0, 8, 16, 2, 1, -1, ctypes.byref(h), None) == -1          # no layer
+    assert create(arr, 0, 8, 16, 2, 1, -1, None, None) == -1                      # no out
+    assert create(arr, 0, 8, 16, 3, 1, -1, ctypes.byref(h), None) == -1          # H does not divide D
+    assert create(arr, 0, 0, 16, 2, 1, -1, ctypes.byref(h), None) == -1
+    assert create(arr, 0, 8, 16, 2, 7, -1, ctypes.byref(h), None) == -2          # dtype
+    assert create(arr, 2, 8, 16, 2, 1, -1, ctypes.byref(h), None) == -1          # from_host
+    assert create(arr, 0, 8, 16, 2, 1, 2, ctypes.byref(h), None) == -1           # fold
+    bad = (api.VitLayer * 1)(api.VitLayer(*[_fake(i + 1).value for i in range(5)] + [None] * 11))
+    assert create(bad, 0, 8, 16, 2, 1, -1, ctypes.byref(h), None) == -1          # null w_mlp2
+    assert not h.value                                                            # untouched
+    # a null handle: every call that takes one rejects it before touching the GPU
+    assert lib.vit_block_w(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
+    assert lib.vit_block_w_host(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
+    assert lib.vit_weights_info(None, None, None, None, None, None, None) == -1
+    assert lib.vit_weights_destroy(None) == 0

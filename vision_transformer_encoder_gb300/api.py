@@ -46,6 +46,13 @@ SIGNATURES = {
     "vit_layernorm": (_int, [_vp, _i64, _i64, _dbl, _vp, _vp, _int, _vp, _int, _vp]),
     "vit_linear": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _int, _vp, _int, _vp]),
     "vit_attention": (_int, [_vp, _i64, _i64, _i64, _i64, _int, _vp, _vp]),
+    "vit_weights_create": (_int, [ctypes.POINTER(VitLayer), _int, _i64, _i64, _i64, _int, _int,
+                                  ctypes.POINTER(_vp), _vp]),
+    "vit_weights_destroy": (_int, [_vp]),
+    "vit_weights_info": (_int, [_vp, ctypes.POINTER(_i64), ctypes.POINTER(_i64), ctypes.POINTER(_i64),
+                                ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "vit_block_w": (_int, [_vp, _vp, _i64, _i64, _dbl, _vp, _vp]),
+    "vit_block_w_host": (_int, [_vp, _vp, _i64, _i64, _dbl, _vp, _vp]),
     "vit_status_string": (ctypes.c_char_p, [_int]),
     "vit_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "vit_launch_count": (_i64, []),
@@ -260,6 +267,97 @@ def vit_block_host(x, w_q, w_k, w_v, w_o, w_mlp1, w_mlp2, H, eps, ln1_g=None, ln
         rc = lib.vit_block_host(*[_ptr(t) for t in ts], N, T, D, F, int(H), float(eps),
                                 _dtype_code(dt), _ptr(out), _stream(stream))
     _check(rc, "vit_block_host")
+    return out
+
+
+class VitWeights:
+    """One block's weights prepared on a device (vit_weights_create): copied once, with
+    the concatenated Q/K/V bias and, when folding, the LayerNorm fold's column terms.
+
+    layer: dict keyed by LAYER_FIELDS (the six weights required), all CUDA tensors on
+    one device, or all host tensors (then copied to `device`). fold: 1 / 0 / -1 (the
+    library's choice). The handle is freed by close() or when the object is collected."""
+
+    def __init__(self, layer, H, fold=-1, device=None, stream=None):
+        lib = load_library()
+        w_q = layer["w_q"]
+        dt = w_q.dtype
+        on_host = not w_q.is_cuda
+        arr = (VitLayer * 1)()
+        for name in LAYER_FIELDS:
+            t = layer.get(name)
+            if t is None:
+                continue
+            if t.is_cuda == on_host or not t.is_contiguous() or t.dtype != dt:
+                raise ValueError("layer %s: all tensors contiguous, of one dtype, all on the host "
+                                 "or all on one device" % name)
+            setattr(arr[0], name, t.data_ptr())
+        D, F = layer["w_mlp1"].shape
+        if device is None:
+            device = 0 if on_host else w_q.device.index
+        self._lib = lib
+        self._h = _vp()
+        self._layer = layer   # keeps the arrays alive until the copies are made
+        with torch.cuda.device(device):
+            rc = lib.vit_weights_create(arr, 1 if on_host else 0, D, F, int(H), _dtype_code(dt), int(fold),
+                                        ctypes.byref(self._h), _stream(stream))
+        self._layer = None
+        _check(rc, "vit_weights_create")
+        d, f, h = _i64(), _i64(), _i64()
+        code, fo, dev = _int(), _int(), _int()
+        _check(lib.vit_weights_info(self._h, ctypes.byref(d), ctypes.byref(f), ctypes.byref(h),
+                                    ctypes.byref(code), ctypes.byref(fo), ctypes.byref(dev)), "vit_weights_info")
+        self.D, self.F, self.H, self.fold, self.device = d.value, f.value, h.value, bool(fo.value), dev.value
+        self.dtype = dt
+
+    @property
+    def handle(self):
+        if not self._h:
+            raise ValueError("the prepared weights have been freed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            h, self._h = self._h, _vp()
+            _check(self._lib.vit_weights_destroy(h), "vit_weights_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def vit_block_w(x, weights, eps, out=None, stream=None):
+    """The block on prepared weights (vit_block_w): x (N, T, D) on the weights' device."""
+    lib = load_library()
+    _dev(x, "x", weights.dtype)
+    N, T, D = x.shape
+    if D != weights.D:
+        raise ValueError("x has width %d, the weights %d" % (D, weights.D))
+    if out is None:
+        out = torch.empty_like(x)
+    _dev(out, "out", weights.dtype)
+    with torch.cuda.device(weights.device):
+        rc = lib.vit_block_w(_ptr(x), weights.handle, N, T, float(eps), _ptr(out), _stream(stream))
+    _check(rc, "vit_block_w")
+    return out
+
+
+def vit_block_w_host(x, weights, eps, out=None, stream=None):
+    """vit_block_w on HOST x and out (pinned for full copy speed); only x and out cross
+    the link, and the stream is synchronised before returning."""
+    lib = load_library()
+    if x.is_cuda or not x.is_contiguous() or x.dtype != weights.dtype:
+        raise ValueError("vit_block_w_host takes a contiguous host x of the weights' dtype")
+    N, T, D = x.shape
+    if D != weights.D:
+        raise ValueError("x has width %d, the weights %d" % (D, weights.D))
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(weights.device):
+        rc = lib.vit_block_w_host(_ptr(x), weights.handle, N, T, float(eps), _ptr(out), _stream(stream))
+    _check(rc, "vit_block_w_host")
     return out
 
 

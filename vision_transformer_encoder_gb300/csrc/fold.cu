@@ -16,6 +16,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace vit {
 namespace {
@@ -25,6 +26,8 @@ constexpr int ST_THREADS = 256;  // 8 rows per CTA
 template <int MAXV>
 __global__ void __launch_bounds__(ST_THREADS)
 row_parts_kernel(const __nv_bfloat16* __restrict__ x, float2* __restrict__ parts, int64_t rows, int D) {
+    griddep_wait();                 // x may be the previous kernel's output
+    griddep_launch_dependents();
     const int64_t row = (int64_t)blockIdx.x * (ST_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -138,9 +141,8 @@ fold_finish_kernel(const FoldPrep d, const float* __restrict__ part_c, const flo
 template <int MAXV>
 cudaError_t launch_parts(const void* x, float2* parts, int64_t rows, int64_t D, cudaStream_t s) {
     const int64_t blocks = (rows + ST_THREADS / 32 - 1) / (ST_THREADS / 32);
-    row_parts_kernel<MAXV><<<(unsigned)blocks, ST_THREADS, 0, s>>>(static_cast<const __nv_bfloat16*>(x), parts,
-                                                                   rows, (int)D);
-    return cudaGetLastError();
+    return launch_dependent(row_parts_kernel<MAXV>, dim3((unsigned)blocks), dim3(ST_THREADS), 0, s,
+                            static_cast<const __nv_bfloat16*>(x), parts, rows, (int)D);
 }
 
 }  // namespace

@@ -25,6 +25,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <vector>
 
 #include "common.cuh"
@@ -151,6 +152,14 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     return x < y + nb && y < x + na;
 }
 
+// Column terms of both LayerNorm folds (and the gain-scaled weights), prepared once
+// per weight set by vit_weights_create.
+struct FoldTerms {
+    const float *colsum1, *colbias1, *colsum2, *colbias2;
+    const void* wq_scaled;   // (3, D, D) diag(ln1_g) w_q, w_k, w_v in bf16, or null (no LN1 gain)
+    const void* w1_scaled;   // (D, F) diag(ln2_g) w_mlp1 in bf16, or null (no LN2 gain)
+};
+
 struct BlockArgs {
     const void *x, *w_q, *w_k, *w_v, *w_o, *w1, *w2;
     const void *ln1_g, *ln1_b, *ln2_g, *ln2_b, *b1, *b2;
@@ -164,14 +173,21 @@ struct BlockArgs {
     int x_dt = -1, out_dt = -1;
     const void *b_q = nullptr, *b_k = nullptr, *b_v = nullptr, *b_o = nullptr;
     void* bias_scratch = nullptr;
+    // Prepared weights: bias_scratch already holds [b_q | b_k | b_v]; fold_terms, when
+    // set, replaces the per-call column terms of the folded path (whose [b_q | b_k | b_v]
+    // and b1 are then inside colbias1 and colbias2).
+    bool qkv_bias_ready = false;
+    const FoldTerms* fold_terms = nullptr;
 };
 
 inline int x_dtype(const BlockArgs& a) { return a.x_dt < 0 ? a.dt : a.x_dt; }
 inline int out_dtype(const BlockArgs& a) { return a.out_dt < 0 ? a.dt : a.out_dt; }
 inline bool has_qkv_bias(const BlockArgs& a) { return a.b_q || a.b_k || a.b_v; }
 
-// [b_q | b_k | b_v] into a.bias_scratch (absent ones zero), in stream order.
+// [b_q | b_k | b_v] into a.bias_scratch (absent ones zero), in stream order; nothing
+// when prepared weights already hold it there.
 cudaError_t concat_qkv_bias(const BlockArgs& a, cudaStream_t s) {
+    if (a.qkv_bias_ready) return cudaSuccess;
     const size_t nb = (size_t)a.D * dt_size(a.dt);
     const void* b[3] = {a.b_q, a.b_k, a.b_v};
     for (int i = 0; i < 3; ++i) {
@@ -266,24 +282,26 @@ Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
         w.sz_yb = round_up((size_t)(M * D) * 2, 256);
         w.sz_p1 = round_up((size_t)M * 8, 256);
         w.sz_p2 = round_up((size_t)M * 8 * w.p2, 256);
-        w.sz_cols = round_up((size_t)(2 * 3 * D + 2 * F) * 4, 256);
-        if (a.ln1_g) w.sz_wq = round_up((size_t)(3 * D * D) * 2, 256);
-        if (a.ln2_g) w.sz_w1 = round_up((size_t)(D * F) * 2, 256);
-        const size_t p1 = fold_prep_scratch_bytes(3 * D, D), p2 = fold_prep_scratch_bytes(F, D);
-        w.sz_prep = round_up(p1 > p2 ? p1 : p2, 256);
+        if (!a.fold_terms) {   // column terms computed in the call
+            w.sz_cols = round_up((size_t)(2 * 3 * D + 2 * F) * 4, 256);
+            if (a.ln1_g) w.sz_wq = round_up((size_t)(3 * D * D) * 2, 256);
+            if (a.ln2_g) w.sz_w1 = round_up((size_t)(D * F) * 2, 256);
+            const size_t p1 = fold_prep_scratch_bytes(3 * D, D), p2 = fold_prep_scratch_bytes(F, D);
+            w.sz_prep = round_up(p1 > p2 ? p1 : p2, 256);
+        }
     }
     w.total = w.sz_buf + w.sz_qkv + w.sz_y + w.sz_h + w.sz_yb + w.sz_p1 + w.sz_p2 + w.sz_cols + w.sz_wq +
               w.sz_w1 + w.sz_prep + w.sz_lo + w.sz_wt;
     return w;
 }
 
-// The bf16 path with LayerNorm folded into the GEMMs (VIT_LN_FOLD=1, with the CTA-pair
-// GEMM):
-//   prep      column terms of both folds (+ gain-scaled weights)
+// The bf16 path with LayerNorm folded into the GEMMs (prepared weights made with the
+// fold, or VIT_LN_FOLD=1; with the CTA-pair GEMM):
+//   prep      column terms of both folds (+ gain-scaled weights), unless prepared
 //   LN1 stats row (mean, M2) of x
 //   QKV GEMM  qkv = rstd (x @ W' - mean colsum) + colbias          (A = x itself)
 //   attention o
-//   Wo GEMM   y = x + o @ w_o (fp32), plus a bf16 copy of y and y's row partials
+//   Wo GEMM   y = x + o @ w_o [+ b_o] (fp32), plus a bf16 copy of y and y's row partials
 //   W1 GEMM   h = GELU(rstd (yb @ W1' - mean colsum) + colbias)    (colbias holds b1)
 //   W2 GEMM   out = y + h @ w_mlp2 [+ b2]
 cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s,
@@ -301,10 +319,16 @@ cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     __nv_bfloat16* wq_scaled = a.ln1_g ? reinterpret_cast<__nv_bfloat16*>(p) : nullptr;  p += w.sz_wq;
     __nv_bfloat16* w1_scaled = a.ln2_g ? reinterpret_cast<__nv_bfloat16*>(p) : nullptr;  p += w.sz_w1;
     float* prep_scratch = reinterpret_cast<float*>(p);
-    float* colsum1 = cols;
-    float* colbias1 = cols + 3 * D;
-    float* colsum2 = cols + 6 * D;
-    float* colbias2 = cols + 6 * D + F;
+    const float* colsum1 = cols;
+    const float* colbias1 = cols + 3 * D;
+    const float* colsum2 = cols + 6 * D;
+    const float* colbias2 = cols + 6 * D + F;
+    if (a.fold_terms) {
+        const FoldTerms& t = *a.fold_terms;
+        colsum1 = t.colsum1; colbias1 = t.colbias1; colsum2 = t.colsum2; colbias2 = t.colbias2;
+        wq_scaled = static_cast<__nv_bfloat16*>(const_cast<void*>(t.wq_scaled));
+        w1_scaled = static_cast<__nv_bfloat16*>(const_cast<void*>(t.w1_scaled));
+    }
     cudaError_t e = cudaSuccess;
     auto step = [&](cudaError_t err) {
         if (e == cudaSuccess) e = err;
@@ -313,7 +337,7 @@ cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     const void* wqkv_used[3] = {a.w_q, a.w_k, a.w_v};
     if (wq_scaled)
         for (int i = 0; i < 3; ++i) wqkv_used[i] = wq_scaled + (size_t)i * D * D;
-    step(run(K_FOLD_PREP, s, [&] {
+    if (!a.fold_terms) step(run(K_FOLD_PREP, s, [&] {
         FoldPrep f1;
         std::memset(&f1, 0, sizeof(f1));
         for (int i = 0; i < 3; ++i) {
@@ -322,7 +346,7 @@ cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }
         f1.n_per_w = D; f1.N = 3 * D; f1.K = D;
         f1.gamma = a.ln1_g; f1.beta = a.ln1_b; f1.bias = nullptr;
-        f1.colsum = colsum1; f1.colbias = colbias1;
+        f1.colsum = cols; f1.colbias = cols + 3 * D;
         cudaError_t r = launch_fold_prep(f1, prep_scratch, s);
         if (r != cudaSuccess) return r;
         FoldPrep f2;
@@ -331,7 +355,7 @@ cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         f2.w_scaled[0] = f2.w_scaled[1] = f2.w_scaled[2] = w1_scaled;
         f2.n_per_w = F; f2.N = F; f2.K = D;
         f2.gamma = a.ln2_g; f2.beta = a.ln2_b; f2.bias = a.b1;
-        f2.colsum = colsum2; f2.colbias = colbias2;
+        f2.colsum = cols + 6 * D; f2.colbias = cols + 6 * D + F;
         return launch_fold_prep(f2, prep_scratch, s);
     }));
     step(run(K_LN1_STATS, s, [&] { return launch_row_parts(a.x, parts1, M, D, s); }));
@@ -353,7 +377,7 @@ cudaError_t launch_block_fused(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     std::memset(&g, 0, sizeof(g));
     g.a = o; g.lda = D; g.w[0] = a.w_o; g.n_w = 1; g.n_per_w = D;
     g.M = M; g.N = D; g.K = D;
-    g.epi = TC_EPI_RESID; g.residual = a.x; g.ldr = D; g.residual_f32 = false;
+    g.epi = TC_EPI_RESID; g.bias = a.b_o; g.residual = a.x; g.ldr = D; g.residual_f32 = false;
     g.out = y; g.ldo = D; g.out_f32 = true;
     g.extra.out_bf16 = yb; g.extra.parts = parts2;
     step(run(K_WO, s, [&] { return launch_gemm_tc(g, dev, s); }));
@@ -803,8 +827,12 @@ bool fused_ok(const BlockArgs& a, const DeviceInfo& dev) {
     return ln_fold_requested() && tc_pair_enabled(dev) && row_parts_supported(a.D, a.x);
 }
 
-int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-    const Workspace w = workspace_layout(a, fused_ok(a, dev));
+// fuse: 1 / 0 runs the LayerNorm-folded / plain bf16 path (the folded one where the
+// shapes and pointers allow it); -1 follows VIT_LN_FOLD.
+int enqueue_block(const BlockArgs& a, const DeviceInfo& dev, cudaStream_t s, int fuse = -1) {
+    const bool f = fuse < 0 ? fused_ok(a, dev)
+                            : fuse == 1 && tc_pair_enabled(dev) && row_parts_supported(a.D, a.x);
+    const Workspace w = workspace_layout(a, f);
     DeviceState* st = nullptr;
     int rc = current_device(&st);
     if (rc != VIT_OK) return rc;
@@ -1055,6 +1083,183 @@ int pipeline_streams(DeviceState* st) {
 
 using namespace vit;
 
+// One block's weights held on one device (vit_weights_create): the tensors of a vit_layer
+// record copied into one allocation, the concatenated [b_q | b_k | b_v], and with the fold
+// the column terms and gain-scaled weights of both folded LayerNorms.
+struct vit_weights_s {
+    int device = -1, dtype = 0;
+    int64_t D = 0, F = 0, H = 0;
+    bool fold = false;
+    void* mem = nullptr;
+    size_t bytes = 0;
+    vit_layer w{};              // device pointers into mem; absent terms null
+    void* qkv_bias = nullptr;   // (3 D) or null
+    FoldTerms terms{};
+};
+
+namespace vit {
+namespace {
+
+// Prepared weights run on the plain path by default: the folded one is barely faster
+// and subtracts mean * c after the product, which loses accuracy when a row's mean is
+// large against its spread (VIT_PREPARED_FOLD=1 makes the fold the default).
+bool prepared_fold_default() {
+    static const bool on = [] {
+        const char* e = std::getenv("VIT_PREPARED_FOLD");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+
+BlockArgs prepared_args(const vit_weights* w, const void* x, int64_t N, int64_t T, double eps, void* out) {
+    const vit_layer& l = w->w;
+    BlockArgs a{x, l.w_q, l.w_k, l.w_v, l.w_o, l.w_mlp1, l.w_mlp2, l.ln1_g, l.ln1_b, l.ln2_g, l.ln2_b,
+                l.b1, l.b2, N, T, w->D, w->F, w->H, eps, w->dtype, out};
+    a.b_q = l.b_q; a.b_k = l.b_k; a.b_v = l.b_v; a.b_o = l.b_o;
+    a.bias_scratch = w->qkv_bias;
+    a.qkv_bias_ready = w->qkv_bias != nullptr;
+    a.fold_terms = w->fold ? &w->terms : nullptr;
+    return a;
+}
+
+// Host-buffer pipeline of vit_block_host and vit_block_w_host. `h` holds host pointers:
+// x and out, and the weights and affine terms unless prepared weights `pw` are given, in
+// which case only x and out cross the link.
+int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
+    const int64_t N = h.N, T = h.T, D = h.D, F = h.F;
+    const int dtype = h.dt;
+    DeviceState* st = nullptr;
+    int rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t es = dt_size(dtype);
+    const size_t xb = (size_t)(N * T * D) * es;
+    const size_t sizes[14] = {xb, (size_t)(D * D) * es, (size_t)(D * D) * es, (size_t)(D * D) * es,
+                              (size_t)(D * D) * es, (size_t)(D * F) * es, (size_t)(D * F) * es,
+                              (size_t)D * es, (size_t)D * es, (size_t)D * es, (size_t)D * es,
+                              (size_t)F * es, (size_t)D * es, xb};
+    const void* src[13] = {h.x, h.w_q, h.w_k, h.w_v, h.w_o, h.w1, h.w2,
+                           h.ln1_g, h.ln1_b, h.ln2_g, h.ln2_b, h.b1, h.b2};
+    if (pw)
+        for (int i = 1; i < 13; ++i) src[i] = nullptr;   // on the device already
+    size_t off[14], total = 0;
+    for (int i = 0; i < 14; ++i) {
+        off[i] = total;
+        if (i < 13 && !src[i]) continue;
+        total += round_up(sizes[i], 256);
+    }
+    const std::vector<int64_t> chunk_n = host_chunks(N, T);
+    const int64_t chunks = (int64_t)chunk_n.size();
+    // copy-in, compute (successive chunks alternate between two streams, so that one
+    // chunk's kernels can fill the SMs another's leave idle at their ends), copy-out
+    cudaStream_t sh = s, sd = s;
+    cudaStream_t scs[2] = {s, s};
+    if (chunks > 1) {
+        rc = pipeline_streams(st);
+        if (rc != VIT_OK) return rc;
+        sh = st->h2d;
+        scs[0] = st->comp;
+        scs[1] = host_compute_streams() > 1 ? st->comp2 : st->comp;
+        sd = st->d2h;
+    }
+    void* dmem = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&dmem, total, st->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    uint8_t* base = static_cast<uint8_t*>(dmem);
+    const void* dev_in[13];
+    for (int i = 0; i < 13; ++i) dev_in[i] = src[i] ? base + off[i] : nullptr;
+    void* dev_out = base + off[13];
+    // events: start, then per chunk x copied and block computed, then copies out done
+    std::vector<cudaEvent_t> ev;
+    auto new_event = [&](cudaEvent_t* out) {
+        cudaError_t r = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev.push_back(*out);
+        return r;
+    };
+    cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp[2] = {nullptr, nullptr};
+    if (chunks > 1) {
+        e = new_event(&start);
+        if (e == cudaSuccess) e = cudaEventRecord(start, s);   // after the allocation
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sh, start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(scs[0], start, 0);
+        if (e == cudaSuccess && scs[1] != scs[0]) e = cudaStreamWaitEvent(scs[1], start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, start, 0);
+    }
+    // weights and affine terms first (none with prepared weights), then x chunk by chunk
+    for (int i = 1; i < 13 && e == cudaSuccess; ++i)
+        if (src[i]) e = cudaMemcpyAsync(base + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, sh);
+    const size_t seq_bytes = (size_t)(T * D) * es;
+    int64_t n0 = 0;
+    for (int64_t c = 0; c < chunks && e == cudaSuccess && rc == VIT_OK; ++c) {
+        const int64_t nc = chunk_n[(size_t)c];
+        const size_t o = (size_t)n0 * seq_bytes, nbytes = (size_t)nc * seq_bytes;
+        cudaStream_t sc = scs[c & 1];
+        e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(h.x) + o, nbytes,
+                            cudaMemcpyHostToDevice, sh);
+        cudaEvent_t in_ready = nullptr, done = nullptr;
+        if (chunks > 1) {
+            if (e == cudaSuccess) e = new_event(&in_ready);
+            if (e == cudaSuccess) e = cudaEventRecord(in_ready, sh);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, in_ready, 0);
+        }
+        if (e != cudaSuccess) break;
+        void* const out_c = static_cast<uint8_t*>(dev_out) + o;
+        if (pw) {
+            rc = enqueue_block(prepared_args(pw, base + off[0] + o, nc, T, h.eps, out_c), st->info, sc,
+                               pw->fold ? 1 : 0);
+        } else {
+            BlockArgs d{base + off[0] + o, dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], dev_in[6],
+                        dev_in[7], dev_in[8], dev_in[9], dev_in[10], dev_in[11], dev_in[12],
+                        nc, T, D, F, h.H, h.eps, dtype, out_c};
+            rc = enqueue_block(d, st->info, sc);
+        }
+        if (rc != VIT_OK) break;
+        if (chunks > 1) {
+            e = new_event(&done);
+            if (e == cudaSuccess) e = cudaEventRecord(done, sc);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, done, 0);
+            end_comp[c & 1] = done;
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(static_cast<uint8_t*>(h.out) + o, out_c, nbytes, cudaMemcpyDeviceToHost, sd);
+        n0 += nc;
+    }
+    if (chunks > 1) {
+        // join: the caller's stream waits for the last copy out and the last block (and
+        // so for every copy in), then frees the buffers in its own order
+        cudaError_t je = new_event(&end_d2h);
+        if (je == cudaSuccess) je = cudaEventRecord(end_d2h, sd);
+        if (je == cudaSuccess) je = cudaStreamWaitEvent(s, end_d2h, 0);
+        for (int i = 0; i < 2; ++i)
+            if (je == cudaSuccess && end_comp[i]) je = cudaStreamWaitEvent(s, end_comp[i], 0);
+        if (je == cudaSuccess) {
+            cudaEvent_t in_done = nullptr;
+            je = new_event(&in_done);
+            if (je == cudaSuccess) je = cudaEventRecord(in_done, sh);
+            if (je == cudaSuccess) je = cudaStreamWaitEvent(s, in_done, 0);
+        }
+        if (e == cudaSuccess) e = je;
+    }
+    cudaError_t fe = cudaFreeAsync(dmem, s);
+    cudaError_t se = cudaStreamSynchronize(s);
+    for (cudaEvent_t x : ev) cudaEventDestroy(x);
+    if (rc != VIT_OK) return rc;
+    if (e == cudaSuccess) e = fe;
+    if (e == cudaSuccess) e = se;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return status_from(e);
+    }
+    return VIT_OK;
+}
+
+}  // namespace
+}  // namespace vit
+
+
 extern "C" {
 
 int vit_block_ex(const void* x, const void* w_q, const void* w_k, const void* w_v, const void* w_o,
@@ -1190,125 +1395,178 @@ int vit_block_host(const void* x_host, const void* w_q_host, const void* w_k_hos
                 N, T, D, F, H, eps, dtype, out_host};
     int rc = validate(a);
     if (rc != VIT_OK) return rc;
+    return host_pipeline(a, nullptr, stream);
+}
+
+int vit_weights_create(const vit_layer* layer, int from_host, int64_t D, int64_t F, int64_t H, int dtype,
+                       int fold, vit_weights** out, void* stream) {
+    if (!layer || !out) return VIT_ERR_ARG;
+    if (dtype != DT_F32 && dtype != DT_BF16 && dtype != DT_F64) return VIT_ERR_DTYPE;
+    if (!layer->w_q || !layer->w_k || !layer->w_v || !layer->w_o || !layer->w_mlp1 || !layer->w_mlp2)
+        return VIT_ERR_ARG;
+    if (D <= 0 || F <= 0 || H <= 0 || D % H != 0 || D > (1 << 20) || F > (1 << 22)) return VIT_ERR_ARG;
+    if (fold < -1 || fold > 1 || (from_host != 0 && from_host != 1)) return VIT_ERR_ARG;
     DeviceState* st = nullptr;
-    rc = current_device(&st);
+    int rc = current_device(&st);
     if (rc != VIT_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the fold runs on the bf16 tensor-core path with the CTA-pair GEMM
+    const bool can_fold = dtype == DT_BF16 && tc_pair_enabled(st->info) && D % 64 == 0 && F % 64 == 0 &&
+                          D <= 2048 && row_parts_supported(D, reinterpret_cast<void*>(256));
+    if (fold == 1 && !can_fold) return VIT_ERR_UNSUPPORTED;
+    const bool use_fold = can_fold && (fold == 1 || (fold == -1 && prepared_fold_default()));
     const size_t es = dt_size(dtype);
-    const size_t xb = (size_t)(N * T * D) * es;
-    const size_t sizes[14] = {xb, (size_t)(D * D) * es, (size_t)(D * D) * es, (size_t)(D * D) * es,
-                              (size_t)(D * D) * es, (size_t)(D * F) * es, (size_t)(D * F) * es,
-                              (size_t)D * es, (size_t)D * es, (size_t)D * es, (size_t)D * es,
-                              (size_t)F * es, (size_t)D * es, xb};
-    const void* src[13] = {x_host, w_q_host, w_k_host, w_v_host, w_o_host, w_mlp1_host, w_mlp2_host,
-                           ln1_g_host, ln1_b_host, ln2_g_host, ln2_b_host, b1_host, b2_host};
-    size_t off[14], total = 0;
-    for (int i = 0; i < 14; ++i) {
+    const void* src[16] = {layer->w_q, layer->w_k, layer->w_v, layer->w_o, layer->w_mlp1, layer->w_mlp2,
+                           layer->ln1_g, layer->ln1_b, layer->ln2_g, layer->ln2_b, layer->b1, layer->b2,
+                           layer->b_q, layer->b_k, layer->b_v, layer->b_o};
+    const size_t n[16] = {(size_t)(D * D), (size_t)(D * D), (size_t)(D * D), (size_t)(D * D),
+                          (size_t)(D * F), (size_t)(D * F), (size_t)D, (size_t)D, (size_t)D, (size_t)D,
+                          (size_t)F, (size_t)D, (size_t)D, (size_t)D, (size_t)D, (size_t)D};
+    const bool qkv_bias = layer->b_q || layer->b_k || layer->b_v;
+    size_t off[16], total = 0;
+    for (int i = 0; i < 16; ++i) {
         off[i] = total;
-        if (i < 13 && !src[i]) continue;
-        total += round_up(sizes[i], 256);
+        if (src[i]) total += round_up(n[i] * es, 256);
     }
-    const std::vector<int64_t> chunk_n = host_chunks(N, T);
-    const int64_t chunks = (int64_t)chunk_n.size();
-    // copy-in, compute (successive chunks alternate between two streams, so that one
-    // chunk's kernels can fill the SMs another's leave idle at their ends), copy-out
-    cudaStream_t sh = s, sd = s;
-    cudaStream_t scs[2] = {s, s};
-    if (chunks > 1) {
-        rc = pipeline_streams(st);
-        if (rc != VIT_OK) return rc;
-        sh = st->h2d;
-        scs[0] = st->comp;
-        scs[1] = host_compute_streams() > 1 ? st->comp2 : st->comp;
-        sd = st->d2h;
-    }
-    void* dmem = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&dmem, total, st->pool, s);
-    if (e != cudaSuccess) {
+    const size_t off_bias = total;
+    if (qkv_bias) total += round_up((size_t)(3 * D) * es, 256);
+    const size_t off_cols = total;
+    if (use_fold) total += round_up((size_t)(2 * 3 * D + 2 * F) * 4, 256);
+    const size_t off_wq = total;
+    if (use_fold && layer->ln1_g) total += round_up((size_t)(3 * D * D) * 2, 256);
+    const size_t off_w1 = total;
+    if (use_fold && layer->ln2_g) total += round_up((size_t)(D * F) * 2, 256);
+    vit_weights* w = new (std::nothrow) vit_weights;
+    if (!w) return VIT_ERR_NOMEM;
+    w->device = st->info.device;
+    w->dtype = dtype;
+    w->D = D; w->F = F; w->H = H;
+    w->fold = use_fold;
+    w->bytes = total;
+    if (cudaMalloc(&w->mem, total) != cudaSuccess) {
         cudaGetLastError();
-        return status_from(e);
+        delete w;
+        return VIT_ERR_NOMEM;
     }
-    uint8_t* base = static_cast<uint8_t*>(dmem);
-    const void* dev_in[13];
-    for (int i = 0; i < 13; ++i) dev_in[i] = src[i] ? base + off[i] : nullptr;
-    void* dev_out = base + off[13];
-    // events: start, then per chunk x copied and block computed, then copies out done
-    std::vector<cudaEvent_t> ev;
-    auto new_event = [&](cudaEvent_t* out) {
-        cudaError_t r = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
-        if (r == cudaSuccess) ev.push_back(*out);
-        return r;
-    };
-    cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp[2] = {nullptr, nullptr};
-    if (chunks > 1) {
-        e = new_event(&start);
-        if (e == cudaSuccess) e = cudaEventRecord(start, s);   // after the allocation
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(sh, start, 0);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(scs[0], start, 0);
-        if (e == cudaSuccess && scs[1] != scs[0]) e = cudaStreamWaitEvent(scs[1], start, 0);
-        if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, start, 0);
+    uint8_t* base = static_cast<uint8_t*>(w->mem);
+    const void* dst[16];
+    for (int i = 0; i < 16; ++i) dst[i] = src[i] ? base + off[i] : nullptr;
+    w->w.w_q = dst[0]; w->w.w_k = dst[1]; w->w.w_v = dst[2]; w->w.w_o = dst[3];
+    w->w.w_mlp1 = dst[4]; w->w.w_mlp2 = dst[5]; w->w.ln1_g = dst[6]; w->w.ln1_b = dst[7];
+    w->w.ln2_g = dst[8]; w->w.ln2_b = dst[9]; w->w.b1 = dst[10]; w->w.b2 = dst[11];
+    w->w.b_q = dst[12]; w->w.b_k = dst[13]; w->w.b_v = dst[14]; w->w.b_o = dst[15];
+    cudaError_t e = cudaSuccess;
+    const cudaMemcpyKind kind = from_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+    for (int i = 0; i < 16 && e == cudaSuccess; ++i)
+        if (src[i]) e = cudaMemcpyAsync(base + off[i], src[i], n[i] * es, kind, s);
+    void* prep = nullptr;
+    if (e == cudaSuccess && qkv_bias) {
+        w->qkv_bias = base + off_bias;
+        BlockArgs a{};
+        a.D = D; a.dt = dtype;
+        a.b_q = w->w.b_q; a.b_k = w->w.b_k; a.b_v = w->w.b_v;
+        a.bias_scratch = w->qkv_bias;
+        e = concat_qkv_bias(a, s);
     }
-    // weights and affine terms first, then x chunk by chunk
-    for (int i = 1; i < 13 && e == cudaSuccess; ++i)
-        if (src[i]) e = cudaMemcpyAsync(base + off[i], src[i], sizes[i], cudaMemcpyHostToDevice, sh);
-    const size_t seq_bytes = (size_t)(T * D) * es;
-    int64_t n0 = 0;
-    for (int64_t c = 0; c < chunks && e == cudaSuccess && rc == VIT_OK; ++c) {
-        const int64_t nc = chunk_n[(size_t)c];
-        const size_t o = (size_t)n0 * seq_bytes, nbytes = (size_t)nc * seq_bytes;
-        cudaStream_t sc = scs[c & 1];
-        e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(x_host) + o, nbytes,
-                            cudaMemcpyHostToDevice, sh);
-        cudaEvent_t in_ready = nullptr, done = nullptr;
-        if (chunks > 1) {
-            if (e == cudaSuccess) e = new_event(&in_ready);
-            if (e == cudaSuccess) e = cudaEventRecord(in_ready, sh);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, in_ready, 0);
+    if (e == cudaSuccess && use_fold) {
+        float* cols = reinterpret_cast<float*>(base + off_cols);
+        __nv_bfloat16* wq_scaled = layer->ln1_g ? reinterpret_cast<__nv_bfloat16*>(base + off_wq) : nullptr;
+        __nv_bfloat16* w1_scaled = layer->ln2_g ? reinterpret_cast<__nv_bfloat16*>(base + off_w1) : nullptr;
+        w->terms.colsum1 = cols;
+        w->terms.colbias1 = cols + 3 * D;
+        w->terms.colsum2 = cols + 6 * D;
+        w->terms.colbias2 = cols + 6 * D + F;
+        w->terms.wq_scaled = wq_scaled;
+        w->terms.w1_scaled = w1_scaled;
+        const size_t p1 = fold_prep_scratch_bytes(3 * D, D), p2 = fold_prep_scratch_bytes(F, D);
+        e = cudaMallocFromPoolAsync(&prep, p1 > p2 ? p1 : p2, st->pool, s);
+        if (e == cudaSuccess) {
+            FoldPrep f1;
+            std::memset(&f1, 0, sizeof(f1));
+            f1.w[0] = w->w.w_q; f1.w[1] = w->w.w_k; f1.w[2] = w->w.w_v;
+            for (int i = 0; i < 3; ++i)
+                f1.w_scaled[i] = wq_scaled ? (void*)(wq_scaled + (size_t)i * D * D) : nullptr;
+            f1.n_per_w = D; f1.N = 3 * D; f1.K = D;
+            f1.gamma = w->w.ln1_g; f1.beta = w->w.ln1_b; f1.bias = w->qkv_bias;
+            f1.colsum = cols; f1.colbias = cols + 3 * D;
+            e = run(K_FOLD_PREP, s, [&] { return launch_fold_prep(f1, static_cast<float*>(prep), s); });
+            FoldPrep f2;
+            std::memset(&f2, 0, sizeof(f2));
+            f2.w[0] = f2.w[1] = f2.w[2] = w->w.w_mlp1;
+            f2.w_scaled[0] = f2.w_scaled[1] = f2.w_scaled[2] = w1_scaled;
+            f2.n_per_w = F; f2.N = F; f2.K = D;
+            f2.gamma = w->w.ln2_g; f2.beta = w->w.ln2_b; f2.bias = w->w.b1;
+            f2.colsum = cols + 6 * D; f2.colbias = cols + 6 * D + F;
+            if (e == cudaSuccess)
+                e = run(K_FOLD_PREP, s, [&] { return launch_fold_prep(f2, static_cast<float*>(prep), s); });
+            cudaError_t fe = cudaFreeAsync(prep, s);
+            if (e == cudaSuccess) e = fe;
         }
-        if (e != cudaSuccess) break;
-        BlockArgs d{base + off[0] + o, dev_in[1], dev_in[2], dev_in[3], dev_in[4], dev_in[5], dev_in[6],
-                    dev_in[7], dev_in[8], dev_in[9], dev_in[10], dev_in[11], dev_in[12],
-                    nc, T, D, F, H, eps, dtype, static_cast<uint8_t*>(dev_out) + o};
-        rc = enqueue_block(d, st->info, sc);
-        if (rc != VIT_OK) break;
-        if (chunks > 1) {
-            e = new_event(&done);
-            if (e == cudaSuccess) e = cudaEventRecord(done, sc);
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, done, 0);
-            end_comp[c & 1] = done;
-        }
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + o, static_cast<uint8_t*>(dev_out) + o, nbytes,
-                                cudaMemcpyDeviceToHost, sd);
-        n0 += nc;
     }
-    if (chunks > 1) {
-        // join: the caller's stream waits for the last copy out and the last block (and
-        // so for every copy in), then frees the buffers in its own order
-        cudaError_t je = new_event(&end_d2h);
-        if (je == cudaSuccess) je = cudaEventRecord(end_d2h, sd);
-        if (je == cudaSuccess) je = cudaStreamWaitEvent(s, end_d2h, 0);
-        for (int i = 0; i < 2; ++i)
-            if (je == cudaSuccess && end_comp[i]) je = cudaStreamWaitEvent(s, end_comp[i], 0);
-        if (je == cudaSuccess) {
-            cudaEvent_t in_done = nullptr;
-            je = new_event(&in_done);
-            if (je == cudaSuccess) je = cudaEventRecord(in_done, sh);
-            if (je == cudaSuccess) je = cudaStreamWaitEvent(s, in_done, 0);
-        }
-        if (e == cudaSuccess) e = je;
-    }
-    cudaError_t fe = cudaFreeAsync(dmem, s);
     cudaError_t se = cudaStreamSynchronize(s);
-    for (cudaEvent_t x : ev) cudaEventDestroy(x);
-    if (rc != VIT_OK) return rc;
-    if (e == cudaSuccess) e = fe;
     if (e == cudaSuccess) e = se;
     if (e != cudaSuccess) {
         cudaGetLastError();
-        return status_from(e);
+        cudaFree(w->mem);
+        delete w;
+        return e == cudaErrorMemoryAllocation ? VIT_ERR_NOMEM : status_from(e);
+    }
+    *out = w;
+    return VIT_OK;
+}
+
+int vit_weights_destroy(vit_weights* w) {
+    if (!w) return VIT_OK;
+    int prev = -1;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e == cudaSuccess && prev != w->device) e = cudaSetDevice(w->device);
+    if (e == cudaSuccess) e = cudaFree(w->mem);
+    if (prev >= 0 && prev != w->device) cudaSetDevice(prev);
+    delete w;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return VIT_ERR_CUDA;
     }
     return VIT_OK;
+}
+
+int vit_weights_info(const vit_weights* w, int64_t* D, int64_t* F, int64_t* H, int* dtype, int* fold,
+                     int* device) {
+    if (!w) return VIT_ERR_ARG;
+    if (D) *D = w->D;
+    if (F) *F = w->F;
+    if (H) *H = w->H;
+    if (dtype) *dtype = w->dtype;
+    if (fold) *fold = w->fold ? 1 : 0;
+    if (device) *device = w->device;
+    return VIT_OK;
+}
+
+int vit_block_w(const void* x, const vit_weights* w, int64_t N, int64_t T, double eps, void* out,
+                void* stream) {
+    if (!w) return VIT_ERR_ARG;
+    const BlockArgs a = prepared_args(w, x, N, T, eps, out);
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VIT_ERR_CUDA;
+    if (dev != w->device) return VIT_ERR_ARG;
+    DeviceState* st = nullptr;
+    rc = current_device(&st);
+    if (rc != VIT_OK) return rc;
+    return enqueue_block(a, st->info, static_cast<cudaStream_t>(stream), w->fold ? 1 : 0);
+}
+
+int vit_block_w_host(const void* x_host, const vit_weights* w, int64_t N, int64_t T, double eps,
+                     void* out_host, void* stream) {
+    if (!w) return VIT_ERR_ARG;
+    const BlockArgs a = prepared_args(w, x_host, N, T, eps, out_host);
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VIT_ERR_CUDA;
+    if (dev != w->device) return VIT_ERR_ARG;
+    return host_pipeline(a, w, stream);
 }
 
 int vit_layernorm(const void* x, int64_t rows, int64_t D, double eps, const void* gamma,
