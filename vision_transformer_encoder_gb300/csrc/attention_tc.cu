@@ -402,17 +402,24 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
                                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
                     m_new = fmaxf(m, mrow * sl2);
                     alpha = exp2_approx(m - m_new);
-                    // P = exp2(s * scale - m) (masked keys give exp2(-inf) = 0) in bf16; pair
-                    // e / 2 goes to sv[e / 2], whose S value has been read already
-                    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    // P = exp2(s * scale - m) (masked keys give exp2(-inf) = 0) in bf16, the
+                    // exponent arguments and row sums in packed fp32 pairs; pair e / 2 goes to
+                    // sv[e / 2], whose S value has been read already
+                    const unsigned long long s2 = f2_pack(sl2, sl2), nm = f2_pack(-m_new, -m_new);
+                    unsigned long long ls[4] = {0ull, 0ull, 0ull, 0ull};   // packed pairs of +0.0f
 #pragma unroll
                     for (int e = 0; e < AT_KEYS; e += 2) {
-                        const float p0 = exp2_approx(fmaf(__uint_as_float(sv[e]), sl2, -m_new));
-                        const float p1 = exp2_approx(fmaf(__uint_as_float(sv[e + 1]), sl2, -m_new));
-                        ls[(e >> 1) & 7] += p0 + p1;
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), s2, nm), x0, x1);
+                        const float p0 = exp2_approx(x0);
+                        const float p1 = exp2_approx(x1);
+                        ls[(e >> 1) & 3] = f2_add(ls[(e >> 1) & 3], f2_pack(p0, p1));
                         sv[e >> 1] = pack_bf16x2(p0, p1);
                     }
-                    lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                    float a0, a1, b0, b1;
+                    f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
+                    f2_unpack(f2_add(ls[2], ls[3]), b0, b1);
+                    lsum = (a0 + a1) + (b0 + b1);
                 }
                 if (j > 0) {
                     // P.V of the previous tile must be done: it reads P, and O is rescaled
