@@ -44,6 +44,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace vit {
@@ -177,6 +178,9 @@ attention_tc_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constan
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = bars->tmem_slot;
+    // the set-up above overlaps the previous kernel's tail; qkv is its output
+    griddep_wait();
+    griddep_launch_dependents();
     // TMEM columns: S_g at [128 g, 128 g + 128); O_g at 256 + 128 g; with PT, P_g (64
     // columns of bf16 pairs) right after O_g at 256 + 128 g + 64.
     const int D = p.D;
@@ -625,8 +629,8 @@ cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t
         attr = true;
     }
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
-    attention_tc_kernel<DH, PT><<<grid, AT_THREADS, L::SMEM, s>>>(tm, tm16, tmO, tmO16, p);
-    return cudaGetLastError();
+    return launch_dependent(attention_tc_kernel<DH, PT>, dim3(grid), dim3(AT_THREADS), L::SMEM, s, tm, tm16, tmO,
+                            tmO16, p);
 }
 
 }  // namespace
