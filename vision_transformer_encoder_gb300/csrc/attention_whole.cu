@@ -29,14 +29,16 @@
 //                    row costs one read of S, each P rounded once.
 //   warps 16-19      epilogue, one per TMEM lane quarter: O into registers, O's slot
 //                    released at once, then O / (l0 + l1) in bf16 to global memory.
-//   warp 20          TMEM owner and MMA issuer. MMA stream: S(0), S(1), PV(0), S(2),
-//                    PV(1), S(3), PV(2), ...: S of the next unit runs while the softmax
-//                    of the current one works, and PV(u) follows as soon as P(u) is in.
-//                    PV reads P of keys below `split` from the slot's first columns and
-//                    P of the rest from the columns starting at `split`.
-//   warps 21-23      TMA loads of Q, K and V (one issuing thread per stream, as a
-//                    thread's TMA copies are issued one after another). Each is
-//                    double-buffered per item; a 3-D tensor map (column, token,
+//   warps 20, 21     MMA issuers, one per group (warp 20 also owns TMEM): group g's
+//                    stream is S(g), PV(g), S(g + 2), PV(g + 2), ...: S of a unit runs
+//                    while the other group's softmax works, and PV(u) follows as soon as
+//                    P(u) is in. (One thread issues an MMA only every ~120 cycles while
+//                    the softmax warps move tensor memory: one issuer for both groups
+//                    reached each P late.) PV reads P of keys below `split` from the
+//                    slot's first columns and P of the rest from the columns from `split`.
+//   warps 22, 23     TMA loads: Q then K of each item (warp 22), V (warp 23); one issuing
+//                    thread per stream, as a thread's TMA copies go one after another.
+//                    Each is double-buffered per item; a 3-D tensor map (column, token,
 //                    sequence) zero-fills tokens past T.
 // TMEM, 512 columns: S / P of even units at [0, 224), of odd units at [224, 448), O at
 // [448, 512). S(u + 2) overwrites P(u) only after PV(u) in the same in-order MMA stream.
@@ -60,7 +62,7 @@ constexpr int AW_DH = 64;
 constexpr int AW_ROWS = 128;               // query rows per unit (TMEM lanes)
 constexpr int AW_MAX_KEYS = 224;           // S columns per unit
 constexpr int AW_THREADS = 768;            // 24 warps
-constexpr int AW_EPI_WARP = 16, AW_MMA_WARP = 20, AW_LOAD_WARP = 21;
+constexpr int AW_EPI_WARP = 16, AW_MMA_WARP = 20, AW_LOAD_WARP = 22;   // MMA: warps 20, 21
 constexpr int AW_BOX = AW_ROWS * 128;      // 128 rows x 64 bf16 columns, 128B swizzle: 16 KB
 constexpr int AW_OFF_Q = 0;                        // [buffer][query tile]
 constexpr int AW_OFF_K = AW_OFF_Q + 4 * AW_BOX;    // [buffer][128-key box]
@@ -86,7 +88,7 @@ struct AwParams {
 struct AwBars {
     uint64_t q_full[2], q_empty[2], k_full[2], k_empty[2], v_full[2], v_empty[2];
     uint64_t s_full[2], p_full[2], l_full[4];
-    uint64_t o_done, o_free, done;
+    uint64_t o_done, o_free[2], done;   // o_free[u & 1]: the epilogue has read O(u)
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -230,18 +232,19 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&bars->q_full[b], 1);
-            ptx::mbar_init(&bars->q_empty[b], 1);
+            ptx::mbar_init(&bars->q_empty[b], 2);    // both MMA issuers
             ptx::mbar_init(&bars->k_full[b], 1);
-            ptx::mbar_init(&bars->k_empty[b], 1);
+            ptx::mbar_init(&bars->k_empty[b], 2);
             ptx::mbar_init(&bars->v_full[b], 1);
-            ptx::mbar_init(&bars->v_empty[b], 1);
+            ptx::mbar_init(&bars->v_empty[b], 2);
             ptx::mbar_init(&bars->s_full[b], 1);
             ptx::mbar_init(&bars->p_full[b], 8);     // the eight softmax warps of a group
         }
         for (int i = 0; i < 4; ++i) ptx::mbar_init(&bars->l_full[i], 8);
         ptx::mbar_init(&bars->o_done, 1);
-        ptx::mbar_init(&bars->o_free, 4);            // the four epilogue warps
-        ptx::mbar_init(&bars->done, 1);
+        ptx::mbar_init(&bars->o_free[0], 4);         // the four epilogue warps
+        ptx::mbar_init(&bars->o_free[1], 4);
+        ptx::mbar_init(&bars->done, 2);
         bars->abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -261,89 +264,116 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
     if (warp >= AW_LOAD_WARP) {
         if (lane == 0) {
             // ------------------------------------------------------------ TMA producers
-            const int role = warp - AW_LOAD_WARP;   // 0 Q, 1 K, 2 V
-            uint64_t* full = role == 0 ? bars->q_full : role == 1 ? bars->k_full : bars->v_full;
-            uint64_t* empty = role == 0 ? bars->q_empty : role == 1 ? bars->k_empty : bars->v_empty;
-            uint8_t* ring = role == 0 ? sQ : role == 1 ? sK : sV;
-            const int boxes = role == 0 ? nq : p.nkb;
-            const int col0 = role * p.D;   // Q at 0, K at D, V at 2D
-            int k = 0;
+            // (one issuing thread per stream, as a thread's copies go one after another):
+            // warp 22 each item's query tiles, then its keys; warp 23 its values
+            const bool qk = warp == AW_LOAD_WARP;
+            int issued[3] = {0, 0, 0};   // items whose copies each stream has issued
             bool ok = true;
-            for (; k < n_items; ++k) {
+            for (int k = 0; k < n_items && ok; ++k) {
                 const int item = (int)blockIdx.x + k * (int)gridDim.x;
                 const int n = item / p.H, h = item - n * p.H;
                 const int b = k & 1;
-                if (!ptx::mbar_wait_bounded<true>(&empty[b], ((k >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                ptx::mbar_arrive_expect_tx(&full[b], boxes * AW_BOX);
-                for (int r = 0; r < boxes; ++r)
-                    ptx::tma_load_3d(ring + (b * 2 + r) * AW_BOX, &tm, &full[b], col0 + h * AW_DH, r * AW_ROWS, n);
+                for (int role = qk ? 0 : 2; role <= (qk ? 1 : 2) && ok; ++role) {   // 0 Q, 1 K, 2 V
+                    uint64_t* full = role == 0 ? bars->q_full : role == 1 ? bars->k_full : bars->v_full;
+                    uint64_t* empty = role == 0 ? bars->q_empty : role == 1 ? bars->k_empty : bars->v_empty;
+                    uint8_t* ring = role == 0 ? sQ : role == 1 ? sK : sV;
+                    const int boxes = role == 0 ? nq : p.nkb;
+                    if (!ptx::mbar_wait_bounded<true>(&empty[b], ((k >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&full[b], boxes * AW_BOX);
+                    for (int r = 0; r < boxes; ++r)   // Q at column 0, K at D, V at 2D
+                        ptx::tma_load_3d(ring + (b * 2 + r) * AW_BOX, &tm, &full[b], role * p.D + h * AW_DH,
+                                         r * AW_ROWS, n);
+                    issued[role] = k + 1;
+                }
             }
             if (!ok) {
                 aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
                 *abort_flag = 1;
             }
             // let the copies in flight land before the CTA can exit
-            for (int b = 0; b < 2; ++b)
-                if (k > b && !ptx::mbar_wait_bounded(&full[b], ((k - 1 - b) >> 1) & 1, nullptr))
-                    aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            for (int role = qk ? 0 : 2; role <= (qk ? 1 : 2); ++role) {
+                uint64_t* full = role == 0 ? bars->q_full : role == 1 ? bars->k_full : bars->v_full;
+                const int kk = issued[role];
+                for (int b = 0; b < 2; ++b)
+                    if (kk > b && !ptx::mbar_wait_bounded(&full[b], ((kk - 1 - b) >> 1) & 1, nullptr))
+                        aw_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            }
         }
-    } else if (warp == AW_MMA_WARP) {
+    } else if (warp >= AW_MMA_WARP) {
         if (lane == 0) {
-            // ------------------------------------------------------------- MMA issuer
+            // --------------------------------------- MMA issuers, one per softmax group
+            // (warp 20: units 0, 2, 4, ...; warp 21: units 1, 3, 5, ...). One thread issues an
+            // MMA only every ~120 cycles while the softmax warps move tensor memory, so each
+            // group's chain S -> P.V gets its own thread. Both use an item's Q, K and V
+            // buffers and release each once (their empty barriers count two); with one
+            // query tile per item (nq == 1) an issuer releases the other's items too, after
+            // their full barriers, so that it never runs a phase ahead.
+            const int g = warp - AW_MMA_WARP;
             const uint32_t idS = ptx::idesc_bf16_f32(AW_ROWS, p.ns, false, false);
             constexpr uint32_t idO = ptx::idesc_bf16_f32(AW_ROWS, AW_DH, false, true);
             const int ksteps = p.ns >> 4, ksplit = p.split >> 4;
             bool ok = true;
-            for (int s = 0; s <= units && ok; ++s) {
-                if (s < units) {
-                    // S(s) = Q K^T into the unit's S slot
-                    const int u = s, k = u / nq, qt = u - k * nq, b = k & 1, g = u & 1;
-                    if (qt == 0) {
-                        if (!ptx::mbar_wait_bounded(&bars->q_full[b], (k >> 1) & 1, abort_flag) ||
-                            !ptx::mbar_wait_bounded(&bars->k_full[b], (k >> 1) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t qa = ptx::smem_addr(sQ + (b * 2 + qt) * AW_BOX);
-                    const uint32_t ka = ptx::smem_addr(sK + b * 2 * AW_BOX);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {   // 64 columns: 128-byte rows, 32 bytes per step
-                        const uint64_t ad = ptx::smem_desc(qa + kk * 32, 16, 1024, ptx::kLayoutSw128);
-                        const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 1024, ptx::kLayoutSw128);
-                        ptx::mma_bf16_ss(tmem + g * AW_MAX_KEYS, ad, bd, idS, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(&bars->s_full[g]);
-                    if (qt == nq - 1) {
-                        ptx::mma_commit(&bars->q_empty[b]);
-                        ptx::mma_commit(&bars->k_empty[b]);
-                    }
-                }
-                if (s >= 1) {
-                    // PV(s - 1): O = P V, P read from tensor memory
-                    const int u = s - 1, k = u / nq, qt = u - k * nq, b = k & 1, g = u & 1;
-                    if (!ptx::mbar_wait_bounded(&bars->p_full[g], (u >> 1) & 1, abort_flag) ||
-                        (qt == 0 && !ptx::mbar_wait_bounded(&bars->v_full[b], (k >> 1) & 1, abort_flag)) ||
-                        (u >= 1 && !ptx::mbar_wait_bounded(&bars->o_free, (u - 1) & 1, abort_flag))) {
+            for (int k = 0; k < n_items && ok; ++k) {
+                const int b = k & 1;
+                const uint32_t ph = (uint32_t)(k >> 1) & 1;
+                if (nq == 1 && (k & 1) != g) {
+                    if (!ptx::mbar_wait_bounded(&bars->q_full[b], ph, abort_flag) ||
+                        !ptx::mbar_wait_bounded(&bars->k_full[b], ph, abort_flag) ||
+                        !ptx::mbar_wait_bounded(&bars->v_full[b], ph, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    ptx::tc_fence_after();
-                    const uint32_t va = ptx::smem_addr(sV + b * 2 * AW_BOX);
-                    const uint32_t tP = tmem + g * AW_MAX_KEYS;
-                    for (int kk = 0; kk < ksteps; ++kk) {
-                        // V: keys are the K dimension (rows of 128 bytes), head columns the
-                        // N dimension (MN-major); P: 16 keys = 8 columns of bf16 pairs, at
-                        // the start of the slot for half 0's keys, from column `split` on
-                        // for half 1's
-                        const uint64_t bd = ptx::smem_desc(va + kk * 2048, 16, 1024, ptx::kLayoutSw128);
-                        const uint32_t pa = kk < ksplit ? tP + kk * 8 : tP + p.split + (kk - ksplit) * 8;
-                        ptx::mma_bf16_ts(tmem + AW_TMEM_O, pa, bd, idO, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(&bars->o_done);
-                    if (qt == nq - 1) ptx::mma_commit(&bars->v_empty[b]);
+                    ptx::mma_commit(&bars->q_empty[b]);
+                    ptx::mma_commit(&bars->k_empty[b]);
+                    ptx::mma_commit(&bars->v_empty[b]);
+                    continue;
                 }
+                const int u = nq == 2 ? 2 * k + g : k;   // this issuer's unit of the item
+                const int qt = u - k * nq;
+                // S(u) = Q K^T into slot g (S(u) follows P.V(u - 2) in this thread's stream,
+                // which has read P(u - 2) from the same columns)
+                if (!ptx::mbar_wait_bounded(&bars->q_full[b], ph, abort_flag) ||
+                    !ptx::mbar_wait_bounded(&bars->k_full[b], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t qa = ptx::smem_addr(sQ + (b * 2 + qt) * AW_BOX);
+                const uint32_t ka = ptx::smem_addr(sK + b * 2 * AW_BOX);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {   // 64 columns: 128-byte rows, 32 bytes per step
+                    const uint64_t ad = ptx::smem_desc(qa + kk * 32, 16, 1024, ptx::kLayoutSw128);
+                    const uint64_t bd = ptx::smem_desc(ka + kk * 32, 16, 1024, ptx::kLayoutSw128);
+                    ptx::mma_bf16_ss(tmem + g * AW_MAX_KEYS, ad, bd, idS, kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bars->s_full[g]);
+                ptx::mma_commit(&bars->q_empty[b]);
+                ptx::mma_commit(&bars->k_empty[b]);
+                // P.V(u): O = P V, P read from tensor memory. O is one accumulator for both
+                // groups: P.V(u) waits until the epilogue has read O(u - 1), on o_free[(u - 1)
+                // & 1], which only the other issuer's units advance: O(u - 3) was read before
+                // this thread issued P.V(u - 2), and O(u + 1) cannot be read before P.V(u),
+                // so the barrier is within one phase of unit u - 1.
+                if (!ptx::mbar_wait_bounded(&bars->p_full[g], (u >> 1) & 1, abort_flag) ||
+                    !ptx::mbar_wait_bounded(&bars->v_full[b], ph, abort_flag) ||
+                    (u >= 1 && !ptx::mbar_wait_bounded(&bars->o_free[(u - 1) & 1], ((u - 1) >> 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t va = ptx::smem_addr(sV + b * 2 * AW_BOX);
+                const uint32_t tP = tmem + g * AW_MAX_KEYS;
+                for (int kk = 0; kk < ksteps; ++kk) {
+                    // V: keys are the K dimension (rows of 128 bytes), head columns the
+                    // N dimension (MN-major); P: 16 keys = 8 columns of bf16 pairs, at
+                    // the start of the slot for half 0's keys, from column `split` on
+                    // for half 1's
+                    const uint64_t bd = ptx::smem_desc(va + kk * 2048, 16, 1024, ptx::kLayoutSw128);
+                    const uint32_t pa = kk < ksplit ? tP + kk * 8 : tP + p.split + (kk - ksplit) * 8;
+                    ptx::mma_bf16_ts(tmem + AW_TMEM_O, pa, bd, idO, kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(&bars->o_done);
+                ptx::mma_commit(&bars->v_empty[b]);
             }
             if (!ok) {
                 aw_error(p.err, ERRBIT_TIMEOUT_MMA);
@@ -501,7 +531,7 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&bars->o_free);
+            if (lane == 0) ptx::mbar_arrive(&bars->o_free[u & 1]);
             const int t = qt * AW_ROWS + row;
             if (live && t < p.T) {
                 __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * AW_DH;
