@@ -164,6 +164,27 @@ def test_attention_bf16(N, T, D, H):
     print("attention %s: max err / bound %.3f" % ((N, T, D, H), _close_attention(out, q, k, v, H)))
 
 
+@pytest.mark.parametrize("N,T,D,H", [
+    (64, 197, 768, 12),     # whole-row kernel, two query tiles per item: ~5 items per CTA
+    (100, 100, 768, 12),    # whole-row, one query tile per item: each MMA issuer also
+                            # releases the buffers of the other issuer's items
+    (33, 128, 768, 12),     # whole-row, one full query tile per item
+    (40, 300, 768, 12),     # key-streaming, head width 64: items of two and of one query tile
+    (20, 257, 1280, 16),    # key-streaming, head width 80: a last key tile of one key
+])
+def test_attention_bf16_many_items_per_cta(N, T, D, H):
+    # Several work items per persistent CTA: item-to-item hand-offs of the query, key and
+    # value buffers, of the score and O slots and of the O staging, over many phases of
+    # every barrier.
+    d = _dev()
+    qkv = _rand((N, T, 3 * D), 90 + T, std=1.5)
+    out = api.attention(qkv.to(d), H)
+    torch.cuda.synchronize()
+    assert api.device_error() == 0
+    q, k, v = qkv[..., :D], qkv[..., D:2 * D], qkv[..., 2 * D:]
+    print("attention %s: max err / bound %.3f" % ((N, T, D, H), _close_attention(out, q, k, v, H)))
+
+
 @pytest.mark.parametrize("T", [197, 224, 40, 100])
 def test_attention_bf16_dominant_later_keys(T):
     # Keys scaled up so that, for many query rows, a key past the first 32 scores far
