@@ -267,6 +267,29 @@ int vit_block_w_host(const void* x_host, const vit_weights* w, int64_t N, int64_
                      void* out_host, void* stream);
 
 /*
+ * vit_block_w_host_async -- vit_block_w_host without waiting: the copy of x in, the block
+ * and the copy of out back are enqueued and the call returns. The work is ordered after
+ * everything enqueued on `stream` before the call, and `stream` is ordered after the work
+ * (out_host holds the result once `stream` has reached that point: synchronise it or
+ * wait on an event recorded on it). Across calls each stage queues on a library stream of
+ * its own (one for copies in, one for blocks, one for copies out), so successive calls
+ * issued on different streams overlap: the copy in of batch i + 1 and the copy out of
+ * batch i - 1 run beside the block of batch i. Calls on one stream run one after another.
+ *
+ *   x_host, out_host  host arrays as in vit_block_w_host; pinned (page-locked) for the
+ *                     copies to run asynchronously (pageable ones work, but a copy out
+ *                     to pageable memory returns only when the copy has completed). Both
+ *                     stay owned by the caller, must stay valid, and x_host unchanged,
+ *                     until `stream` has reached the end of the call's work.
+ *   stream            as above; the handle `w` must outlive the enqueued work
+ * Returns VIT_OK once everything is enqueued. Argument errors as vit_block_w, with no
+ * work enqueued; errors of the enqueued work surface on `stream` and in vit_device_error.
+ * Results equal vit_block_w's on the same batch, bit for bit.
+ */
+int vit_block_w_host_async(const void* x_host, const vit_weights* w, int64_t N, int64_t T, double eps,
+                           void* out_host, void* stream);
+
+/*
  * vit_block_cls -- one block computed for the CLS row (row 0 of each sequence) alone.
  *
  * Definition: lecture transcript (nipunbatra.github.io), Page 55 -- when only the CLS

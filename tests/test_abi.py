@@ -172,5 +172,6 @@ def test_prepared_weights_argument_checks(lib):
     # a null handle: every call that takes one rejects it before touching the GPU
     assert lib.vit_block_w(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
     assert lib.vit_block_w_host(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
+    assert lib.vit_block_w_host_async(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
     assert lib.vit_weights_info(None, None, None, None, None, None, None) == -1
     assert lib.vit_weights_destroy(None) == 0

@@ -1,4 +1,5 @@
-"""Prepared weights: vit_weights_create, vit_block_w and vit_block_w_host.
+"""Prepared weights: vit_weights_create, vit_block_w, vit_block_w_host and
+vit_block_w_host_async.
 
 A handle holds one block's weights on the device, copied once, with the concatenated
 Q/K/V bias and, for a fold handle, the per-column terms of both folded LayerNorms
@@ -178,3 +179,45 @@ def test_fold_is_refused_where_unavailable_and_closed_handles_refuse_use():
     with pytest.raises(ValueError):
         api.vit_block_w(d.x, w, 1e-5)
     w.close()                       # closing twice is harmless
+
+
+def test_async_host_calls_overlap_and_equal_device_calls():
+    # six batches issued back to back on a ring of three streams, each into its own pinned
+    # output: every output equals vit_block_w on the same batch, bit for bit
+    dev = _dev()
+    d = make_inputs(32, 197, 768, 3072, seed=21, dtype=torch.bfloat16, affine=True)
+    w = api.VitWeights(_layer(d.to(device=dev), True), 12, fold=0)
+    xs = [make_inputs(32 + 3 * i, 197, 768, 3072, seed=40 + i, dtype=torch.bfloat16).x.pin_memory()
+          for i in range(6)]
+    outs = [torch.full_like(x, float("nan")).pin_memory() for x in xs]
+    streams = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    for i, (x, o) in enumerate(zip(xs, outs)):
+        api.vit_block_w_host_async(x, w, 1e-6, o, streams[i % 3])
+    for s in streams:
+        s.synchronize()
+    for x, o in zip(xs, outs):
+        ref = api.vit_block_w(x.to(dev), w, 1e-6)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref.cpu())
+    w.close()
+
+
+def test_async_host_calls_on_one_stream_run_in_order():
+    # two blocks chained through host memory on one stream, with no wait in between: the
+    # second call reads the first call's output buffer as its input, so it must start
+    # only after the first call's copy out has landed
+    dev = _dev()
+    d = make_inputs(4, 197, 192, 768, seed=8, dtype=torch.bfloat16, affine=True)
+    w = api.VitWeights(_layer(d.to(device=dev), True), 3, fold=1)
+    x_host = d.x.pin_memory()
+    mid = torch.full_like(x_host, float("nan")).pin_memory()
+    out = torch.full_like(x_host, float("nan")).pin_memory()
+    s = torch.cuda.Stream(device=dev)
+    api.vit_block_w_host_async(x_host, w, 1e-6, mid, s)
+    api.vit_block_w_host_async(mid, w, 1e-6, out, s)
+    s.synchronize()
+    r1 = api.vit_block_w(d.x.to(dev), w, 1e-6)
+    r2 = api.vit_block_w(r1, w, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.equal(mid, r1.cpu()) and torch.equal(out, r2.cpu())
+    w.close()

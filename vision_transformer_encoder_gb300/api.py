@@ -53,6 +53,7 @@ SIGNATURES = {
                                 ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
     "vit_block_w": (_int, [_vp, _vp, _i64, _i64, _dbl, _vp, _vp]),
     "vit_block_w_host": (_int, [_vp, _vp, _i64, _i64, _dbl, _vp, _vp]),
+    "vit_block_w_host_async": (_int, [_vp, _vp, _i64, _i64, _dbl, _vp, _vp]),
     "vit_status_string": (ctypes.c_char_p, [_int]),
     "vit_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "vit_launch_count": (_i64, []),
@@ -358,6 +359,28 @@ def vit_block_w_host(x, weights, eps, out=None, stream=None):
     with torch.cuda.device(weights.device):
         rc = lib.vit_block_w_host(_ptr(x), weights.handle, N, T, float(eps), _ptr(out), _stream(stream))
     _check(rc, "vit_block_w_host")
+    return out
+
+
+def vit_block_w_host_async(x, weights, eps, out, stream):
+    """vit_block_w_host without waiting: enqueues the copy of host x in, the block and the
+    copy back into host `out` after the work on `stream`, and returns. `out` holds the
+    result once `stream` has reached that point; x, out and the handle must outlive the
+    work. Successive calls on different streams overlap their copies with each other's
+    blocks (pinned x and out)."""
+    lib = load_library()
+    if x.is_cuda or not x.is_contiguous() or x.dtype != weights.dtype:
+        raise ValueError("vit_block_w_host_async takes a contiguous host x of the weights' dtype")
+    if out is None or out.is_cuda or not out.is_contiguous() or out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("vit_block_w_host_async takes a contiguous host out shaped like x")
+    if stream is None:
+        raise ValueError("vit_block_w_host_async needs an explicit stream to order its work")
+    N, T, D = x.shape
+    if D != weights.D:
+        raise ValueError("x has width %d, the weights %d" % (D, weights.D))
+    with torch.cuda.device(weights.device):
+        rc = lib.vit_block_w_host_async(_ptr(x), weights.handle, N, T, float(eps), _ptr(out), _stream(stream))
+    _check(rc, "vit_block_w_host_async")
     return out
 
 

@@ -1125,7 +1125,12 @@ BlockArgs prepared_args(const vit_weights* w, const void* x, int64_t N, int64_t 
 // Host-buffer pipeline of vit_block_host and vit_block_w_host. `h` holds host pointers:
 // x and out, and the weights and affine terms unless prepared weights `pw` are given, in
 // which case only x and out cross the link.
-int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
+// Host x in, host out. Synchronous: chunks of whole sequences overlap their copies with
+// each other's blocks, and `stream` is synchronised before returning. Asynchronous: the
+// whole batch is one chunk and nothing waits on the host; the stages of successive calls
+// (copy in, block, copy out) queue on the three library streams, so a call's copies run
+// beside the blocks of the calls before and after it.
+int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream, bool async = false) {
     const int64_t N = h.N, T = h.T, D = h.D, F = h.F;
     const int dtype = h.dt;
     DeviceState* st = nullptr;
@@ -1148,18 +1153,19 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
         if (i < 13 && !src[i]) continue;
         total += round_up(sizes[i], 256);
     }
-    const std::vector<int64_t> chunk_n = host_chunks(N, T);
+    const std::vector<int64_t> chunk_n = async ? std::vector<int64_t>{N} : host_chunks(N, T);
     const int64_t chunks = (int64_t)chunk_n.size();
+    const bool staged = async || chunks > 1;   // on the library streams
     // copy-in, compute (successive chunks alternate between two streams, so that one
     // chunk's kernels can fill the SMs another's leave idle at their ends), copy-out
     cudaStream_t sh = s, sd = s;
     cudaStream_t scs[2] = {s, s};
-    if (chunks > 1) {
+    if (staged) {
         rc = pipeline_streams(st);
         if (rc != VIT_OK) return rc;
         sh = st->h2d;
         scs[0] = st->comp;
-        scs[1] = host_compute_streams() > 1 ? st->comp2 : st->comp;
+        scs[1] = !async && host_compute_streams() > 1 ? st->comp2 : st->comp;
         sd = st->d2h;
     }
     void* dmem = nullptr;
@@ -1180,7 +1186,7 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
         return r;
     };
     cudaEvent_t start = nullptr, end_d2h = nullptr, end_comp[2] = {nullptr, nullptr};
-    if (chunks > 1) {
+    if (staged) {
         e = new_event(&start);
         if (e == cudaSuccess) e = cudaEventRecord(start, s);   // after the allocation
         if (e == cudaSuccess) e = cudaStreamWaitEvent(sh, start, 0);
@@ -1200,7 +1206,7 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
         e = cudaMemcpyAsync(base + off[0] + o, static_cast<const uint8_t*>(h.x) + o, nbytes,
                             cudaMemcpyHostToDevice, sh);
         cudaEvent_t in_ready = nullptr, done = nullptr;
-        if (chunks > 1) {
+        if (staged) {
             if (e == cudaSuccess) e = new_event(&in_ready);
             if (e == cudaSuccess) e = cudaEventRecord(in_ready, sh);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, in_ready, 0);
@@ -1217,7 +1223,7 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
             rc = enqueue_block(d, st->info, sc);
         }
         if (rc != VIT_OK) break;
-        if (chunks > 1) {
+        if (staged) {
             e = new_event(&done);
             if (e == cudaSuccess) e = cudaEventRecord(done, sc);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(sd, done, 0);
@@ -1227,7 +1233,7 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
             e = cudaMemcpyAsync(static_cast<uint8_t*>(h.out) + o, out_c, nbytes, cudaMemcpyDeviceToHost, sd);
         n0 += nc;
     }
-    if (chunks > 1) {
+    if (staged) {
         // join: the caller's stream waits for the last copy out and the last block (and
         // so for every copy in), then frees the buffers in its own order
         cudaError_t je = new_event(&end_d2h);
@@ -1244,7 +1250,8 @@ int host_pipeline(const BlockArgs& h, const vit_weights* pw, void* stream) {
         if (e == cudaSuccess) e = je;
     }
     cudaError_t fe = cudaFreeAsync(dmem, s);
-    cudaError_t se = cudaStreamSynchronize(s);
+    // an event destroyed before it completes is released once it does
+    cudaError_t se = async ? cudaSuccess : cudaStreamSynchronize(s);
     for (cudaEvent_t x : ev) cudaEventDestroy(x);
     if (rc != VIT_OK) return rc;
     if (e == cudaSuccess) e = fe;
@@ -1567,6 +1574,18 @@ int vit_block_w_host(const void* x_host, const vit_weights* w, int64_t N, int64_
     if (cudaGetDevice(&dev) != cudaSuccess) return VIT_ERR_CUDA;
     if (dev != w->device) return VIT_ERR_ARG;
     return host_pipeline(a, w, stream);
+}
+
+int vit_block_w_host_async(const void* x_host, const vit_weights* w, int64_t N, int64_t T, double eps,
+                           void* out_host, void* stream) {
+    if (!w) return VIT_ERR_ARG;
+    const BlockArgs a = prepared_args(w, x_host, N, T, eps, out_host);
+    int rc = validate(a);
+    if (rc != VIT_OK) return rc;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VIT_ERR_CUDA;
+    if (dev != w->device) return VIT_ERR_ARG;
+    return host_pipeline(a, w, stream, true);
 }
 
 int vit_layernorm(const void* x, int64_t rows, int64_t D, double eps, const void* gamma,
