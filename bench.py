@@ -297,20 +297,26 @@ def run_reference(args):
     return 0
 
 
-OTHER_CONFIGS = ("vit_ti16", "vit_l16_384", "vit_h14_448")
+# the other block shapes of the workload list in bf16, and the fp32 path (3xTF32 tensor
+# cores) at the ViT-Ti/16 shape, which the list gives in fp32 too, and at ViT-B/16
+OTHER_CONFIGS = (("vit_ti16", False), ("vit_l16_384", False), ("vit_h14_448", False),
+                 ("vit_ti16", True), ("vit_b16", True))
 
 
 def time_other_configs(K, W, flush, stream, sampler):
-    """The other block shapes of the workload list (bf16), after the headline: per shape W
-    warm-up steps, K steps timed with events on the launching stream (L2 flushed between
-    steps, outside the events), then K steps with per-kernel events for the slowest
-    kernel. Returns {name: figures}."""
+    """The other workloads, after the headline: per workload W warm-up steps, K steps
+    timed with events on the launching stream (L2 flushed between steps, outside the
+    events), then K steps with per-kernel events for the slowest kernel. Returns
+    {name: figures}; fp32 entries are named "<shape>_f32" and their fractions are of the
+    3xTF32 contraction peak."""
     peaks, _ = load_peaks()
     dev = torch.device("cuda", torch.cuda.current_device())
     res = {}
-    for name in OTHER_CONFIGS:
+    for name, f32 in OTHER_CONFIGS:
         c = CONFIGS[name]
-        d = make_config_inputs(name, seed=0, dtype=torch.bfloat16).to(device=dev)
+        dt = torch.float32 if f32 else torch.bfloat16
+        tc_peak = peaks["bf16_tflops"] * (TF32X3_OF_BF16 if f32 else 1.0)
+        d = make_config_inputs(name, seed=0, dtype=dt).to(device=dev)
         out = torch.empty_like(d.x)
 
         def step():
@@ -338,16 +344,17 @@ def time_other_configs(K, W, flush, stream, sampler):
         api.timing_enable(False)
         pk = {k: v for k, v in api.timing_collect().items() if v[1] > 0}
         dom = max(pk, key=lambda k: pk[k][0])
-        bound, amount, _u = kernel_work(c)[dom]
+        bound, amount, _u = kernel_work(c, f32)[dom]
         dom_s = pk[dom][0] / pk[dom][1] / 1e3
         tfl = flops_per_step(c) / (ms / 1e3) / 1e12
-        dom_fig = amount / dom_s / (1e12 if bound == "tensor" else 1e9)
-        dom_peak = peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"]
-        res[name] = {"workload": workload_name(name, c), "ms_per_step": ms,
+        dom_fig = amount / dom_s / (1e9 if bound == "hbm" else 1e12)
+        dom_peak = {"tensor": tc_peak, "alu": FP32_ALU_TFLOPS, "hbm": peaks["hbm_gbs"]}[bound]
+        res[name + ("_f32" if f32 else "")] = {
+                     "workload": workload_name(name, c), "dtype": "f32" if f32 else "bf16", "ms_per_step": ms,
                      "tokens_per_s": c["N"] * c["T"] / (ms / 1e3), "tflops": tfl,
-                     "frac_of_peak": tfl / peaks["bf16_tflops"], "steps": K, "warmup": W,
+                     "frac_of_peak": tfl / tc_peak, "steps": K, "warmup": W,
                      "dominant_kernel": {"kernel": dom, "avg_us": dom_s * 1e6, "bound": bound,
-                                         "achieved": dom_fig, "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
+                                         "achieved": dom_fig, "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
                                          "frac": dom_fig / dom_peak},
                      "kernels_us": {k: 1e3 * v[0] / v[1] for k, v in pk.items()},
                      "clocks": sampler.summary(t0, t1)}
