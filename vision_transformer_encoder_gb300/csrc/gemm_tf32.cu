@@ -8,12 +8,12 @@
 // Serves the fp32 path of the block ("ViT Encoder Block" (crackedaicode): the Q, K, V,
 // output and MLP products). Split kernels first write A_lo (same layout as A) and, for a
 // weight stored (in, out), its transpose W^T and W^T_lo (out rows, K contiguous), so both
-// operands are K-major. The GEMM is a single-CTA persistent kernel: 128 x 128 output
-// tiles, K blocks of 32 (one 128-byte swizzled row of fp32), three stages of four 16 KB
-// TMA boxes (A, A_lo, W^T, W^T_lo), one box per producer warp; the MMA warp issues per
-// 8-element K step the three kind::tf32 MMAs into a double-buffered TMEM accumulator;
-// four epilogue warps (one per TMEM lane quarter) add bias and residual or apply GELU
-// (fp32 tanh) and store fp32 rows. Every wait is bounded.
+// operands are K-major. The GEMM is a persistent CTA-pair kernel: 256 x 256 output tiles,
+// K blocks of 32 (one 128-byte swizzled row of fp32), three stages of four 16 KB TMA boxes
+// per CTA (A, A_lo, W^T, W^T_lo), one box per producer warp; the leader's MMA thread issues
+// per 8-element K step the three kind::tf32 pair MMAs into a double-buffered TMEM
+// accumulator; eight epilogue warps per CTA add bias and residual or apply GELU (fp32
+// tanh) and store fp32 rows. Every wait is bounded.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -21,19 +21,16 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "ptx.cuh"
 
 namespace vit {
 namespace {
 
-constexpr int XM = 128, XN = 128, XK = 32, XSTAGES = 3;
+constexpr int XM = 128, XK = 32, XSTAGES = 3;     // rows per CTA, K block, ring stages
 constexpr int X_BOX = 128 * XK * 4;                  // 16 KB: 128 rows x 32 fp32
 constexpr int X_STAGE = 4 * X_BOX;                   // A, A_lo, W^T, W^T_lo
-constexpr int X_ACC_COLS = XN;
-constexpr int X_TMEM_COLS = 2 * X_ACC_COLS;
-constexpr int X_THREADS = 288;   // warps 0-3 epilogue, 4-7 TMA (one operand each), 8 MMA
 constexpr int X_BAR_BYTES = 256;
-constexpr int X_SMEM = XSTAGES * X_STAGE + X_BAR_BYTES + 1024;
 
 struct XParams {
     int M, N, K;
@@ -50,16 +47,6 @@ __device__ __forceinline__ void x_error(uint32_t* err, uint32_t bit) {
     if (err) atomicOr(err, bit);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // Instruction descriptor, kind::tf32: D fp32 (bits 4-5 = 1), A and B TF32 (format 2 at
 // bits 7-9 and 10-12), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
@@ -68,10 +55,39 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
 
 __device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
 
-__global__ void __launch_bounds__(X_THREADS, 1)
-gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
-                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
-                   const XParams p) {
+// The two CTAs of a cluster compute a 256 x 256 output tile with
+// tcgen05.mma.cta_group::2.kind::tf32 (M 256 split 128 / 128 over the CTAs, N 256 split
+// 128 / 128 over their shared memory). Per K block of 32 each CTA stages four 16 KB boxes
+// (its 128 rows of A and A_lo, its 128 rows of W^T and W^T_lo); the MMA reads both CTAs'
+// halves of W^T, so each operand byte feeds twice the products of a single-CTA 128 x 128
+// tile.
+//   warps 0, 2, 3, 4  TMA producers (A, A_lo, W^T, W^T_lo), both CTAs; every copy of the
+//                     pair completes on the leader's ring barrier
+//   warp 1            allocates 512 TMEM columns (two 256-column accumulators) on both
+//                     CTAs; the leader's lane 0 issues the pair MMAs and multicasts its
+//                     commits (ring slot free, accumulator ready) to both CTAs
+//   warps 5-12        epilogue, two warps per TMEM lane quarter (128 columns each): bias,
+//                     fp32 tanh GELU or residual, fp32 rows stored from registers
+constexpr int XP_THREADS = 416;
+constexpr int XP_EPI_WARPS = 8;
+constexpr int XP_ACC_COLS = 256;
+constexpr int XP_TMEM_COLS = 2 * XP_ACC_COLS;
+constexpr int XP_SMEM = XSTAGES * X_STAGE + X_BAR_BYTES + 1024;
+
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(XP_THREADS, 1)
+gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
+                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
+                        const XParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -84,74 +100,88 @@ gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m_tiles = (p.M + XM - 1) / XM;
-    const int n_tiles = (p.N + XN - 1) / XN;
+    const uint32_t rank = ptx::cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const int m_tiles = (p.M + 2 * XM - 1) / (2 * XM);
+    const int n_tiles = (p.N + XP_ACC_COLS - 1) / XP_ACC_COLS;
     const int num_tiles = m_tiles * n_tiles;
     const int kblocks = (p.K + XK - 1) / XK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < XSTAGES; ++s) {
-            ptx::mbar_init(full + s, 4);     // one expect-tx arrival per producer warp
+            ptx::mbar_init(full + s, 1);    // the leader's expect-tx arrival; bytes of both CTAs
             ptx::mbar_init(empty + s, 1);
         }
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(tfull + a, 1);
-            ptx::mbar_init(tempty + a, 128);
+            ptx::mbar_init(tempty + a, 2 * XP_EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 8) {
-        ptx::tmem_alloc(tmem_slot, X_TMEM_COLS);
-        ptx::tmem_relinquish();
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmAlo);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmBlo);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(tmem_slot, XP_TMEM_COLS);
+        ptx::tmem_relinquish_pair();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    ptx::cluster_sync();  // barriers of both CTAs initialised before any remote arrive
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the set-up above overlaps the previous kernel's tail; A and A_lo are its output
+    griddep_wait();
+    griddep_launch_dependents();
 
-    if (warp >= 4 && warp <= 7) {
+    const int prod = warp == 0 ? 0 : (warp >= 2 && warp <= 4) ? warp - 1 : -1;   // 0 A, 1 A_lo, 2 W^T, 3 W^T_lo
+    if (prod >= 0) {
         if (lane == 0) {
-            // ------------------------------------------ TMA producers, one operand each
-            const int which = warp - 4;   // 0 A, 1 A_lo, 2 W^T, 3 W^T_lo
-            const CUtensorMap* tm = which == 0 ? &tmA : which == 1 ? &tmAlo : which == 2 ? &tmB : &tmBlo;
-            ptx::prefetch_tensormap(tm);
+            // -------------------------------------------- TMA producers (both ranks)
+            const CUtensorMap* tm = prod == 0 ? &tmA : prod == 1 ? &tmAlo : prod == 2 ? &tmB : &tmBlo;
+            const uint32_t full0 = ptx::mapa_shared(ptx::smem_addr(full), 0);   // leader's
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int r0 = which < 2 ? (tile / n_tiles) * XM : (tile % n_tiles) * XN;
+            for (int tile = cluster; tile < num_tiles && ok; tile += nclusters) {
+                const int r0 = prod < 2 ? (tile / n_tiles) * 2 * XM + (int)rank * XM
+                                        : (tile % n_tiles) * XP_ACC_COLS + (int)rank * (XP_ACC_COLS / 2);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % XSTAGES, u = it / XSTAGES;
                     if (!ptx::mbar_wait_bounded<true>(empty + s, (u & 1) ^ 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(full + s, X_BOX);
-                    ptx::tma_load_2d(smem + s * X_STAGE + which * X_BOX, tm, full + s, kb * XK, r0);
+                    if (prod == 0 && rank == 0) ptx::mbar_arrive_expect_tx(full + s, 2 * X_STAGE);
+                    ptx::tma_load_2d_pair(smem + s * X_STAGE + prod * X_BOX, tm, full0 + s * 8, kb * XK, r0);
                 }
             }
             if (!ok) {
                 x_error(p.err, ERRBIT_TIMEOUT_PRODUCER);
                 *abort_flag = 1;
             }
-            // let the copies this thread issued land before the CTA can exit
-            for (uint32_t s = 0; s < XSTAGES; ++s) {
-                if (it > s) {
-                    const uint32_t u_last = (it - 1 - s) / XSTAGES;
-                    if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
-                        x_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+            if (prod == 0 && rank == 0) {
+                // every copy of both CTAs completes on these barriers: let them land
+                for (uint32_t s = 0; s < XSTAGES; ++s) {
+                    if (it > s) {
+                        const uint32_t u_last = (it - 1 - s) / XSTAGES;
+                        if (!ptx::mbar_wait_bounded(full + s, u_last & 1, nullptr))
+                            x_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
+                    }
                 }
             }
         }
-    } else if (warp == 8) {
-        if (lane == 0) {
-            // ---------------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_tf32(XM, XN);
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // -------------------------------------------- pair MMA issuer (leader)
+            constexpr uint32_t idesc = idesc_tf32(2 * XM, XP_ACC_COLS);
             uint32_t it = 0;
             int local = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
                 const int acc = local & 1;
                 const uint32_t v = (uint32_t)(local >> 1);
                 if (!ptx::mbar_wait_bounded(tempty + acc, (v & 1) ^ 1, abort_flag)) {
@@ -159,7 +189,7 @@ gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * X_ACC_COLS;
+                const uint32_t d_tmem = tmem_base + acc * XP_ACC_COLS;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const uint32_t s = it % XSTAGES, u = it / XSTAGES;
                     if (!ptx::mbar_wait_bounded(full + s, u & 1, abort_flag)) {
@@ -175,27 +205,29 @@ gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         const uint64_t alo = ptx::smem_desc(st + X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
                         const uint64_t b = ptx::smem_desc(st + 2 * X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
                         const uint64_t blo = ptx::smem_desc(st + 3 * X_BOX + k * 32, 16, 1024, ptx::kLayoutSw128);
-                        mma_tf32(d_tmem, alo, b, idesc, (kb | k) != 0 ? 1u : 0u);
-                        mma_tf32(d_tmem, a, blo, idesc, 1u);
-                        mma_tf32(d_tmem, a, b, idesc, 1u);
+                        mma_tf32_pair(d_tmem, alo, b, idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_tf32_pair(d_tmem, a, blo, idesc, 1u);
+                        mma_tf32_pair(d_tmem, a, b, idesc, 1u);
                     }
-                    ptx::mma_commit(empty + s);
+                    ptx::mma_commit_pair_mc(empty + s, 0x3);
                 }
                 if (!ok) break;
-                ptx::mma_commit(tfull + acc);
+                ptx::mma_commit_pair_mc(tfull + acc, 0x3);
             }
             if (!ok) {
                 x_error(p.err, ERRBIT_TIMEOUT_MMA);
                 *abort_flag = 1;
             }
-            ptx::mma_commit(done);
+            ptx::mma_commit_pair(done);
             if (!ptx::mbar_wait_bounded(done, 0, nullptr)) x_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------- epilogue warps 0-3
-        const int quarter = warp;
+    } else {
+        // ---------------------------------------------- epilogue warps 5..12 (both ranks)
+        const int quarter = warp & 3;               // TMEM lane quarter this warp may read
+        const int half = (warp - 5) >> 2;           // which 128 of the 256 columns
+        const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);   // leader's
         int local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
             const int acc = local & 1;
             const uint32_t v = (uint32_t)(local >> 1);
             const bool ok = __all_sync(0xffffffffu, ptx::mbar_wait_bounded<true>(tfull + acc, v & 1, abort_flag));
@@ -205,11 +237,12 @@ gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 break;
             }
             ptx::tc_fence_after();
-            const int row = (tile / n_tiles) * XM + quarter * 32 + lane;
-            const int n0 = (tile % n_tiles) * XN;
-            const uint32_t t_row = tmem_base + acc * X_ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+            const int row = (tile / n_tiles) * 2 * XM + (int)rank * XM + quarter * 32 + lane;
+            const int n0 = (tile % n_tiles) * XP_ACC_COLS + half * 128;
+            const uint32_t t_row =
+                tmem_base + acc * XP_ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll 1
-            for (int c = 0; c < XN / 32; ++c) {
+            for (int c = 0; c < 4; ++c) {
                 uint32_t r[32];
                 ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
                 ptx::tmem_ld_wait();
@@ -238,14 +271,16 @@ gemm_tf32x3_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 }
             }
             ptx::tc_fence_before();
-            ptx::mbar_arrive(tempty + acc);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive_cluster_relaxed(tempty0 + acc * 8);   // orders TMEM reads only
         }
     }
 
     __syncthreads();
-    if (warp == 8) {
+    ptx::cluster_sync();  // no CTA leaves while its peer may still touch its memory
+    if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, X_TMEM_COLS);
+        ptx::tmem_dealloc_pair(tmem_base, XP_TMEM_COLS);
     }
 }
 
@@ -362,14 +397,15 @@ cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cud
     p.err = dev.err_word;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, X_SMEM);
+        cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             XP_SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    const int64_t tiles = ((d.M + XM - 1) / XM) * ((d.N + XN - 1) / XN);
-    const int grid = (int)(tiles < dev.num_sms ? tiles : dev.num_sms);
-    gemm_tf32x3_kernel<<<grid, X_THREADS, X_SMEM, s>>>(ma, malo, mb, mblo, p);
-    return cudaGetLastError();
+    const int64_t tiles = ((d.M + 2 * XM - 1) / (2 * XM)) * ((d.N + XP_ACC_COLS - 1) / XP_ACC_COLS);
+    const int64_t pairs = dev.num_sms / 2;
+    const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
+    return launch_dependent(gemm_tf32x3_pair_kernel, dim3(grid), dim3(XP_THREADS), XP_SMEM, s, ma, malo, mb, mblo, p);
 }
 
 }  // namespace vit
