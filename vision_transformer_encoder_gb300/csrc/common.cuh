@@ -63,6 +63,12 @@ __device__ __forceinline__ float tanh_approx(float x) {
     return y;
 }
 
+// x - x_hi, where x_hi is x with its 13 low mantissa bits cleared (the TF32 value a
+// tensor core takes from an fp32 operand): the low part of a 3xTF32 product, exact in fp32.
+__device__ __forceinline__ float tf32_low_part(float x) {
+    return x - __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
 // Hardware base-2 exponential approximation (MUFU).
 __device__ __forceinline__ float exp2_approx(float x) {
     float y;

@@ -17,6 +17,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -296,12 +297,25 @@ __global__ void split_lo_kernel(const float* __restrict__ a, int64_t rows, int64
     }
 }
 
-// W (K x N, ldw) -> W^T and W^T_lo (N x K) at rows [row0, row0 + N) of the outputs,
-// through 32 x 32 shared-memory tiles.
-__global__ void split_wt_kernel(const float* __restrict__ w, int64_t K, int64_t N, int64_t ldw, int64_t row0,
-                                float* __restrict__ wt, float* __restrict__ wt_lo) {
+// Up to kMaxSplitJobs weights per launch: job j is W_j (K x N, ldw) -> W_j^T and W_j^T_lo
+// (N x K) at rows [row0, row0 + N) of its outputs, through 32 x 32 shared-memory tiles;
+// the launch's CTAs cover the jobs' tiles one after another (first[j] = first CTA of j).
+struct SplitWtBatch {
+    SplitWtJob job[kMaxSplitJobs];
+    int first[kMaxSplitJobs + 1];
+    int njobs;
+};
+
+__global__ void split_wt_kernel(const __grid_constant__ SplitWtBatch b) {
     __shared__ float tile[32][33];
-    const int64_t k0 = (int64_t)blockIdx.y * 32, n0 = (int64_t)blockIdx.x * 32;
+    int j = 0;
+    while (j + 1 < b.njobs && (int)blockIdx.x >= b.first[j + 1]) ++j;
+    const float* __restrict__ w = b.job[j].w;
+    const int64_t K = b.job[j].K, N = b.job[j].N, ldw = b.job[j].ldw, row0 = b.job[j].row0;
+    float* __restrict__ wt = b.job[j].wt;
+    float* __restrict__ wt_lo = b.job[j].wt_lo;
+    const int64_t ntx = (N + 31) / 32, t = (int64_t)blockIdx.x - b.first[j];
+    const int64_t k0 = (t / ntx) * 32, n0 = (t % ntx) * 32;
     for (int i = threadIdx.y; i < 32; i += blockDim.y) {
         const int64_t k = k0 + i, n = n0 + threadIdx.x;
         tile[i][threadIdx.x] = (k < K && n < N) ? w[k * ldw + n] : 0.f;
@@ -366,11 +380,21 @@ cudaError_t launch_split_lo(const float* a, int64_t rows, int64_t cols, int64_t 
     return cudaGetLastError();
 }
 
-cudaError_t launch_split_wt(const float* w, int64_t K, int64_t N, int64_t ldw, int64_t row0, float* wt, float* wt_lo,
-                            cudaStream_t s) {
-    if (K <= 0 || N <= 0) return cudaSuccess;
-    const dim3 grid((unsigned)((N + 31) / 32), (unsigned)((K + 31) / 32));
-    split_wt_kernel<<<grid, dim3(32, 8), 0, s>>>(w, K, N, ldw, row0, wt, wt_lo);
+cudaError_t launch_split_wt(const SplitWtJob* jobs, int njobs, cudaStream_t s) {
+    if (njobs <= 0 || njobs > kMaxSplitJobs) return cudaErrorInvalidValue;
+    SplitWtBatch b;
+    std::memset(&b, 0, sizeof(b));
+    int64_t total = 0;
+    b.njobs = njobs;
+    for (int j = 0; j < njobs; ++j) {
+        b.job[j] = jobs[j];
+        b.first[j] = (int)total;
+        if (jobs[j].K > 0 && jobs[j].N > 0) total += ((jobs[j].N + 31) / 32) * ((jobs[j].K + 31) / 32);
+        if (total > 0x7fffffff) return cudaErrorInvalidValue;
+    }
+    b.first[njobs] = (int)total;
+    if (total == 0) return cudaSuccess;
+    split_wt_kernel<<<(unsigned)total, dim3(32, 8), 0, s>>>(b);
     return cudaGetLastError();
 }
 

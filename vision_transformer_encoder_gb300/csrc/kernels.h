@@ -27,6 +27,10 @@ cudaError_t launch_selftest_wait(int abort_first, uint32_t* err, cudaStream_t s)
 // ---- LayerNorm (layernorm.cu) -------------------------------------------------
 // out = LN(x) [* gamma + beta] row by row. Pairs: bf16->bf16, f32->bf16, f32->f32,
 // f64->f64, bf16->f32. gamma/beta (either may be null) have element type gb_dt.
+// fp32 LayerNorm that also writes the low part of each output (tf32_low_part) to lo,
+// contiguous rows x D: the A_lo operand of a following 3xTF32 product.
+cudaError_t launch_layernorm_f32_lo(const float* x, float* out, float* lo, const void* gamma, const void* beta,
+                                    int gb_dt, int64_t rows, int64_t D, double eps, cudaStream_t s);
 cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt,
                              const void* gamma, const void* beta, int gb_dt, int64_t rows,
                              int64_t D, double eps, cudaStream_t s);
@@ -150,8 +154,17 @@ struct Tf32GemmDesc {
 };
 bool tf32x3_supported(int64_t M, int64_t N, int64_t K, int64_t lda, const void* a);
 cudaError_t launch_split_lo(const float* a, int64_t rows, int64_t cols, int64_t lda, float* lo, cudaStream_t s);
-cudaError_t launch_split_wt(const float* w, int64_t K, int64_t N, int64_t ldw, int64_t row0, float* wt, float* wt_lo,
-                            cudaStream_t s);
+// One weight of launch_split_wt: W (K x N, row stride ldw) -> W^T and W^T_lo (N x K) at
+// rows [row0, row0 + N) of wt and wt_lo.
+struct SplitWtJob {
+    const float* w;
+    int64_t K, N, ldw, row0;
+    float* wt;
+    float* wt_lo;
+};
+constexpr int kMaxSplitJobs = 6;
+// All jobs in one launch (at most kMaxSplitJobs).
+cudaError_t launch_split_wt(const SplitWtJob* jobs, int njobs, cudaStream_t s);
 cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cudaStream_t s);
 
 // ---- Patch embedding (patch_embed.cu) ----------------------------------------

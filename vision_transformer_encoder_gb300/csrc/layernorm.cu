@@ -152,7 +152,8 @@ __device__ __forceinline__ A ld_param(const void* p, int dt, int64_t i) {
 template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(LN_THREADS)
 ln_generic_kernel(const TIn* __restrict__ x, TOut* __restrict__ out, const void* __restrict__ gamma,
-                  const void* __restrict__ beta, int gb_dt, int64_t rows, int64_t D, double eps) {
+                  const void* __restrict__ beta, int gb_dt, int64_t rows, int64_t D, double eps,
+                  float* __restrict__ lo) {
     using A = typename std::conditional<std::is_same<TIn, double>::value, double, float>::type;
     const int64_t row = (int64_t)blockIdx.x * (LN_THREADS / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -173,16 +174,19 @@ ln_generic_kernel(const TIn* __restrict__ x, TOut* __restrict__ out, const void*
         A o = (to_acc<A>(xr[j]) - mean) / denom;
         if (gamma) o = ld_param<A>(gamma, gb_dt, j) * o;
         if (beta) o = o + ld_param<A>(beta, gb_dt, j);
-        orow[j] = from_acc<TOut>(o);
+        const TOut v = from_acc<TOut>(o);
+        orow[j] = v;
+        if constexpr (std::is_same<TOut, float>::value)
+            if (lo) lo[row * D + j] = tf32_low_part(v);
     }
 }
 
 template <typename TIn, typename TOut>
 cudaError_t launch_generic(const void* x, void* out, const void* g, const void* b, int gb_dt,
-                           int64_t rows, int64_t D, double eps, cudaStream_t s) {
+                           int64_t rows, int64_t D, double eps, cudaStream_t s, float* lo = nullptr) {
     const int64_t blocks = (rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32);
     ln_generic_kernel<TIn, TOut><<<(unsigned)blocks, LN_THREADS, 0, s>>>(
-        static_cast<const TIn*>(x), static_cast<TOut*>(out), g, b, gb_dt, rows, D, eps);
+        static_cast<const TIn*>(x), static_cast<TOut*>(out), g, b, gb_dt, rows, D, eps, lo);
     return cudaGetLastError();
 }
 
@@ -219,6 +223,13 @@ cudaError_t launch_fast(const void* x, void* out, const void* g, const void* b, 
 }
 
 }  // namespace
+
+cudaError_t launch_layernorm_f32_lo(const float* x, float* out, float* lo, const void* gamma, const void* beta,
+                                    int gb_dt, int64_t rows, int64_t D, double eps, cudaStream_t s) {
+    if (rows <= 0 || D <= 0) return cudaSuccess;
+    if ((rows + LN_THREADS / 32 - 1) / (LN_THREADS / 32) > 0x7fffffff) return cudaErrorInvalidValue;
+    return launch_generic<float, float>(x, out, gamma, beta, gb_dt, rows, D, eps, s, lo);
+}
 
 cudaError_t launch_layernorm(const void* x, int in_dt, void* out, int out_dt, const void* gamma,
                              const void* beta, int gb_dt, int64_t rows, int64_t D, double eps,

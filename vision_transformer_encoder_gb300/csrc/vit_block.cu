@@ -483,7 +483,10 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
             return launch_gemm_simt(sd, s);
         }));
     } else if (w.tf32) {
-        // fp32: LayerNorm and attention on the CUDA cores, the products as 3xTF32
+        // fp32: LayerNorm on the CUDA cores, attention and the products as 3xTF32. Each
+        // product's A_lo (the low part of its A operand) is written by the LayerNorm that
+        // makes A, or by a split pass after attention and after W1 (whose row-per-thread
+        // stores measured slower writing a second output than the pass costs).
         uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // A_lo, then the split weights
         float* lo = reinterpret_cast<float*>(tail);
         float* wt = reinterpret_cast<float*>(tail + w.sz_lo);
@@ -498,23 +501,22 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         float* fh = static_cast<float*>(h);
         step(run(K_TF32_SPLIT, s, [&] {
             const void* wq[3] = {a.w_q, a.w_k, a.w_v};
-            cudaError_t r = cudaSuccess;
-            for (int i = 0; i < 3 && r == cudaSuccess; ++i)
-                r = launch_split_wt(static_cast<const float*>(wq[i]), D, D, D, i * D, wqkv_t, wqkv_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo, s);
-            return r;
+            const SplitWtJob jobs[6] = {
+                {static_cast<const float*>(wq[0]), D, D, D, 0, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(wq[1]), D, D, D, D, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(wq[2]), D, D, D, 2 * D, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo},
+                {static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo},
+                {static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo}};
+            return launch_split_wt(jobs, 6, s);
         }));
         auto gemm = [&](const float* A, int64_t K, const float* bt, const float* btlo, int64_t N, int epi,
                         const void* bias, const float* res, float* out) {
-            cudaError_t r = launch_split_lo(A, M, K, K, lo, s);
-            if (r != cudaSuccess) return r;
             Tf32GemmDesc g{A, K, lo, bt, btlo, M, N, K, epi, static_cast<const float*>(bias), res, N, out, N};
             return launch_gemm_tf32x3(g, dev, s);
         };
         step(run(K_LN1, s, [&] {
-            return launch_layernorm(a.x, DT_F32, buf, DT_F32, a.ln1_g, a.ln1_b, DT_F32, M, D, a.eps, s);
+            return launch_layernorm_f32_lo(fx, fbuf, lo, a.ln1_g, a.ln1_b, DT_F32, M, D, a.eps, s);
         }));
         if (has_qkv_bias(a)) step(concat_qkv_bias(a, s));
         const void* bqkv = has_qkv_bias(a) ? a.bias_scratch : nullptr;
@@ -524,13 +526,17 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
                 return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s);
             return launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
         }));
-        step(run(K_WO, s, [&] { return gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy); }));
+        step(run(K_WO, s, [&] {
+            cudaError_t r = launch_split_lo(fbuf, M, D, D, lo, s);
+            return r == cudaSuccess ? gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy) : r;
+        }));
         step(run(K_LN2, s, [&] {
-            return launch_layernorm(y, DT_F32, buf, DT_F32, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
+            return launch_layernorm_f32_lo(fy, fbuf, lo, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
         }));
         step(run(K_W1, s, [&] { return gemm(fbuf, D, w1_t, w1_lo, F, TC_EPI_GELU, a.b1, nullptr, fh); }));
         step(run(K_W2, s, [&] {
-            return gemm(fh, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, fy, static_cast<float*>(a.out));
+            cudaError_t r = launch_split_lo(fh, M, F, F, lo, s);
+            return r == cudaSuccess ? gemm(fh, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, fy, static_cast<float*>(a.out)) : r;
         }));
     } else {
         const int dt = a.dt;
@@ -746,13 +752,14 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         float* w2_t = w1_lo + F * D, *w2_lo = w2_t + D * F;
         step(run(K_TF32_SPLIT, s, [&] {
             const void* wq[3] = {a.w_q, a.w_k, a.w_v};
-            cudaError_t r = cudaSuccess;
-            for (int i = 0; i < 3 && r == cudaSuccess; ++i)
-                r = launch_split_wt(static_cast<const float*>(wq[i]), D, D, D, i * D, wqkv_t, wqkv_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo, s);
-            if (r == cudaSuccess) r = launch_split_wt(static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo, s);
-            return r;
+            const SplitWtJob jobs[6] = {
+                {static_cast<const float*>(wq[0]), D, D, D, 0, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(wq[1]), D, D, D, D, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(wq[2]), D, D, D, 2 * D, wqkv_t, wqkv_lo},
+                {static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo},
+                {static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo},
+                {static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo}};
+            return launch_split_wt(jobs, 6, s);
         }));
         // out (rows, N) = epi(A (rows, K; row stride lda) @ W + bias [+ res (row stride ldr)])
         auto gemm = [&](const void* A, int64_t rows, int64_t K, int64_t lda, const float* bt, const float* btlo,
@@ -1362,7 +1369,8 @@ int vit_patch_embed(const void* images, int64_t N, int64_t C, int64_t Hi, int64_
                 float* lo = reinterpret_cast<float*>(base + sa + se);
                 float* wt = reinterpret_cast<float*>(base + sa + se + slo);
                 float* wt_lo = reinterpret_cast<float*>(base + sa + se + slo + swt);
-                cudaError_t r = launch_split_wt(static_cast<const float*>(w), K, D, D, 0, wt, wt_lo, s);
+                const SplitWtJob job{static_cast<const float*>(w), K, D, D, 0, wt, wt_lo};
+                cudaError_t r = launch_split_wt(&job, 1, s);
                 if (r == cudaSuccess) r = launch_split_lo(static_cast<const float*>(A), M, K, K, lo, s);
                 if (r != cudaSuccess) return r;
                 Tf32GemmDesc g{static_cast<const float*>(A), K, lo, wt, wt_lo, M, D, K, TC_EPI_STORE,
