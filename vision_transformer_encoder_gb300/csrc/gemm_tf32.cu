@@ -41,6 +41,7 @@ struct XParams {
     int64_t ldr;
     float* out;
     int64_t ldo;
+    bool lo;                 // also store the low part of each output (out_lo)
     uint32_t* err;
 };
 
@@ -68,12 +69,17 @@ __device__ __forceinline__ float tf32_hi(float v) { return __uint_as_float(__flo
 //                     CTAs; the leader's lane 0 issues the pair MMAs and multicasts its
 //                     commits (ring slot free, accumulator ready) to both CTAs
 //   warps 5-12        epilogue, two warps per TMEM lane quarter (128 columns each): bias,
-//                     fp32 tanh GELU or residual, fp32 rows stored from registers
+//                     fp32 tanh GELU or residual; each 32 x 32 fp32 chunk goes through a
+//                     128B-swizzled staging tile to a TMA store (and, when asked, its low
+//                     parts through the same tile to a second TMA store)
 constexpr int XP_THREADS = 416;
 constexpr int XP_EPI_WARPS = 8;
 constexpr int XP_ACC_COLS = 256;
 constexpr int XP_TMEM_COLS = 2 * XP_ACC_COLS;
-constexpr int XP_SMEM = XSTAGES * X_STAGE + X_BAR_BYTES + 1024;
+constexpr int XP_STG = 32 * 128;                       // one 32 x 32 fp32 staging tile
+constexpr int XP_OFF_STG = XSTAGES * X_STAGE + 1024;   // after the ring and the barriers, 1 KB aligned
+constexpr int XP_SMEM = XP_OFF_STG + XP_EPI_WARPS * XP_STG + 1024;
+static_assert(X_BAR_BYTES <= 1024, "barriers fit before the staging tiles");
 
 __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                               uint32_t accumulate) {
@@ -88,6 +94,7 @@ __device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(XP_THREADS, 1)
 gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmAlo,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmBlo,
+                        const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmOutLo,
                         const XParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -126,6 +133,8 @@ gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         ptx::prefetch_tensormap(&tmAlo);
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmBlo);
+        ptx::prefetch_tensormap(&tmOut);
+        if (p.lo) ptx::prefetch_tensormap(&tmOutLo);
     }
     if (warp == 1) {
         ptx::tmem_alloc_pair(tmem_slot, XP_TMEM_COLS);
@@ -227,6 +236,8 @@ gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
         const int quarter = warp & 3;               // TMEM lane quarter this warp may read
         const int half = (warp - 5) >> 2;           // which 128 of the 256 columns
         const uint32_t tempty0 = ptx::mapa_shared(ptx::smem_addr(tempty), 0);   // leader's
+        uint8_t* stage = smem + XP_OFF_STG + (warp - 5) * XP_STG;
+        uint8_t* srow = stage + lane * 128;   // 16-byte unit u of this lane's row at u ^ (lane % 8)
         int local = 0;
         for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
             const int acc = local & 1;
@@ -238,7 +249,8 @@ gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 break;
             }
             ptx::tc_fence_after();
-            const int row = (tile / n_tiles) * 2 * XM + (int)rank * XM + quarter * 32 + lane;
+            const int row0 = (tile / n_tiles) * 2 * XM + (int)rank * XM + quarter * 32;
+            const int row = row0 + lane;
             const int n0 = (tile % n_tiles) * XP_ACC_COLS + half * 128;
             const uint32_t t_row =
                 tmem_base + acc * XP_ACC_COLS + half * 128 + ((uint32_t)(quarter * 32) << 16);
@@ -248,26 +260,53 @@ gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
                 ptx::tmem_ld_32x32b_x32(t_row + c * 32, r);
                 ptx::tmem_ld_wait();
                 const int col0 = n0 + c * 32;
-                if (row < p.M && col0 < p.N) {
-                    float* orow = p.out + (int64_t)row * p.ldo;
-                    const float* rrow = p.epi == TC_EPI_RESID ? p.residual + (int64_t)row * p.ldr : nullptr;
+                if (row0 >= p.M || col0 >= p.N) continue;   // the whole chunk lies outside out
+                const float* rrow = p.epi == TC_EPI_RESID && row < p.M ? p.residual + (int64_t)row * p.ldr : nullptr;
+                float4 vv[8];
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const int col = col0 + 4 * j4;
-                        if (col >= p.N) break;   // N is a multiple of 4
-                        float vv[4];
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const int col = col0 + 4 * j4;
+                    float x[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) x[e] = __uint_as_float(r[4 * j4 + e]);
+                    if (col < p.N) {   // N is a multiple of 4
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            float x = __uint_as_float(r[4 * j4 + e]);
-                            if (p.bias) x += p.bias[col + e];
-                            if (p.epi == TC_EPI_GELU) x = gelu_tanh_acc(x);
-                            vv[e] = x;
+                            if (p.bias) x[e] += p.bias[col + e];
+                            if (p.epi == TC_EPI_GELU) x[e] = gelu_tanh_acc(x[e]);
                         }
                         if (rrow) {
                             const float4 rv = *reinterpret_cast<const float4*>(rrow + col);
-                            vv[0] += rv.x; vv[1] += rv.y; vv[2] += rv.z; vv[3] += rv.w;
+                            x[0] += rv.x; x[1] += rv.y; x[2] += rv.z; x[3] += rv.w;
                         }
-                        *reinterpret_cast<float4*>(orow + col) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+                    }
+                    vv[j4] = make_float4(x[0], x[1], x[2], x[3]);
+                }
+                // the previous store from the staging tile has read it; rows past M and
+                // columns past N fall outside the tensor and are not written
+                if (lane == 0) ptx::bulk_wait_group_read<0>();
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) *reinterpret_cast<float4*>(srow + ((u ^ (lane & 7)) << 4)) = vv[u];
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&tmOut, stage, col0, row0);
+                    ptx::bulk_commit_group();
+                }
+                if (p.lo) {
+                    if (lane == 0) ptx::bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<float4*>(srow + ((u ^ (lane & 7)) << 4)) =
+                            make_float4(tf32_low_part(vv[u].x), tf32_low_part(vv[u].y), tf32_low_part(vv[u].z),
+                                        tf32_low_part(vv[u].w));
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmOutLo, stage, col0, row0);
+                        ptx::bulk_commit_group();
                     }
                 }
             }
@@ -275,6 +314,7 @@ gemm_tf32x3_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_co
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive_cluster_relaxed(tempty0 + acc * 8);   // orders TMEM reads only
         }
+        if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
     }
 
     __syncthreads();
@@ -350,13 +390,14 @@ EncodeTiledFn x_encode_fn() {
     return fn;
 }
 
-// fp32 rows x cols (ld elements), box 32 x 128, 128-byte swizzle, zero fill past the edges.
-bool make_map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+// fp32 rows x cols (ld elements), box 32 columns x box_rows, 128-byte swizzle, zero fill past
+// the edges (loads) or clipped there (stores).
+bool make_map_f32(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows = 128) {
     EncodeTiledFn fn = x_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(ld * 4)};
-    cuuint32_t box[2] = {(cuuint32_t)XK, 128u};
+    cuuint32_t box[2] = {(cuuint32_t)XK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -401,12 +442,14 @@ cudaError_t launch_split_wt(const SplitWtJob* jobs, int njobs, cudaStream_t s) {
 cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cudaStream_t s) {
     if (d.M <= 0 || d.N <= 0) return cudaSuccess;
     if (!tf32x3_supported(d.M, d.N, d.K, d.lda, d.a) || !aligned16(d.a_lo) || !aligned16(d.wt) ||
-        !aligned16(d.wt_lo) || !aligned16(d.out) || d.ldo % 4 != 0 ||
+        !aligned16(d.wt_lo) || !aligned16(d.out) || d.ldo % 4 != 0 || (d.out_lo && !aligned16(d.out_lo)) ||
         (d.epi == TC_EPI_RESID && (!aligned16(d.residual) || d.ldr % 4 != 0)))
         return cudaErrorInvalidValue;
-    alignas(64) CUtensorMap ma, malo, mb, mblo;
+    alignas(64) CUtensorMap ma, malo, mb, mblo, mo, molo;
     if (!make_map_f32(&ma, d.a, d.M, d.K, d.lda) || !make_map_f32(&malo, d.a_lo, d.M, d.K, d.K) ||
-        !make_map_f32(&mb, d.wt, d.N, d.K, d.K) || !make_map_f32(&mblo, d.wt_lo, d.N, d.K, d.K))
+        !make_map_f32(&mb, d.wt, d.N, d.K, d.K) || !make_map_f32(&mblo, d.wt_lo, d.N, d.K, d.K) ||
+        !make_map_f32(&mo, d.out, d.M, d.N, d.ldo, 32) ||
+        !make_map_f32(&molo, d.out_lo ? d.out_lo : d.out, d.M, d.N, d.ldo, 32))
         return cudaErrorInvalidValue;
     XParams p;
     p.M = (int)d.M;
@@ -418,6 +461,7 @@ cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cud
     p.ldr = d.ldr;
     p.out = d.out;
     p.ldo = d.ldo;
+    p.lo = d.out_lo != nullptr;
     p.err = dev.err_word;
     static bool attr = false;
     if (!attr) {
@@ -429,7 +473,7 @@ cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cud
     const int64_t tiles = ((d.M + 2 * XM - 1) / (2 * XM)) * ((d.N + XP_ACC_COLS - 1) / XP_ACC_COLS);
     const int64_t pairs = dev.num_sms / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
-    return launch_dependent(gemm_tf32x3_pair_kernel, dim3(grid), dim3(XP_THREADS), XP_SMEM, s, ma, malo, mb, mblo, p);
+    return launch_dependent(gemm_tf32x3_pair_kernel, dim3(grid), dim3(XP_THREADS), XP_SMEM, s, ma, malo, mb, mblo, mo, molo, p);
 }
 
 }  // namespace vit

@@ -151,6 +151,7 @@ struct Tf32GemmDesc {
     int64_t ldr;
     float* out;
     int64_t ldo;
+    float* out_lo;   // optional: the low part of each output (tf32_low_part), stride ldo
 };
 bool tf32x3_supported(int64_t M, int64_t N, int64_t K, int64_t lda, const void* a);
 cudaError_t launch_split_lo(const float* a, int64_t rows, int64_t cols, int64_t lda, float* lo, cudaStream_t s);

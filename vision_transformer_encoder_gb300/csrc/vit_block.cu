@@ -275,7 +275,8 @@ Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     w.tf32 = !w.fast && a.dt == DT_F32 && tf32x3_supported(M, 3 * D, D, D, a.x) && F % 4 == 0 &&
              tf32_requested();
     if (w.tf32) {
-        w.sz_lo = round_up((size_t)(M * (F > D ? F : D)) * 4, 256);
+        // low parts of the products' A operands: xn, o, yn (M x D, one after another), h (M x F)
+        w.sz_lo = round_up((size_t)(M * D) * 4, 256) + round_up((size_t)(M * F) * 4, 256);
         w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
     }
     if (w.fused) {
@@ -484,11 +485,12 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
     } else if (w.tf32) {
         // fp32: LayerNorm on the CUDA cores, attention and the products as 3xTF32. Each
-        // product's A_lo (the low part of its A operand) is written by the LayerNorm that
-        // makes A, or by a split pass after attention and after W1 (whose row-per-thread
-        // stores measured slower writing a second output than the pass costs).
-        uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // A_lo, then the split weights
-        float* lo = reinterpret_cast<float*>(tail);
+        // product's A_lo (the low part of its A operand) is written by the kernel that makes
+        // A (the LayerNorms, the W1 product), or by a split pass after attention (whose
+        // row-per-thread stores measured slower writing a second output than the pass costs).
+        uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // the A_lo parts, then the split weights
+        float* lo = reinterpret_cast<float*>(tail);                                         // M x D
+        float* lo_h = reinterpret_cast<float*>(tail + round_up((size_t)(M * D) * 4, 256));   // M x F
         float* wt = reinterpret_cast<float*>(tail + w.sz_lo);
         float* wqkv_t = wt, *wqkv_lo = wqkv_t + 3 * D * D;
         float* wo_t = wqkv_lo + 3 * D * D, *wo_lo = wo_t + D * D;
@@ -510,9 +512,9 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
                 {static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo}};
             return launch_split_wt(jobs, 6, s);
         }));
-        auto gemm = [&](const float* A, int64_t K, const float* bt, const float* btlo, int64_t N, int epi,
-                        const void* bias, const float* res, float* out) {
-            Tf32GemmDesc g{A, K, lo, bt, btlo, M, N, K, epi, static_cast<const float*>(bias), res, N, out, N};
+        auto gemm = [&](const float* A, const float* A_lo, int64_t K, const float* bt, const float* btlo, int64_t N,
+                        int epi, const void* bias, const float* res, float* out, float* out_lo) {
+            Tf32GemmDesc g{A, K, A_lo, bt, btlo, M, N, K, epi, static_cast<const float*>(bias), res, N, out, N, out_lo};
             return launch_gemm_tf32x3(g, dev, s);
         };
         step(run(K_LN1, s, [&] {
@@ -520,7 +522,9 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
         if (has_qkv_bias(a)) step(concat_qkv_bias(a, s));
         const void* bqkv = has_qkv_bias(a) ? a.bias_scratch : nullptr;
-        step(run(K_QKV, s, [&] { return gemm(fbuf, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, bqkv, nullptr, fqkv); }));
+        step(run(K_QKV, s, [&] {
+            return gemm(fbuf, lo, D, wqkv_t, wqkv_lo, 3 * D, TC_EPI_STORE, bqkv, nullptr, fqkv, nullptr);
+        }));
         step(run(K_ATTN, s, [&] {
             if (attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
                 return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s);
@@ -528,15 +532,14 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
         step(run(K_WO, s, [&] {
             cudaError_t r = launch_split_lo(fbuf, M, D, D, lo, s);
-            return r == cudaSuccess ? gemm(fbuf, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy) : r;
+            return r == cudaSuccess ? gemm(fbuf, lo, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy, nullptr) : r;
         }));
         step(run(K_LN2, s, [&] {
             return launch_layernorm_f32_lo(fy, fbuf, lo, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
         }));
-        step(run(K_W1, s, [&] { return gemm(fbuf, D, w1_t, w1_lo, F, TC_EPI_GELU, a.b1, nullptr, fh); }));
+        step(run(K_W1, s, [&] { return gemm(fbuf, lo, D, w1_t, w1_lo, F, TC_EPI_GELU, a.b1, nullptr, fh, lo_h); }));
         step(run(K_W2, s, [&] {
-            cudaError_t r = launch_split_lo(fh, M, F, F, lo, s);
-            return r == cudaSuccess ? gemm(fh, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, fy, static_cast<float*>(a.out)) : r;
+            return gemm(fh, lo_h, F, w2_t, w2_lo, D, TC_EPI_RESID, a.b2, fy, static_cast<float*>(a.out), nullptr);
         }));
     } else {
         const int dt = a.dt;
