@@ -126,19 +126,21 @@ bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const v
 }
 
 cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                 const DeviceInfo& dev, cudaStream_t s) {
+                                 const DeviceInfo& dev, cudaStream_t s, float* o_lo) {
     if (N <= 0 || T <= 0) return cudaSuccess;
-    // head width 64 and at most 224 tokens: the 3xTF32 tensor-core kernel
-    if (attention_tf32_supported(N, T, D, H, qkv, o)) return launch_attention_tf32(qkv, o, N, T, D, H, dev, s);
+    // head width 64 and at most 224 tokens: the 3xTF32 tensor-core kernel (writes o_lo itself)
+    if (attention_tf32_supported(N, T, D, H, qkv, o)) return launch_attention_tf32(qkv, o, N, T, D, H, dev, s, o_lo);
+    cudaError_t e = cudaErrorInvalidValue;
     switch (D / H) {
-        case 32: return launch_dh<32, 1>(qkv, o, N, T, D, s);
-        case 48: return launch_dh<48, 1>(qkv, o, N, T, D, s);
-        case 64: return launch_dh<64, 1>(qkv, o, N, T, D, s);
-        case 80: return launch_dh<80, 2>(qkv, o, N, T, D, s);
-        case 96: return launch_dh<96, 2>(qkv, o, N, T, D, s);
-        case 128: return launch_dh<128, 2>(qkv, o, N, T, D, s);
+        case 32: e = launch_dh<32, 1>(qkv, o, N, T, D, s); break;
+        case 48: e = launch_dh<48, 1>(qkv, o, N, T, D, s); break;
+        case 64: e = launch_dh<64, 1>(qkv, o, N, T, D, s); break;
+        case 80: e = launch_dh<80, 2>(qkv, o, N, T, D, s); break;
+        case 96: e = launch_dh<96, 2>(qkv, o, N, T, D, s); break;
+        case 128: e = launch_dh<128, 2>(qkv, o, N, T, D, s); break;
     }
-    return cudaErrorInvalidValue;
+    if (e == cudaSuccess && o_lo) e = launch_split_lo(static_cast<const float*>(o), N * T, D, D, o_lo, s);
+    return e;
 }
 
 }  // namespace vit

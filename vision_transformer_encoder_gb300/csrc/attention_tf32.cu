@@ -61,7 +61,9 @@ constexpr int A3_OFF_VTL = A3_OFF_K + 7 * A3_VTBLK;
 constexpr int A3_OFF_MX = A3_OFF_K + 4 * A3_KBOX;       // row maxima [half][row]
 constexpr int A3_OFF_L = A3_OFF_MX + 2 * A3_ROWS * 4;   // row sums [half][row]
 constexpr int A3_OFF_BAR = A3_OFF_L + 2 * A3_ROWS * 4;
-constexpr int A3_SMEM = A3_OFF_BAR + 128 + 1024;        // + alignment slack
+constexpr int A3_STG = 32 * 128;                        // one 32 x 32 fp32 staging tile (128B swizzle)
+constexpr int A3_OFF_STG = (A3_OFF_BAR + 128 + 1023) / 1024 * 1024;   // [epilogue warp][2 tiles]
+constexpr int A3_SMEM = A3_OFF_STG + 4 * 2 * A3_STG + 1024;          // + alignment slack
 constexpr uint32_t A3_TMEM_PL = 224, A3_TMEM_O = 448;
 static_assert(2 * A3_KBOX <= A3_OFF_K, "raw V fits where Q and Q_lo were");
 static_assert(2 * 7 * A3_VTBLK <= 4 * A3_KBOX, "V^T and V^T_lo fit where K and K_lo were");
@@ -74,6 +76,7 @@ struct A3Params {
     int units;       // N * H * nq
     float sl2;       // log2(e) / sqrt(64)
     float* o;
+    bool lo;         // also write the low part of o (tmOlo)
     uint32_t* err;
 };
 
@@ -126,6 +129,7 @@ __device__ __forceinline__ void a3_unit(const A3Params& p, int u, int& n, int& h
 
 __global__ void __launch_bounds__(A3_THREADS, 1)
 attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmOlo,
                       const A3Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -382,13 +386,54 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
                 ptx::tmem_ld_32x32b_x32(to, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
                 ptx::tmem_ld_32x32b_x32(to + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
                 ptx::tmem_ld_wait();
-                if (t < p.T) {
-                    const float inv = 1.f / (sL[row] + sL[A3_ROWS + row]);
-                    float4* orow = reinterpret_cast<float4*>(p.o + ((int64_t)n * p.T + t) * p.D + h * A3_DH);
+                // O / l through two 32 x 32 staging tiles (128-byte rows, 16-byte unit u of
+                // row r at u ^ (r % 8)) to TMA stores over (column, token, sequence): rows
+                // past T lie outside the tensor and are not written. With p.lo the same tiles
+                // then carry the low parts to a second pair of stores.
+                const float inv = t < p.T ? 1.f / (sL[row] + sL[A3_ROWS + row]) : 0.f;
+                uint8_t* stg = smem + A3_OFF_STG + (warp - A3_HELP_WARP) * 2 * A3_STG;
+                const int col0 = h * A3_DH, t0 = qt * A3_ROWS + quarter * 32;
+                if (lane == 0) ptx::bulk_wait_group_read<0>();   // the previous unit's stores have read the tiles
+                __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        orow[c] = make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
-                                              __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+                for (int b = 0; b < 2; ++b) {
+                    uint8_t* srow = stg + b * A3_STG + lane * 128;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int c = 8 * b + u;
+                        *reinterpret_cast<float4*>(srow + ((u ^ (lane & 7)) << 4)) =
+                            make_float4(__uint_as_float(ov[4 * c]) * inv, __uint_as_float(ov[4 * c + 1]) * inv,
+                                        __uint_as_float(ov[4 * c + 2]) * inv, __uint_as_float(ov[4 * c + 3]) * inv);
+                    }
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&tmO, stg, col0, t0, n);
+                    ptx::tma_store_3d(&tmO, stg + A3_STG, col0 + 32, t0, n);
+                    ptx::bulk_commit_group();
+                }
+                if (p.lo) {
+                    if (lane == 0) ptx::bulk_wait_group_read<0>();
+                    __syncwarp();
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        uint8_t* srow = stg + b * A3_STG + lane * 128;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const int c = 8 * b + u;
+                            *reinterpret_cast<float4*>(srow + ((u ^ (lane & 7)) << 4)) = make_float4(
+                                tf32_lo(__uint_as_float(ov[4 * c]) * inv), tf32_lo(__uint_as_float(ov[4 * c + 1]) * inv),
+                                tf32_lo(__uint_as_float(ov[4 * c + 2]) * inv), tf32_lo(__uint_as_float(ov[4 * c + 3]) * inv));
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_3d(&tmOlo, stg, col0, t0, n);
+                        ptx::tma_store_3d(&tmOlo, stg + A3_STG, col0 + 32, t0, n);
+                        ptx::bulk_commit_group();
+                    }
                 }
             }
         }
@@ -397,7 +442,9 @@ attention_tf32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_cons
         if (*abort_flag) break;   // the same value for every thread after the barrier
     }
 
-    // teardown: every MMA issued has finished and every copy issued has landed
+    // teardown: every MMA issued has finished, every copy issued has landed and every
+    // store issued has completed
+    if (warp >= A3_HELP_WARP && warp < A3_HELP_WARP + 4 && lane == 0) ptx::bulk_wait_group<0>();
     if (issuer) {
         ptx::mma_commit(&bars->fin);
         if (!ptx::mbar_wait_bounded(&bars->fin, 0, nullptr)) a3_error(p.err, ERRBIT_TIMEOUT_TEARDOWN);
@@ -449,9 +496,10 @@ bool attention_tf32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const 
 }
 
 cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                  const DeviceInfo& dev, cudaStream_t s) {
+                                  const DeviceInfo& dev, cudaStream_t s, float* o_lo) {
     if (N <= 0 || T <= 0) return cudaSuccess;
     if (!attention_tf32_supported(N, T, D, H, qkv, o)) return cudaErrorInvalidValue;
+    if (o_lo && (reinterpret_cast<uintptr_t>(o_lo) & 15)) return cudaErrorInvalidValue;
     EncodeTiledFn fn = a3_encode_fn();
     const int ns = (int)((T + 15) / 16 * 16);
     alignas(64) CUtensorMap tq, tkv;
@@ -466,6 +514,18 @@ cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // o and o_lo over (column, token, sequence), box 32 x 32 x 1 (128-byte rows), for stores
+    alignas(64) CUtensorMap to, tol;
+    cuuint64_t odims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)N};
+    cuuint64_t ostr[2] = {(cuuint64_t)(D * 4), (cuuint64_t)(T * D * 4)};
+    cuuint32_t obox[3] = {32, 32, 1};
+    if (fn(&to, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS ||
+        fn(&tol, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, o_lo ? static_cast<void*>(o_lo) : o, odims, ostr, obox, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     A3Params p;
     p.T = (int)T;
     p.D = (int)D;
@@ -475,6 +535,7 @@ cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T
     p.units = (int)(N * H * p.nq);
     p.sl2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
     p.o = static_cast<float*>(o);
+    p.lo = o_lo != nullptr;
     p.err = dev.err_word;
     static bool attr = false;
     if (!attr) {
@@ -484,7 +545,7 @@ cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T
         attr = true;
     }
     const int grid = p.units < dev.num_sms ? p.units : dev.num_sms;
-    return launch_dependent(attention_tf32_kernel, dim3(grid), dim3(A3_THREADS), A3_SMEM, s, tq, tkv, p);
+    return launch_dependent(attention_tf32_kernel, dim3(grid), dim3(A3_THREADS), A3_SMEM, s, tq, tkv, to, tol, p);
 }
 
 }  // namespace vit

@@ -177,15 +177,16 @@ cudaError_t launch_patchify(const void* images, int dt, int64_t N, int64_t C, in
 cudaError_t launch_patch_assemble(const void* E, int e_dt, const void* cls, const void* pos, int dt, int64_t N,
                                   int64_t NP, int64_t D, void* out, cudaStream_t s);
 
-// fp32 qkv -> fp32 o on the CUDA cores (head widths 32, 48, 64, 80, 96, 128).
+// fp32 qkv -> fp32 o on the CUDA cores (head widths 32, 48, 64, 80, 96, 128). With o_lo,
+// the low part of o (tf32_low_part, contiguous (N T) x D) is written too.
 bool attention_f32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o);
 cudaError_t launch_attention_f32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                 const DeviceInfo& dev, cudaStream_t s);
+                                 const DeviceInfo& dev, cudaStream_t s, float* o_lo = nullptr);
 // fp32 qkv -> fp32 o on the tensor cores, three TF32 products per step (attention_tf32.cu):
 // head width 64, T <= 224. VIT_ATTN_F32_TC=0 turns it off.
 bool attention_tf32_supported(int64_t N, int64_t T, int64_t D, int64_t H, const void* qkv, const void* o);
 cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,
-                                  const DeviceInfo& dev, cudaStream_t s);
+                                  const DeviceInfo& dev, cudaStream_t s, float* o_lo = nullptr);
 // Head width 64 and T <= 224: all keys of a row in one S tile, exact one-pass softmax.
 bool attention_whole_supported(int64_t T, int64_t D, int64_t H);
 cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, int64_t H,

@@ -486,8 +486,8 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
     } else if (w.tf32) {
         // fp32: LayerNorm on the CUDA cores, attention and the products as 3xTF32. Each
         // product's A_lo (the low part of its A operand) is written by the kernel that makes
-        // A (the LayerNorms, the W1 product), or by a split pass after attention (whose
-        // row-per-thread stores measured slower writing a second output than the pass costs).
+        // A: the LayerNorms, the attention and the W1 product (a split pass after the
+        // CUDA-core attention that other shapes take).
         uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // the A_lo parts, then the split weights
         float* lo = reinterpret_cast<float*>(tail);                                         // M x D
         float* lo_h = reinterpret_cast<float*>(tail + round_up((size_t)(M * D) * 4, 256));   // M x F
@@ -527,13 +527,11 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         }));
         step(run(K_ATTN, s, [&] {
             if (attention_f32_supported(a.N, a.T, D, a.H, qkv, buf))
-                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s);
-            return launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
+                return launch_attention_f32(qkv, buf, a.N, a.T, D, a.H, dev, s, lo);
+            cudaError_t r = launch_attention_simt(qkv, DT_F32, buf, a.N, a.T, D, a.H, s);
+            return r == cudaSuccess ? launch_split_lo(fbuf, M, D, D, lo, s) : r;
         }));
-        step(run(K_WO, s, [&] {
-            cudaError_t r = launch_split_lo(fbuf, M, D, D, lo, s);
-            return r == cudaSuccess ? gemm(fbuf, lo, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy, nullptr) : r;
-        }));
+        step(run(K_WO, s, [&] { return gemm(fbuf, lo, D, wo_t, wo_lo, D, TC_EPI_RESID, a.b_o, fx, fy, nullptr); }));
         step(run(K_LN2, s, [&] {
             return launch_layernorm_f32_lo(fy, fbuf, lo, a.ln2_g, a.ln2_b, DT_F32, M, D, a.eps, s);
         }));
