@@ -28,7 +28,8 @@
 //                    rescales. With typical scores no chunk passes the start by 8 and the
 //                    row costs one read of S, each P rounded once.
 //   warps 16-19      epilogue, one per TMEM lane quarter: O into registers, O's slot
-//                    released at once, then O / (l0 + l1) in bf16 to global memory.
+//                    released at once, then O / (l0 + l1) in bf16 through a swizzled
+//                    staging tile to one TMA store per warp and unit.
 //   warps 20, 21     MMA issuers, one per group (warp 20 also owns TMEM): group g's
 //                    stream is S(g), PV(g), S(g + 2), PV(g + 2), ...: S of a unit runs
 //                    while the other group's softmax works, and PV(u) follows as soon as
@@ -70,7 +71,10 @@ constexpr int AW_OFF_V = AW_OFF_K + 4 * AW_BOX;    // [buffer][128-key box]
 constexpr int AW_OFF_L = AW_OFF_V + 4 * AW_BOX;    // row sums [unit % 4][half][row]
 constexpr int AW_OFF_MX = AW_OFF_L + 4 * 2 * AW_ROWS * 4;   // row maxima [group][half][row]
 constexpr int AW_OFF_BAR = AW_OFF_MX + 2 * 2 * AW_ROWS * 4;
-constexpr int AW_SMEM = AW_OFF_BAR + 256 + 1024;   // + alignment slack
+constexpr int AW_STG = 32 * 128;                   // one 32-row x 64-column bf16 staging tile
+constexpr int AW_OFF_STG = (AW_OFF_BAR + 256 + 1023) / 1024 * 1024;   // [epilogue warp]
+constexpr int AW_SMEM = AW_OFF_STG + 4 * AW_STG + 1024;               // + alignment slack
+static_assert(AW_SMEM <= 227 * 1024, "shared memory");
 constexpr uint32_t AW_TMEM_O = 448;
 
 struct AwParams {
@@ -212,7 +216,8 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&v)[W], float cm, float 
 }
 
 __global__ void __launch_bounds__(AW_THREADS, 1)
-attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p) {
+attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmO,
+                       const AwParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -508,7 +513,6 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
         // ------------------------------------------------------------------ epilogue
         const int quarter = warp & 3;
         const uint32_t tO = tmem + AW_TMEM_O + ((uint32_t)(quarter * 32) << 16);
-        const int D = p.D;
         bool ok = true;
         for (int u = 0; u < units; ++u) {
             const int k = u / nq, qt = u - k * nq;
@@ -532,9 +536,14 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&bars->o_free[u & 1]);
-            const int t = qt * AW_ROWS + row;
-            if (live && t < p.T) {
-                __nv_bfloat16* orow = p.o + ((int64_t)n * p.T + t) * D + h * AW_DH;
+            if (live) {
+                // O / l in bf16 through a 32 x 64 staging tile (128-byte rows, 16-byte unit c
+                // of row r at c ^ (r % 8)) to one TMA store over (column, token, sequence):
+                // rows past T lie outside the tensor and are not written
+                uint8_t* stg = smem + AW_OFF_STG + quarter * AW_STG;
+                uint8_t* srow = stg + lane * 128;
+                if (lane == 0) ptx::bulk_wait_group_read<0>();   // the previous store has read the tile
+                __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint4 w;
@@ -542,10 +551,17 @@ attention_whole_kernel(const __grid_constant__ CUtensorMap tm, const AwParams p)
                     w.y = pack_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
                     w.z = pack_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
                     w.w = pack_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
-                    *reinterpret_cast<uint4*>(orow + c * 8) = w;
+                    *reinterpret_cast<uint4*>(srow + ((c ^ (lane & 7)) << 4)) = w;
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_3d(&tmO, stg, h * AW_DH, qt * AW_ROWS + quarter * 32, n);
+                    ptx::bulk_commit_group();
                 }
             }
         }
+        if (lane == 0) ptx::bulk_wait_group<0>();   // stores complete before the CTA exits
         if (!ok) {
             if (lane == 0) aw_error(p.err, ERRBIT_TIMEOUT_ATTENTION);
             *abort_flag = 1;
@@ -604,6 +620,15 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // o over (column, token, sequence), box 64 x 32 x 1 (128-byte rows), for the stores
+    alignas(64) CUtensorMap to;
+    cuuint64_t odims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)N};
+    cuuint64_t ostr[2] = {(cuuint64_t)(D * 2), (cuuint64_t)(T * D * 2)};
+    cuuint32_t obox[3] = {AW_DH, 32, 1};
+    if (fn(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, odims, ostr, obox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     AwParams p;
     p.T = (int)T;
     p.D = (int)D;
@@ -631,7 +656,7 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
         attr = true;
     }
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
-    return launch_dependent(attention_whole_kernel, dim3(grid), dim3(AW_THREADS), AW_SMEM, s, tm, p);
+    return launch_dependent(attention_whole_kernel, dim3(grid), dim3(AW_THREADS), AW_SMEM, s, tm, to, p);
 }
 
 }  // namespace vit
