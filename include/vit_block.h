@@ -228,7 +228,10 @@ int vit_encoder(const void* x, const vit_layer* layers, int64_t L, const void* l
  *              synchronises it before returning: the caller may then free or change
  *              its arrays
  * Memory: 2 (4 D^2 + 2 D F) bytes of bf16 weights (4 for fp32) plus the gains and biases;
- * with the fold another 8 (3 D + F) bytes and, with LN gains, 2 (3 D^2 + D F) bytes.
+ * with the fold another 8 (3 D + F) bytes and, with LN gains, 2 (3 D^2 + D F) bytes. An
+ * fp32 handle (D and F multiples of 4) also holds the weights transposed with their low
+ * parts for the 3xTF32 tensor-core products, 8 (4 D^2 + 2 D F) bytes, made once here
+ * instead of in every call.
  * Errors: VIT_ERR_ARG (null layer/out/weight, bad sizes, from_host or fold out of range),
  * VIT_ERR_DTYPE, VIT_ERR_NOMEM, VIT_ERR_CUDA, VIT_ERR_UNSUPPORTED.
  */

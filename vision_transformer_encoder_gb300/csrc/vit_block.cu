@@ -178,6 +178,9 @@ struct BlockArgs {
     // and b1 are then inside colbias1 and colbias2).
     bool qkv_bias_ready = false;
     const FoldTerms* fold_terms = nullptr;
+    // Prepared fp32 weights: transposed with their low parts once (tf32_weight_layout), so
+    // the fp32 tensor-core path skips its per-call split.
+    const float* tf32_wt = nullptr;
 };
 
 inline int x_dtype(const BlockArgs& a) { return a.x_dt < 0 ? a.dt : a.x_dt; }
@@ -258,6 +261,37 @@ bool tf32_requested() {
     return on;
 }
 
+// The fp32 tensor-core path's weights, each transposed (out rows, K contiguous) and
+// followed by its low part: [w_q | w_k | w_v]^T, w_o^T, w_mlp1^T, w_mlp2^T.
+struct Tf32Weights {
+    float *wqkv_t, *wqkv_lo, *wo_t, *wo_lo, *w1_t, *w1_lo, *w2_t, *w2_lo;
+};
+size_t tf32_weight_bytes(int64_t D, int64_t F) { return round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256); }
+Tf32Weights tf32_weight_layout(float* base, int64_t D, int64_t F) {
+    Tf32Weights t;
+    t.wqkv_t = base;
+    t.wqkv_lo = t.wqkv_t + 3 * D * D;
+    t.wo_t = t.wqkv_lo + 3 * D * D;
+    t.wo_lo = t.wo_t + D * D;
+    t.w1_t = t.wo_lo + D * D;
+    t.w1_lo = t.w1_t + F * D;
+    t.w2_t = t.w1_lo + F * D;
+    t.w2_lo = t.w2_t + D * F;
+    return t;
+}
+// The six transposes and splits, in one launch.
+cudaError_t tf32_split_weights(const BlockArgs& a, const Tf32Weights& t, cudaStream_t s) {
+    const int64_t D = a.D, F = a.F;
+    const SplitWtJob jobs[6] = {
+        {static_cast<const float*>(a.w_q), D, D, D, 0, t.wqkv_t, t.wqkv_lo},
+        {static_cast<const float*>(a.w_k), D, D, D, D, t.wqkv_t, t.wqkv_lo},
+        {static_cast<const float*>(a.w_v), D, D, D, 2 * D, t.wqkv_t, t.wqkv_lo},
+        {static_cast<const float*>(a.w_o), D, D, D, 0, t.wo_t, t.wo_lo},
+        {static_cast<const float*>(a.w1), D, F, F, 0, t.w1_t, t.w1_lo},
+        {static_cast<const float*>(a.w2), F, D, D, 0, t.w2_t, t.w2_lo}};
+    return launch_split_wt(jobs, 6, s);
+}
+
 Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     Workspace w;
     const int64_t M = a.N * a.T, D = a.D, F = a.F;
@@ -277,7 +311,7 @@ Workspace workspace_layout(const BlockArgs& a, bool fused_ok) {
     if (w.tf32) {
         // low parts of the products' A operands: xn, o, yn (M x D, one after another), h (M x F)
         w.sz_lo = round_up((size_t)(M * D) * 4, 256) + round_up((size_t)(M * F) * 4, 256);
-        w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
+        w.sz_wt = a.tf32_wt ? 0 : tf32_weight_bytes(D, F);
     }
     if (w.fused) {
         w.sz_yb = round_up((size_t)(M * D) * 2, 256);
@@ -491,27 +525,16 @@ cudaError_t launch_block_steps(const BlockArgs& a, const DeviceInfo& dev, cudaSt
         uint8_t* tail = static_cast<uint8_t*>(h) + w.sz_h;   // the A_lo parts, then the split weights
         float* lo = reinterpret_cast<float*>(tail);                                         // M x D
         float* lo_h = reinterpret_cast<float*>(tail + round_up((size_t)(M * D) * 4, 256));   // M x F
-        float* wt = reinterpret_cast<float*>(tail + w.sz_lo);
-        float* wqkv_t = wt, *wqkv_lo = wqkv_t + 3 * D * D;
-        float* wo_t = wqkv_lo + 3 * D * D, *wo_lo = wo_t + D * D;
-        float* w1_t = wo_lo + D * D, *w1_lo = w1_t + F * D;
-        float* w2_t = w1_lo + F * D, *w2_lo = w2_t + D * F;
+        const Tf32Weights tw = tf32_weight_layout(
+            a.tf32_wt ? const_cast<float*>(a.tf32_wt) : reinterpret_cast<float*>(tail + w.sz_lo), D, F);
+        float *wqkv_t = tw.wqkv_t, *wqkv_lo = tw.wqkv_lo, *wo_t = tw.wo_t, *wo_lo = tw.wo_lo;
+        float *w1_t = tw.w1_t, *w1_lo = tw.w1_lo, *w2_t = tw.w2_t, *w2_lo = tw.w2_lo;
         const float* fx = static_cast<const float*>(a.x);
         float* fbuf = static_cast<float*>(buf);
         float* fqkv = static_cast<float*>(qkv);
         float* fy = static_cast<float*>(y);
         float* fh = static_cast<float*>(h);
-        step(run(K_TF32_SPLIT, s, [&] {
-            const void* wq[3] = {a.w_q, a.w_k, a.w_v};
-            const SplitWtJob jobs[6] = {
-                {static_cast<const float*>(wq[0]), D, D, D, 0, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(wq[1]), D, D, D, D, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(wq[2]), D, D, D, 2 * D, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo},
-                {static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo},
-                {static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo}};
-            return launch_split_wt(jobs, 6, s);
-        }));
+        if (!a.tf32_wt) step(run(K_TF32_SPLIT, s, [&] { return tf32_split_weights(a, tw, s); }));
         auto gemm = [&](const float* A, const float* A_lo, int64_t K, const float* bt, const float* btlo, int64_t N,
                         int epi, const void* bias, const float* res, float* out, float* out_lo) {
             Tf32GemmDesc g{A, K, A_lo, bt, btlo, M, N, K, epi, static_cast<const float*>(bias), res, N, out, N, out_lo};
@@ -626,7 +649,7 @@ ClsWorkspace cls_workspace_layout(const BlockArgs& a, const DeviceInfo& dev) {
     if (w.tf32) {
         const int64_t lo = M * D > N * F ? M * D : N * F;
         w.sz_lo = round_up((size_t)lo * 4, 256);
-        w.sz_wt = round_up((size_t)(2 * (4 * D * D + 2 * D * F)) * 4, 256);
+        w.sz_wt = tf32_weight_bytes(D, F);
     }
     w.sz_split = 0;
     if (w.fast) {
@@ -747,21 +770,10 @@ cudaError_t launch_block_cls_steps(const BlockArgs& a, const DeviceInfo& dev, cu
         }));
     } else if (w.tf32) {
         float* lo = reinterpret_cast<float*>(tail);
-        float* wqkv_t = reinterpret_cast<float*>(tail + w.sz_lo), *wqkv_lo = wqkv_t + 3 * D * D;
-        float* wo_t = wqkv_lo + 3 * D * D, *wo_lo = wo_t + D * D;
-        float* w1_t = wo_lo + D * D, *w1_lo = w1_t + F * D;
-        float* w2_t = w1_lo + F * D, *w2_lo = w2_t + D * F;
-        step(run(K_TF32_SPLIT, s, [&] {
-            const void* wq[3] = {a.w_q, a.w_k, a.w_v};
-            const SplitWtJob jobs[6] = {
-                {static_cast<const float*>(wq[0]), D, D, D, 0, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(wq[1]), D, D, D, D, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(wq[2]), D, D, D, 2 * D, wqkv_t, wqkv_lo},
-                {static_cast<const float*>(a.w_o), D, D, D, 0, wo_t, wo_lo},
-                {static_cast<const float*>(a.w1), D, F, F, 0, w1_t, w1_lo},
-                {static_cast<const float*>(a.w2), F, D, D, 0, w2_t, w2_lo}};
-            return launch_split_wt(jobs, 6, s);
-        }));
+        const Tf32Weights tw = tf32_weight_layout(reinterpret_cast<float*>(tail + w.sz_lo), D, F);
+        float *wqkv_t = tw.wqkv_t, *wqkv_lo = tw.wqkv_lo, *wo_t = tw.wo_t, *wo_lo = tw.wo_lo;
+        float *w1_t = tw.w1_t, *w1_lo = tw.w1_lo, *w2_t = tw.w2_t, *w2_lo = tw.w2_lo;
+        step(run(K_TF32_SPLIT, s, [&] { return tf32_split_weights(a, tw, s); }));
         // out (rows, N) = epi(A (rows, K; row stride lda) @ W + bias [+ res (row stride ldr)])
         auto gemm = [&](const void* A, int64_t rows, int64_t K, int64_t lda, const float* bt, const float* btlo,
                         int64_t Nc, int epi, const void* bias, const void* res, int64_t ldr, void* out) {
@@ -1103,6 +1115,7 @@ struct vit_weights_s {
     vit_layer w{};              // device pointers into mem; absent terms null
     void* qkv_bias = nullptr;   // (3 D) or null
     FoldTerms terms{};
+    float* tf32_wt = nullptr;   // fp32: the weights transposed with their low parts, or null
 };
 
 namespace vit {
@@ -1127,6 +1140,7 @@ BlockArgs prepared_args(const vit_weights* w, const void* x, int64_t N, int64_t 
     a.bias_scratch = w->qkv_bias;
     a.qkv_bias_ready = w->qkv_bias != nullptr;
     a.fold_terms = w->fold ? &w->terms : nullptr;
+    a.tf32_wt = w->tf32_wt;
     return a;
 }
 
@@ -1452,6 +1466,10 @@ int vit_weights_create(const vit_layer* layer, int from_host, int64_t D, int64_t
     if (use_fold && layer->ln1_g) total += round_up((size_t)(3 * D * D) * 2, 256);
     const size_t off_w1 = total;
     if (use_fold && layer->ln2_g) total += round_up((size_t)(D * F) * 2, 256);
+    // fp32 on the 3xTF32 tensor-core path: the weights transposed with their low parts
+    const bool prep_tf32 = dtype == DT_F32 && tf32_requested() && D % 4 == 0 && F % 4 == 0;
+    const size_t off_wt = total;
+    if (prep_tf32) total += tf32_weight_bytes(D, F);
     vit_weights* w = new (std::nothrow) vit_weights;
     if (!w) return VIT_ERR_NOMEM;
     w->device = st->info.device;
@@ -1483,6 +1501,15 @@ int vit_weights_create(const vit_layer* layer, int from_host, int64_t D, int64_t
         a.b_q = w->w.b_q; a.b_k = w->w.b_k; a.b_v = w->w.b_v;
         a.bias_scratch = w->qkv_bias;
         e = concat_qkv_bias(a, s);
+    }
+    if (e == cudaSuccess && prep_tf32) {
+        w->tf32_wt = reinterpret_cast<float*>(base + off_wt);
+        BlockArgs a{};
+        a.D = D; a.F = F;
+        a.w_q = w->w.w_q; a.w_k = w->w.w_k; a.w_v = w->w.w_v;
+        a.w_o = w->w.w_o; a.w1 = w->w.w_mlp1; a.w2 = w->w.w_mlp2;
+        const Tf32Weights tw = tf32_weight_layout(w->tf32_wt, D, F);
+        e = run(K_TF32_SPLIT, s, [&] { return tf32_split_weights(a, tw, s); });
     }
     if (e == cudaSuccess && use_fold) {
         float* cols = reinterpret_cast<float*>(base + off_cols);
