@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 
 namespace vit {
 namespace {
@@ -227,13 +228,9 @@ template <int DH>
 cudaError_t launch_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t D, cudaStream_t s) {
     constexpr int LDS = DH + 8;
     constexpr int smem = (BQ + 4 * BKV) * LDS * 2;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_mma_kernel<DH>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t e = set_smem_limit_once(attention_mma_kernel<DH>, smem, attr);
+    if (e != cudaSuccess) return e;
     const int64_t H = D / DH;
     dim3 grid((unsigned)((T + BQ - 1) / BQ), (unsigned)H, (unsigned)N);
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)DH);

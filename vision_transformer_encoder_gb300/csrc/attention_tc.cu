@@ -621,13 +621,9 @@ cudaError_t launch_tc_dh(const void* qkv, void* o, int64_t N, int64_t T, int64_t
     p.scale_log2 = 1.4426950408889634f / sqrtf((float)DH);
     p.o = static_cast<__nv_bfloat16*>(o);
     p.err = dev.err_word;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tc_kernel<DH, PT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t ae = set_smem_limit_once(attention_tc_kernel<DH, PT>, L::SMEM, attr);
+    if (ae != cudaSuccess) return ae;
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
     return launch_dependent(attention_tc_kernel<DH, PT>, dim3(grid), dim3(AT_THREADS), L::SMEM, s, tm, tm16, tmO,
                             tmO16, p);

@@ -537,13 +537,9 @@ cudaError_t launch_attention_tf32(const void* qkv, void* o, int64_t N, int64_t T
     p.o = static_cast<float*>(o);
     p.lo = o_lo != nullptr;
     p.err = dev.err_word;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_tf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             A3_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t ae = set_smem_limit_once(attention_tf32_kernel, A3_SMEM, attr);
+    if (ae != cudaSuccess) return ae;
     const int grid = p.units < dev.num_sms ? p.units : dev.num_sms;
     return launch_dependent(attention_tf32_kernel, dim3(grid), dim3(A3_THREADS), A3_SMEM, s, tq, tkv, to, tol, p);
 }

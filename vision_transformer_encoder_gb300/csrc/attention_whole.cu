@@ -648,13 +648,9 @@ cudaError_t launch_attention_whole(const void* qkv, void* o, int64_t N, int64_t 
     p.scale_log2 = 1.4426950408889634f / 8.0f;   // log2(e) / sqrt(64)
     p.o = static_cast<__nv_bfloat16*>(o);
     p.err = dev.err_word;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(attention_whole_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             AW_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t ae = set_smem_limit_once(attention_whole_kernel, AW_SMEM, attr);
+    if (ae != cudaSuccess) return ae;
     const int grid = p.items < dev.num_sms ? p.items : dev.num_sms;
     return launch_dependent(attention_whole_kernel, dim3(grid), dim3(AW_THREADS), AW_SMEM, s, tm, to, p);
 }

@@ -649,12 +649,9 @@ cudaError_t launch_inst_pair(const CUtensorMap& a, const CUtensorMap* b, const C
                              const CUtensorMap& out2, const CUtensorMap& res, const Params& p, int grid,
                              cudaStream_t s) {
     auto k = gemm_tc_pair_kernel<EPI, OutT, ResT, FOLD, EXTRA>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem_bytes<EPI, OutT, ResT>());
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t e = set_smem_limit_once(k, pair_smem_bytes<EPI, OutT, ResT>(), attr);
+    if (e != cudaSuccess) return e;
     return launch_dependent(k, dim3(grid), dim3(P_THREADS), pair_smem_bytes<EPI, OutT, ResT>(), s, a, b[0], b[1],
                             b[2], out, out2, res, p);
 }

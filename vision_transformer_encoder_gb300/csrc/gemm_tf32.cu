@@ -463,13 +463,9 @@ cudaError_t launch_gemm_tf32x3(const Tf32GemmDesc& d, const DeviceInfo& dev, cud
     p.ldo = d.ldo;
     p.lo = d.out_lo != nullptr;
     p.err = dev.err_word;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tf32x3_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             XP_SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr{0};
+    cudaError_t ae = set_smem_limit_once(gemm_tf32x3_pair_kernel, XP_SMEM, attr);
+    if (ae != cudaSuccess) return ae;
     const int64_t tiles = ((d.M + 2 * XM - 1) / (2 * XM)) * ((d.N + XP_ACC_COLS - 1) / XP_ACC_COLS);
     const int64_t pairs = dev.num_sms / 2;
     const int grid = 2 * (int)(tiles < pairs ? tiles : pairs);
