@@ -79,11 +79,12 @@ def kernel_work(c, f32=False):
     M = N * T
     if f32:
         return {
-            "ln1": ("hbm", M * D * (4 + 4), "bytes"),
+            # LayerNorms read fp32 rows and write xn and its low part (the next product's A_lo)
+            "ln1": ("hbm", M * D * (4 + 4 + 4), "bytes"),
             "qkv_gemm": ("tensor", 2 * M * D * 3 * D, "flops"),
             "attention": ("tensor" if D // c["H"] == 64 and T <= 224 else "alu", 4 * N * T * T * D, "flops"),
             "wo_gemm_residual": ("tensor", 2 * M * D * D, "flops"),
-            "ln2": ("hbm", M * D * (4 + 4), "bytes"),
+            "ln2": ("hbm", M * D * (4 + 4 + 4), "bytes"),
             "w1_gemm_gelu": ("tensor", 2 * M * D * F, "flops"),
             "w2_gemm_residual": ("tensor", 2 * M * F * D, "flops"),
             # weights read once, written twice (transposed high and low parts)

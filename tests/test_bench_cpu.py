@@ -33,9 +33,9 @@ def test_kernel_work_adds_up_to_the_step(f32):
     assert gemm == 2 * M * (4 * D * D + 2 * D * F)
     assert w["attention"][1] == 4 * N * T * T * D
     assert gemm + w["attention"][1] == bench.flops_per_step(c)
-    es = 4 if f32 else 2
-    assert w["ln1"] == ("hbm", M * D * (es + es), "bytes")   # read x, write xn
-    assert w["ln2"][1] == M * D * ((4 + 4) if f32 else (4 + 2))   # read fp32 y, write yn
+    # bf16: read x, write xn; fp32: read x, write xn and its low part (A_lo of the next product)
+    assert w["ln1"] == ("hbm", M * D * ((4 + 4 + 4) if f32 else (2 + 2)), "bytes")
+    assert w["ln2"][1] == M * D * ((4 + 4 + 4) if f32 else (4 + 2))   # read fp32 y
     assert w["attention"][0] == "tensor"   # head width 64, T <= 224: tensor cores on both paths
     for k in block_gemms:
         assert w[k][0] == "tensor"
