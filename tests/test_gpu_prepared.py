@@ -50,6 +50,8 @@ def _maxerr(gpu, ref):
     (torch.bfloat16, (8, 197, 768, 12, 3072), False),    # ViT-B/16 block shape
     (torch.bfloat16, (8, 197, 768, 12, 3072), True),
     (torch.float32, (4, 197, 192, 3, 768), True),        # ViT-Ti/16 block shape, fp32 path
+    (torch.float32, (6, 197, 768, 12, 3072), True),      # ViT-B/16 block shape, fp32: the handle's
+                                                         # prepared weight split on multi-tile products
 ])
 def test_plain_handle_equals_vit_block_ex(dtype, shape, affine):
     dev = _dev()
