@@ -175,3 +175,26 @@ def test_prepared_weights_argument_checks(lib):
     assert lib.vit_block_w_host_async(_fake(0), None, 2, 5, 1e-5, _fake(10), None) == -1
     assert lib.vit_weights_info(None, None, None, None, None, None, None) == -1
     assert lib.vit_weights_destroy(None) == 0
+
+
+def test_async_host_binding_checks_its_arguments(lib):
+    # the binding's own checks run before any call into the library (no GPU needed)
+    import torch
+
+    class _Handle:   # stands in for a VitWeights: only the fields the checks read
+        dtype, D, device, handle = torch.bfloat16, 8, 0, None
+
+    x = torch.zeros(2, 3, 8, dtype=torch.bfloat16)
+    out = torch.empty_like(x)
+    with pytest.raises(ValueError):
+        api.vit_block_w_host_async(x, _Handle(), 1e-6, None, 0)           # no output array
+    with pytest.raises(ValueError):
+        api.vit_block_w_host_async(x, _Handle(), 1e-6, out, None)         # no stream to order on
+    with pytest.raises(ValueError):
+        api.vit_block_w_host_async(x, _Handle(), 1e-6, out[:1], 0)        # out not shaped like x
+    with pytest.raises(ValueError):
+        api.vit_block_w_host_async(x.float(), _Handle(), 1e-6, out, 0)    # x not of the weights' dtype
+    w = _Handle()
+    w.D = 16
+    with pytest.raises(ValueError):
+        api.vit_block_w_host_async(x, w, 1e-6, out, 0)                    # width differs from the weights'
